@@ -1,0 +1,135 @@
+// Shared device/host helpers of libcsa2 (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstddef>
+#include <cmath>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// ------------------------------------------------------------------ host side
+// Records a one-line reason for the calling thread and returns `status`.
+int fail(int status, const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Device error word bits (OR-ed by kernels, read by csa2_last_device_status).
+enum : unsigned { ERR_BOUNDS = 1u, ERR_TIMEOUT = 2u };
+
+// Each translation unit that reports device errors owns one word and registers a
+// reader; csa2_last_device_status ORs all of them.
+using err_reader = unsigned (*)();
+void register_err_reader(err_reader f);
+
+// Entry positions visible to query position t (entry s covers tokens s*m..s*m+m-1).
+__host__ __device__ inline int n_visible(long long t, int m, int n_entries) {
+  long long v = (t + 1) / m;
+  if (v < 0) v = 0;
+  return int(v < n_entries ? v : n_entries);
+}
+
+// ------------------------------------------------------------------ device side
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(uint32_t(b) << 16);
+}
+
+// Order-preserving map float -> uint32 (larger float -> larger key); -0 == +0.
+__device__ __forceinline__ uint32_t f32_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// E2M1 magnitude of code & 7 (0, .5, 1, 1.5, 2, 3, 4, 6): exponent e = c >> 1, mantissa
+// bit c & 1; e == 0 is the subnormal 0.5 * m, otherwise 2^(e-1) * (1 + m/2).
+__device__ __forceinline__ float e2m1_mag(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  return e == 0 ? 0.5f * float(m) : __uint_as_float(((e + 126u) << 23) | (m << 22));
+}
+
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const float v = e2m1_mag(c);
+  return (c & 8u) ? -v : v;
+}
+
+// E4M3 (OCP FN) byte -> float: bias 7, subnormals m * 2^-9.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
+  float v = (e == 0) ? float(m) * 0.001953125f
+                     : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  return (b & 0x80u) ? -v : v;
+}
+
+// float32 >= 0 -> E4M3 byte, round to nearest even, saturating at 448.
+// Subnormal range (x < 2^-6): m * 2^-9 with m = rint(x * 512).  Normal range: round
+// the 23-bit mantissa to 3 bits (a carry moves into the exponent), re-bias 127 -> 7.
+__device__ __forceinline__ uint32_t e4m3_rne_satfinite(float x) {
+  if (!(x < 448.0f)) return 0x7Eu;
+  if (x < 0.015625f) return uint32_t(rintf(x * 512.0f));
+  const uint32_t b = __float_as_uint(x);
+  uint32_t q = b >> 20;
+  const uint32_t rem = b & 0xFFFFFu;
+  if (rem > 0x80000u || (rem == 0x80000u && (q & 1u))) ++q;
+  const uint32_t code = q - (120u << 3);
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// |u| -> E2M1 magnitude code, nearest with ties to the even code, saturating at 6.
+__device__ __forceinline__ uint32_t e2m1_rne_mag(float a) {
+  if (a <= 0.25f) return 0u;
+  if (a < 0.75f) return 1u;
+  if (a <= 1.25f) return 2u;
+  if (a < 1.75f) return 3u;
+  if (a <= 2.5f) return 4u;
+  if (a < 3.5f) return 5u;
+  if (a <= 5.0f) return 6u;
+  return 7u;
+}
+
+// One 32-value block held one value per lane of a full warp: returns this lane's
+// 4-bit code and (same on all lanes) the E4M3 scale byte.
+__device__ __forceinline__ uint32_t fp4_quant_lane(float v, uint32_t& scale_byte) {
+  float a = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const uint32_t sb = e4m3_rne_satfinite(__fdiv_rn(a, 6.0f));
+  scale_byte = sb;
+  if (sb == 0u) return 0u;
+  const float s = e4m3_value(sb);
+  const float u = __fdiv_rn(v, s);
+  const uint32_t sign = (__float_as_uint(u) >> 31) << 3;
+  return sign | e2m1_rne_mag(fabsf(u));
+}
+
+// RoPE angle cos/sin for position pos and pair i (of 32), computed in double.
+__device__ __forceinline__ void rope_cs(long long pos, int i, float rope_base, float& c,
+                                        float& s) {
+  const double th = pow(double(rope_base), -double(i) / 32.0);
+  double sd, cd;
+  sincos(double(pos) * th, &sd, &cd);
+  c = float(cd);
+  s = float(sd);
+}
+
+}  // namespace csa2
+
+// Defines a translation-unit-local device error word `name` plus a reader that
+// returns and clears it, registered with csa2_last_device_status.
+#define CSA2_DEFINE_ERR_WORD(name)                                                  \
+  static __device__ unsigned name;                                                  \
+  static unsigned name##_read() {                                                   \
+    unsigned v = 0, z = 0;                                                          \
+    if (cudaMemcpyFromSymbol(&v, name, sizeof(v)) != cudaSuccess) return 0;         \
+    cudaMemcpyToSymbol(name, &z, sizeof(z));                                        \
+    return v;                                                                       \
+  }                                                                                 \
+  static const int name##_registered = (csa2::register_err_reader(&name##_read), 0);

@@ -1,0 +1,279 @@
+// Stage 1 (compressor) and stage 2 (indexer key + FP4) of the CSA2 hot path.
+//
+// [P1] "DeepSeek-V4.1 模型结构（2）：序列维度（中），CSA2 的三种模式" (blog.javazero.top):
+//      §压缩算子去掉了重叠和位置偏置 -- disjoint groups of m tokens, per-channel softmax
+//      pooling, no position bias, m = 1 without a gate, RMSNorm, RoPE on the last 64
+//      dims at the group's first token; §indexer K 改由 main KV 投影 -- indexer key
+//      projected 512 -> 128 from the entry before RoPE, its own RoPE on the last 64
+//      dims, no Hadamard, FP4 with one scale per 32 dims.
+// [P2] "DeepSeek v4.1 Flash技术剖析——架构篇" (myhz0606.com) §Compressor.
+//
+// Kernels
+//   proj_gemm_kernel   P[M, Nout] = X[M, K] . [W_kv; W_gate]^T (bf16 in, fp32 accumulate)
+//   compress_epilogue  per entry: softmax-pool over the group, RMSNorm, RoPE, stores
+//   index_k_kernel     per entry: 512 -> 128 projection, RoPE, FP4 quantisation
+#include "common.cuh"
+
+CSA2_DEFINE_ERR_WORD(d_err_compress)
+
+namespace csa2 {
+namespace {
+
+constexpr int GM = 128, GN = 128, GK = 32, GT = 256;
+
+// Register-tiled SIMT GEMM.  Each of 256 threads owns an 8x8 sub-tile with rows
+// ty + 16 i and columns tx + 16 j; tiles staged in shared memory as float32, K-major.
+__global__ void __launch_bounds__(GT) proj_gemm_kernel(const uint16_t* __restrict__ X,
+                                                       const uint16_t* __restrict__ W0,
+                                                       const uint16_t* __restrict__ W1, int M,
+                                                       int K, int Nout, float* __restrict__ P) {
+  __shared__ float As[GK][GM + 4];
+  __shared__ float Bs[GK][GN + 4];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.y * GM, n0 = blockIdx.x * GN;
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  for (int k0 = 0; k0 < K; k0 += GK) {
+    // 128 rows x 32 k = 512 chunks of 8 bf16; 2 chunks per thread for A and for B
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int chunk = tid + c * GT, r = chunk >> 2, kc = (chunk & 3) * 8;
+      uint4 va = make_uint4(0, 0, 0, 0);
+      if (m0 + r < M) va = *reinterpret_cast<const uint4*>(X + size_t(m0 + r) * K + k0 + kc);
+      const int n = n0 + r;
+      const uint16_t* wrow = (n < 512) ? (W0 + size_t(n) * K) : (W1 + size_t(n - 512) * K);
+      uint4 vb = *reinterpret_cast<const uint4*>(wrow + k0 + kc);
+      const uint16_t* pa = reinterpret_cast<const uint16_t*>(&va);
+      const uint16_t* pb = reinterpret_cast<const uint16_t*>(&vb);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        As[kc + u][r] = bf16_to_f32(pa[u]);
+        Bs[kc + u][r] = bf16_to_f32(pb[u]);
+      }
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < GK; ++kk) {
+      float a[8], b[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = m0 + ty + 16 * i;
+    if (r >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) P[size_t(r) * Nout + n0 + tx + 16 * j] = acc[i][j];
+  }
+}
+
+// One block of 128 threads per entry (b, g); thread owns channels 4t..4t+3.
+__global__ void __launch_bounds__(128) compress_epilogue_kernel(
+    const float* __restrict__ P, int Nout, int B, int T, int m, int pos0, int G,
+    const float* __restrict__ norm_w, float eps, float rope_base, uint16_t* __restrict__ kv_cache,
+    int n_cap, float* __restrict__ kv_pre) {
+  const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x;
+  const size_t row0 = size_t(b) * T + size_t(g) * m;
+  float pooled[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = 4 * t + u;
+    if (m == 1) {
+      pooled[u] = P[row0 * Nout + c];
+    } else {
+      float mx = -INFINITY;
+      for (int i = 0; i < m; ++i) mx = fmaxf(mx, P[(row0 + i) * Nout + 512 + c]);
+      float num = 0.f, den = 0.f;
+      for (int i = 0; i < m; ++i) {
+        const float w = expf(P[(row0 + i) * Nout + 512 + c] - mx);
+        den += w;
+        num = fmaf(w, P[(row0 + i) * Nout + c], num);
+      }
+      pooled[u] = num / den;
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) ss = fmaf(pooled[u], pooled[u], ss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  __shared__ float red[4];
+  if ((t & 31) == 0) red[t >> 5] = ss;
+  __syncthreads();
+  const float tot = (red[0] + red[1]) + (red[2] + red[3]);
+  const float inv = 1.0f / sqrtf(tot / 512.0f + eps);
+  float y[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) y[u] = norm_w[4 * t + u] * (pooled[u] * inv);
+  if (kv_pre) {
+    float4 v = make_float4(y[0], y[1], y[2], y[3]);
+    *reinterpret_cast<float4*>(kv_pre + size_t(e) * 512 + 4 * t) = v;
+  }
+  if (4 * t >= 448) {
+    const long long pos = (long long)pos0 + (long long)g * m;
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const int i = (4 * t - 448) / 2 + pr;
+      float c, s;
+      rope_cs(pos, i, rope_base, c, s);
+      const float a = y[2 * pr], bb = y[2 * pr + 1];
+      y[2 * pr] = a * c - bb * s;
+      y[2 * pr + 1] = a * s + bb * c;
+    }
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
+  uint2 st;
+  st.x = *reinterpret_cast<uint32_t*>(&lo);
+  st.y = *reinterpret_cast<uint32_t*>(&hi);
+  const size_t crow = size_t(b) * n_cap + size_t(pos0 / m) + g;
+  *reinterpret_cast<uint2*>(kv_cache + crow * 512 + 4 * t) = st;
+}
+
+constexpr int IK_E = 8;  // entries per block
+
+// 128 threads: thread j computes key dim j for IK_E entries; warp w then quantises
+// block w (dims 32w..32w+31) of each entry.
+__global__ void __launch_bounds__(128) index_k_kernel(const float* __restrict__ kv_pre, int B,
+                                                      int G, int entry0, int m,
+                                                      const uint16_t* __restrict__ w_ik,
+                                                      float rope_base, uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales, int n_cap,
+                                                      float* __restrict__ k_out) {
+  __shared__ float kv[IK_E][512];
+  const int j = threadIdx.x, lane = j & 31, w = j >> 5;
+  const int total = B * G;
+  const int e0 = blockIdx.x * IK_E;
+  for (int idx = j; idx < IK_E * 512; idx += 128) {
+    const int e = e0 + idx / 512;
+    kv[idx / 512][idx % 512] = (e < total) ? kv_pre[size_t(e) * 512 + idx % 512] : 0.f;
+  }
+  __syncthreads();
+  float acc[IK_E];
+#pragma unroll
+  for (int e = 0; e < IK_E; ++e) acc[e] = 0.f;
+  const uint16_t* wr = w_ik + size_t(j) * 512;
+  for (int h = 0; h < 512; h += 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(wr + h);
+    const uint16_t* pv = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wv = bf16_to_f32(pv[u]);
+#pragma unroll
+      for (int e = 0; e < IK_E; ++e) acc[e] = fmaf(wv, kv[e][h + u], acc[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < IK_E; ++e) {
+    const int ei = e0 + e;
+    if (ei >= total) break;  // uniform across the block
+    const int b = ei / G, g = ei % G;
+    const long long ent = (long long)entry0 + g;
+    float v = acc[e];
+    const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+    if (j >= 64) {
+      float c, s;
+      rope_cs(ent * m, (j - 64) >> 1, rope_base, c, s);
+      v = (j & 1) ? (partner * s + v * c) : (v * c - partner * s);
+    }
+    if (k_out) k_out[size_t(ei) * 128 + j] = v;
+    uint32_t sb;
+    const uint32_t code = fp4_quant_lane(v, sb);
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+    const size_t crow = size_t(b) * n_cap + size_t(ent);
+    if ((lane & 1) == 0) codes[crow * 64 + (j >> 1)] = uint8_t(code | (hi << 4));
+    if (lane == 0) scales[crow * 4 + w] = uint8_t(sb);
+  }
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+size_t csa2_compress_workspace_size(int B, int T, int hidden, int m) {
+  (void)hidden;
+  if (B <= 0 || T <= 0 || (m != 1 && m != 2)) return 0;
+  const int nout = (m == 1) ? 512 : 1024;
+  return align_up(size_t(B) * T * nout * sizeof(float), 256);
+}
+
+int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, const void* w_kv,
+                  const void* w_gate, const float* norm_w, float eps, float rope_base,
+                  void* kv_cache, int n_cap, float* kv_pre, void* workspace, size_t ws_bytes,
+                  void* stream) {
+  if (m != 1 && m != 2) return fail(CSA2_ERR_UNSUPPORTED, "compress: m must be 1 or 2 (got %d)", m);
+  if (!x || !w_kv || !norm_w || !kv_cache)
+    return fail(CSA2_ERR_INVALID_ARG, "compress: null tensor pointer");
+  if ((m == 1) != (w_gate == nullptr))
+    return fail(CSA2_ERR_INVALID_ARG, "compress: w_gate must be NULL exactly when m == 1");
+  if (B <= 0 || T <= 0 || hidden <= 0 || hidden % 64 != 0)
+    return fail(CSA2_ERR_INVALID_ARG, "compress: bad shape B=%d T=%d hidden=%d", B, T, hidden);
+  if (pos0 < 0 || pos0 % m != 0)
+    return fail(CSA2_ERR_INVALID_ARG, "compress: pos0=%d must be >= 0 and a multiple of m", pos0);
+  const int G = T / m;
+  if (n_cap <= 0 || (long long)pos0 / m + G > n_cap)
+    return fail(CSA2_ERR_INVALID_ARG, "compress: entries %d..%d exceed n_cap=%d", pos0 / m,
+                pos0 / m + G - 1, n_cap);
+  if (!(eps >= 0.f) || !(rope_base > 0.f))
+    return fail(CSA2_ERR_INVALID_ARG, "compress: bad eps / rope_base");
+  if (!aligned16(x) || !aligned16(w_kv) || (w_gate && !aligned16(w_gate)) || !aligned16(norm_w) ||
+      !aligned16(kv_cache) || (kv_pre && !aligned16(kv_pre)))
+    return fail(CSA2_ERR_INVALID_ARG, "compress: pointers must be 16-byte aligned");
+  if ((long long)B * T > (1ll << 30))
+    return fail(CSA2_ERR_UNSUPPORTED, "compress: B*T too large for one call");
+  const size_t need = csa2_compress_workspace_size(B, T, hidden, m);
+  if (!workspace || ws_bytes < need || !aligned256(workspace))
+    return fail(CSA2_ERR_WORKSPACE, "compress: workspace needs %zu bytes, 256-aligned", need);
+  if (G == 0) return CSA2_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int M = B * T, nout = (m == 1) ? 512 : 1024;
+  float* P = static_cast<float*>(workspace);
+  dim3 grid(nout / GN, ceil_div(M, GM));
+  proj_gemm_kernel<<<grid, GT, 0, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
+                                        (const uint16_t*)w_gate, M, hidden, nout, P);
+  compress_epilogue_kernel<<<B * G, 128, 0, st>>>(P, nout, B, T, m, pos0, G, norm_w, eps,
+                                                   rope_base, (uint16_t*)kv_cache, n_cap, kv_pre);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "compress launch");
+  return CSA2_OK;
+}
+
+int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, const void* w_ik,
+                       float rope_base, uint8_t* codes, uint8_t* scales, int n_cap, float* k_out,
+                       void* stream) {
+  if (!kv_pre || !w_ik || !codes || !scales)
+    return fail(CSA2_ERR_INVALID_ARG, "index_k_quant: null tensor pointer");
+  if (B <= 0 || G < 0 || entry0 < 0 || m < 1 || n_cap <= 0 || (long long)entry0 + G > n_cap)
+    return fail(CSA2_ERR_INVALID_ARG, "index_k_quant: bad shape B=%d G=%d entry0=%d n_cap=%d", B,
+                G, entry0, n_cap);
+  if (!(rope_base > 0.f)) return fail(CSA2_ERR_INVALID_ARG, "index_k_quant: bad rope_base");
+  if (!aligned16(kv_pre) || !aligned16(w_ik) || !aligned16(codes) || !aligned16(scales) ||
+      (k_out && !aligned16(k_out)))
+    return fail(CSA2_ERR_INVALID_ARG, "index_k_quant: pointers must be 16-byte aligned");
+  if ((long long)B * G > (1ll << 31) - IK_E)
+    return fail(CSA2_ERR_UNSUPPORTED, "index_k_quant: too many entries for one call");
+  if (G == 0) return CSA2_OK;
+  const int total = B * G;
+  index_k_kernel<<<ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream>>>(
+      kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "index_k_quant launch");
+  return CSA2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,289 @@
+// Stage 3: lightning-indexer scores, causal top-k, HSI candidate pools.
+//
+// [P1] "DeepSeek-V4.1 模型结构（2）：序列维度（中），CSA2 的三种模式" (blog.javazero.top),
+//      §indexer K 改由 main KV 投影: score of entry s for token t is the sum over the 32
+//      indexer heads of the head weight times ReLU(q_{t,j} . k_s), 128 dims per head;
+//      512 entries are kept per query.
+// [P2] "DeepSeek v4.1 Flash技术剖析——架构篇" (myhz0606.com), §Indexer (causally visible
+//      set), §CSA2-ReIndex (block max scores, top blocks form the pool, the newest
+//      visible block is forced in, non-pool entries scored -inf).
+// [P3] "DeepSeek-V4.1-Flash：把百万 Token 的记忆，压缩成一套分级缓存" (junki.cn), §五 HSI.
+//
+// Kernels
+//   score_kernel   one CTA per (query row, chunk of 1024 entries or pool slots): the CTA
+//                  quantises its query to FP4 (same rule as the keys), then each thread
+//                  scores one entry per pass: 32 heads x 4 blocks of 32 dims; the block
+//                  partial sums are exact in float32 and are scaled once by the key scale.
+//   topk_kernel    one CTA per query row: radix select (select.cuh).
+//   hsi_kernel     one CTA per query row: top-nb blocks with the newest block forced.
+#include "common.cuh"
+#include "select.cuh"
+
+CSA2_DEFINE_ERR_WORD(d_err_indexer)
+
+namespace csa2 {
+namespace {
+
+constexpr int SC_T = 256;       // threads per scoring CTA
+constexpr int SC_CHUNK = 1024;  // entries (or pool slots) per scoring CTA
+
+struct ScoreArgs {
+  const uint16_t* q_idx;   // [rows, 32, 128]
+  const float* w;          // [rows, 32]
+  int rows, Tq, q_pos0;
+  const uint8_t* codes;    // [B, n_cap, 64]
+  const uint8_t* scales;   // [B, n_cap, 4]
+  int n_cap, n_entries, m;
+  const int32_t* cand;     // [rows, nb] or null
+  int nb, blk, n_blocks;   // n_blocks = ceil(n_entries / blk)
+  float* scores;           // [rows, row_len]
+  int row_len;
+  float* blockmax;         // [rows, n_blocks] or null
+  int n_chunks;
+};
+
+__global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
+  __shared__ __align__(16) float qh[32][128];
+  __shared__ float wsh[32];
+  __shared__ float sbuf[SC_T];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x / a.n_chunks, chunk = blockIdx.x % a.n_chunks;
+  const int b = row / a.Tq, i = row % a.Tq;
+  const long long t = (long long)a.q_pos0 + i;
+  const int n_vis = n_visible(t, a.m, a.n_entries);
+  const int c0 = chunk * SC_CHUNK;
+  const bool pool = a.cand != nullptr;
+  const int limit = pool ? a.row_len : n_vis;
+  if (c0 >= limit && a.blockmax == nullptr) return;   // uniform
+
+  // FP4-quantise the query: warp w handles 16 (head, block) pairs, lane = element
+  const uint16_t* qrow = a.q_idx + size_t(row) * 32 * 128;
+  for (int pb = warp; pb < 128; pb += SC_T / 32) {
+    const int h = pb >> 2, blk4 = pb & 3;
+    const float v = bf16_to_f32(qrow[h * 128 + blk4 * 32 + lane]);
+    uint32_t sb;
+    const uint32_t code = fp4_quant_lane(v, sb);
+    qh[h][blk4 * 32 + lane] = e2m1_value(code) * e4m3_value(sb);
+  }
+  if (tid < 32) wsh[tid] = a.w[size_t(row) * 32 + tid];
+  __syncthreads();
+
+  const size_t cache_row0 = size_t(b) * a.n_cap;
+  for (int it = 0; it < SC_CHUNK / SC_T; ++it) {
+    const int p = c0 + it * SC_T + tid;
+    float score = -INFINITY;
+    long long e = -1;
+    if (p < limit) {
+      if (pool) {
+        const int cb = a.cand[size_t(row) * a.nb + p / a.blk];
+        if (cb >= 0) {
+          if (cb >= a.n_blocks) {
+            atomicOr(&d_err_indexer, ERR_BOUNDS);
+          } else {
+            const long long ee = (long long)cb * a.blk + (p % a.blk);
+            if (ee < n_vis) e = ee;
+          }
+        }
+      } else {
+        e = p;
+      }
+    }
+    if (e >= 0) {
+      const uint8_t* crow = a.codes + (cache_row0 + size_t(e)) * 64;
+      const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(a.scales + (cache_row0 + size_t(e)) * 4);
+      float d[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) d[j] = 0.f;
+#pragma unroll 1
+      for (int kb = 0; kb < 4; ++kb) {
+        const uint4 cv = *reinterpret_cast<const uint4*>(crow + kb * 16);
+        const uint32_t wds[4] = {cv.x, cv.y, cv.z, cv.w};
+        float kv[32];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int nn = 0; nn < 8; ++nn) kv[u * 8 + nn] = e2m1_value((wds[u] >> (4 * nn)) & 0xFu);
+        const float sk = e4m3_value((sc4 >> (8 * kb)) & 0xFFu);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float4* qv = reinterpret_cast<const float4*>(&qh[j][kb * 32]);
+          float part = 0.f;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 q4 = qv[u];
+            part = fmaf(q4.x, kv[4 * u + 0], part);
+            part = fmaf(q4.y, kv[4 * u + 1], part);
+            part = fmaf(q4.z, kv[4 * u + 2], part);
+            part = fmaf(q4.w, kv[4 * u + 3], part);
+          }
+          d[j] = fmaf(part, sk, d[j]);
+        }
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) s = fmaf(wsh[j], fmaxf(d[j], 0.f), s);
+      score = s;
+    }
+    if (p < a.row_len && (pool || p < n_vis)) a.scores[size_t(row) * a.row_len + p] = score;
+    if (a.blockmax) {
+      sbuf[tid] = score;
+      __syncthreads();
+      const int per = SC_T / a.blk;   // blocks in this pass (blk <= 256, power of two)
+      if (tid < per) {
+        float mx = -INFINITY;
+        for (int u = 0; u < a.blk; ++u) mx = fmaxf(mx, sbuf[tid * a.blk + u]);
+        const int bi = (c0 + it * SC_T) / a.blk + tid;
+        if (bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = mx;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+constexpr int TK_T = 512;
+constexpr int TK_SMEM_KEYS = 11264;   // rows up to this length are staged in shared memory
+
+struct TopkArgs {
+  const float* scores;
+  int row_len, Tq, q_pos0, m, n_entries;
+  const int32_t* cand;   // pool mode
+  int nb, blk, k;
+  int32_t* out;
+};
+
+__global__ void __launch_bounds__(TK_T) topk_kernel(TopkArgs a) {
+  extern __shared__ unsigned keys_sm[];
+  __shared__ SelectSmem sm;
+  const int row = blockIdx.x, i = row % a.Tq;
+  const long long t = (long long)a.q_pos0 + i;
+  const bool pool = a.cand != nullptr;
+  const int n = pool ? a.row_len : n_visible(t, a.m, a.n_entries);
+  const float* srow = a.scores + size_t(row) * a.row_len;
+  const bool staged = n <= TK_SMEM_KEYS;
+  if (staged) {
+    for (int j = threadIdx.x; j < n; j += TK_T) {
+      const float f = srow[j];
+      keys_sm[j] = (f == -INFINITY) ? 0u : f32_key(f);
+    }
+    __syncthreads();
+  }
+  auto key_of = [&](int j) -> unsigned {
+    if (staged) return keys_sm[j];
+    const float f = srow[j];
+    return (f == -INFINITY) ? 0u : f32_key(f);
+  };
+  int32_t* orow = a.out + size_t(row) * a.k;
+  const int32_t* crow = pool ? a.cand + size_t(row) * a.nb : nullptr;
+  auto emit = [&](int pos, int j) {
+    int32_t v = -1;
+    if (j >= 0) v = pool ? crow[j / a.blk] * a.blk + (j % a.blk) : j;
+    orow[pos] = v;
+  };
+  radix_topk<TK_T>(n, a.k, key_of, emit, sm);
+}
+
+struct HsiArgs {
+  const float* blockmax;
+  int n_blocks, Tq, q_pos0, m, n_entries, blk, nb;
+  int32_t* out;
+};
+
+__global__ void __launch_bounds__(TK_T) hsi_kernel(HsiArgs a) {
+  __shared__ SelectSmem sm;
+  const int row = blockIdx.x, i = row % a.Tq;
+  const long long t = (long long)a.q_pos0 + i;
+  const int n_vis = n_visible(t, a.m, a.n_entries);
+  const int nb_vis = (n_vis + a.blk - 1) / a.blk;
+  const int forced = n_vis > 0 ? (n_vis - 1) / a.blk : -1;
+  const float* brow = a.blockmax + size_t(row) * a.n_blocks;
+  auto key_of = [&](int j) -> unsigned {
+    if (j == forced) return 0xFFFFFFFFu;
+    const float f = brow[j];
+    return (f == -INFINITY) ? 0u : f32_key(f);
+  };
+  int32_t* orow = a.out + size_t(row) * a.nb;
+  auto emit = [&](int pos, int j) { orow[pos] = j; };
+  radix_topk<TK_T>(nb_vis, a.nb, key_of, emit, sm);
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+size_t csa2_indexer_workspace_size(int B, int Tq, int n_entries, int nb, int blk, int with_cand) {
+  if (B <= 0 || Tq <= 0) return 0;
+  const long long row_len = with_cand ? (long long)nb * blk : n_entries;
+  if (row_len <= 0) return 0;
+  return align_up(size_t(B) * Tq * size_t(row_len) * sizeof(float), 256);
+}
+
+int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
+                            const uint8_t* codes, const uint8_t* scales, int n_cap, int n_entries,
+                            int m, const int32_t* cand, int nb, int blk, int k, int32_t* topk_out,
+                            float* blockmax_out, float* scores_out, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  if (!q_idx || !w || !codes || !scales || !topk_out)
+    return fail(CSA2_ERR_INVALID_ARG, "indexer: null tensor pointer");
+  if (B <= 0 || Tq <= 0 || q_pos0 < 0 || m < 1 || n_entries < 0 || n_cap < n_entries ||
+      n_cap <= 0)
+    return fail(CSA2_ERR_INVALID_ARG, "indexer: bad shape B=%d Tq=%d q_pos0=%d m=%d N=%d n_cap=%d",
+                B, Tq, q_pos0, m, n_entries, n_cap);
+  if (k < 1 || k > CSA2_MAX_TOPK) return fail(CSA2_ERR_INVALID_ARG, "indexer: k=%d out of [1, 2048]", k);
+  if (cand && blockmax_out)
+    return fail(CSA2_ERR_INVALID_ARG, "indexer: blockmax is produced by Full (cand == NULL) calls only");
+  if ((cand || blockmax_out) && (!is_pow2(blk) || blk > 256))
+    return fail(CSA2_ERR_UNSUPPORTED, "indexer: blk=%d must be a power of two <= 256", blk);
+  if (cand && (nb < 1 || nb > CSA2_MAX_TOPK))
+    return fail(CSA2_ERR_INVALID_ARG, "indexer: nb=%d out of [1, 2048]", nb);
+  if (!aligned16(q_idx) || !aligned16(w) || !aligned16(codes) || !aligned16(scales) ||
+      !aligned16(topk_out) || (cand && !aligned16(cand)) ||
+      (blockmax_out && !aligned16(blockmax_out)) || (scores_out && !aligned16(scores_out)))
+    return fail(CSA2_ERR_INVALID_ARG, "indexer: pointers must be 16-byte aligned");
+  const long long rows = (long long)B * Tq;
+  const long long row_len = cand ? (long long)nb * blk : n_entries;
+  if (rows * ((row_len + SC_CHUNK - 1) / SC_CHUNK) > (1ll << 31) - 1 || row_len > (1ll << 30))
+    return fail(CSA2_ERR_UNSUPPORTED, "indexer: problem too large for one call");
+  float* scores = scores_out;
+  if (!scores) {
+    const size_t need = csa2_indexer_workspace_size(B, Tq, n_entries, nb, blk, cand != nullptr);
+    if (need && (!workspace || ws_bytes < need || !aligned256(workspace)))
+      return fail(CSA2_ERR_WORKSPACE, "indexer: workspace needs %zu bytes, 256-aligned", need);
+    scores = static_cast<float*>(workspace);
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  const int n_blocks = (cand || blockmax_out) ? ceil_div(n_entries, blk) : 0;
+  if (row_len > 0) {
+    ScoreArgs sa{(const uint16_t*)q_idx, w, int(rows), Tq, q_pos0, codes, scales, n_cap,
+                 n_entries, m, cand, nb, blk, n_blocks, scores, int(row_len), blockmax_out,
+                 int((row_len + SC_CHUNK - 1) / SC_CHUNK)};
+    score_kernel<<<unsigned(rows * sa.n_chunks), SC_T, 0, st>>>(sa);
+  }
+  TopkArgs ta{scores, int(row_len), Tq, q_pos0, m, n_entries, cand, nb, blk, k, topk_out};
+  const int staged = int(row_len < TK_SMEM_KEYS ? row_len : TK_SMEM_KEYS);
+  topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+  return CSA2_OK;
+}
+
+int csa2_hsi_candidates(const float* blockmax, int B, int Tq, int q_pos0, int n_entries, int m,
+                        int blk, int nb, int32_t* cand_out, void* stream) {
+  if (!blockmax || !cand_out) return fail(CSA2_ERR_INVALID_ARG, "hsi: null tensor pointer");
+  if (B <= 0 || Tq <= 0 || q_pos0 < 0 || m < 1 || n_entries < 0 || blk < 1)
+    return fail(CSA2_ERR_INVALID_ARG, "hsi: bad shape");
+  if (nb < 1 || nb > CSA2_MAX_TOPK) return fail(CSA2_ERR_INVALID_ARG, "hsi: nb=%d out of [1, 2048]", nb);
+  if (!aligned16(blockmax) || !aligned16(cand_out))
+    return fail(CSA2_ERR_INVALID_ARG, "hsi: pointers must be 16-byte aligned");
+  const long long rows = (long long)B * Tq;
+  if (rows > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "hsi: too many rows");
+  HsiArgs ha{blockmax, ceil_div(n_entries, blk), Tq, q_pos0, m, n_entries, blk, nb, cand_out};
+  hsi_kernel<<<unsigned(rows), TK_T, 0, (cudaStream_t)stream>>>(ha);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "hsi launch");
+  return CSA2_OK;
+}
+
+}  // extern "C"

@@ -100,7 +100,8 @@ def run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k, hsi_blk=64, hsi_n
                 prev_scales [B,n0,4] with n0 = x_pos0 // m
       Full / Reindex: q_idx [B,Tq,32,128], w_idx [B,Tq,32]
     Returns (outs, trace): outs[l] = [B,Tq,H,512] float64; trace[l] holds the
-    layer's top-k [B,Tq,k] (and candidates for a Full layer that builds a pool).
+    layer's top-k [B,Tq,k], its scores / competing masks per (b, i), and candidates for
+    a Full layer that builds a pool.
     """
     modes = layer_modes(kv_src, idx_src)
     builds_pool = {l: use_hsi and any(modes[r] == REINDEX and kv_src[r] == l
@@ -134,6 +135,7 @@ def run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k, hsi_blk=64, hsi_n
             N = kv_all.shape[1]
             k_hat = R.fp4.dequantize_rows(codes_all, scales_all)          # [B, N, 128]
             topk_out = np.full((B, Tq, k), -1, dtype=np.int32)
+            tr["scores"], tr["valid"] = {}, {}
             cand_out = None
             if md == FULL and builds_pool[l]:
                 cand_out = np.full((B, Tq, hsi_nb), -1, dtype=np.int32)
@@ -147,6 +149,7 @@ def run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k, hsi_blk=64, hsi_n
                     if md == REINDEX and use_hsi:
                         valid = R.pool_mask(slots["candidates"][b, i], nv, hsi_blk, nv)
                     topk_out[b, i] = R.topk(sc, valid, k)
+                    tr["scores"][b, i], tr["valid"][b, i] = sc, valid
                     if cand_out is not None:
                         bm = R.block_max(sc, nv, hsi_blk)
                         cand_out[b, i] = R.hsi_candidates(bm, nv, hsi_blk, hsi_nb)

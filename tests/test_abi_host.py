@@ -1,0 +1,147 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and
+rejects bad calls on the host before any launch (no compute call is made)."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import compressed_sparse_attention_04_gb300._lib as L
+from compressed_sparse_attention_04_gb300 import build as B
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build_all()
+    return L.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(csa2_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported_and_bound(lib):
+    names = _declared_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in L.SIGNATURES, f"{n} has no ctypes signature"
+    assert set(L.SIGNATURES) == set(names)
+
+
+def test_struct_layouts_match_header():
+    # csa2_layer_io: 16 pointers + 6 ints; csa2_step_params: 8 ints + 4 floats
+    assert C.sizeof(L.LayerIO) == 16 * 8 + 6 * 4
+    assert C.sizeof(L.StepParams) == 12 * 4
+
+
+def test_status_strings(lib):
+    assert lib.csa2_status_str(0) == b"CSA2_OK"
+    assert lib.csa2_status_str(3) == b"CSA2_ERR_WORKSPACE"
+    assert lib.csa2_version().startswith(b"csa2")
+
+
+def _vp(x):
+    return C.c_void_p(x)
+
+
+FAKE = 0x10000   # never dereferenced: every call below fails validation first
+
+
+def test_compress_validation(lib):
+    f = lib.csa2_compress
+    args = dict(x=_vp(FAKE), B=2, T=8, hidden=128, m=2, pos0=0, w_kv=_vp(FAKE), w_gate=_vp(FAKE),
+                norm_w=_vp(FAKE), eps=1e-6, base=1e4, kv=_vp(FAKE), n_cap=4, kv_pre=_vp(FAKE),
+                ws=_vp(FAKE), wsb=0, st=_vp(0))
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(*a.values())
+
+    assert call(m=3) == L.ERR_UNSUPPORTED
+    assert call(x=_vp(0)) == L.ERR_INVALID_ARG
+    assert call(w_gate=_vp(0)) == L.ERR_INVALID_ARG          # m = 2 needs a gate
+    assert call(m=1) == L.ERR_INVALID_ARG                    # m = 1 must not have one
+    assert call(hidden=100) == L.ERR_INVALID_ARG
+    assert call(pos0=1) == L.ERR_INVALID_ARG
+    assert call(n_cap=3) == L.ERR_INVALID_ARG                # 4 entries do not fit
+    assert call(x=_vp(FAKE + 4)) == L.ERR_INVALID_ARG        # misaligned
+    assert call() == L.ERR_WORKSPACE                         # workspace too small
+    assert b"workspace" in lib.csa2_last_error_message()
+
+
+def test_indexer_and_hsi_validation(lib):
+    f = lib.csa2_indexer_score_topk
+    base = [_vp(FAKE), _vp(FAKE), 1, 1, 10, _vp(FAKE), _vp(FAKE), 64, 32, 1, _vp(0), 0, 64, 16,
+            _vp(FAKE), _vp(0), _vp(0), _vp(0), 0, _vp(0)]
+
+    def call(**over):
+        a = list(base)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a13=0) == L.ERR_INVALID_ARG                  # k = 0
+    assert call(a13=4096) == L.ERR_INVALID_ARG               # k > 2048
+    assert call(a7=16) == L.ERR_INVALID_ARG                  # n_cap < n_entries
+    assert call(a10=_vp(FAKE), a11=4, a12=48) == L.ERR_UNSUPPORTED   # blk not a power of 2
+    assert call(a10=_vp(FAKE), a11=0) == L.ERR_INVALID_ARG   # nb = 0
+    assert call(a10=_vp(FAKE), a11=4, a15=_vp(FAKE)) == L.ERR_INVALID_ARG  # pool + blockmax
+    assert call() == L.ERR_WORKSPACE
+    h = lib.csa2_hsi_candidates
+    assert h(_vp(0), 1, 1, 0, 10, 1, 64, 4, _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
+    assert h(_vp(FAKE), 1, 1, 0, 10, 1, 64, 0, _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
+
+
+def test_sparse_attn_validation(lib):
+    f = lib.csa2_sparse_attn
+    base = [_vp(FAKE), 1, 1, 4, 200, _vp(FAKE), 64, 32, _vp(FAKE), 8, _vp(FAKE), 128, 73, 128,
+            _vp(0), 0.05, _vp(FAKE), _vp(0), _vp(0), 0, _vp(0)]
+
+    def call(**over):
+        a = list(base)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a12=74) == L.ERR_INVALID_ARG    # window row 73 not in the window cache
+    assert call(a11=127) == L.ERR_INVALID_ARG   # query row 200 not in it
+    assert call(a8=_vp(0)) == L.ERR_INVALID_ARG  # k > 0 without top-k
+    assert call(a3=0) == L.ERR_INVALID_ARG
+    assert call(a13=0) == L.ERR_INVALID_ARG
+    assert call(a15=0.0) == L.ERR_INVALID_ARG
+
+
+def _runner(lib, kv, idx, ratio, blk=64, nb=64):
+    n = len(kv)
+    arr = C.c_int32 * n
+    h = C.c_void_p()
+    st = lib.csa2_runner_create(n, arr(*kv), arr(*idx), arr(*ratio), blk, nb, C.byref(h))
+    return st, h
+
+
+def test_runner_modes_and_rejections(lib):
+    import sys
+    sys.path.insert(0, ROOT)
+    from oracle import layers as Lr   # the oracle's table reader is the reference here
+    kv, idx, ratio = Lr.v41_flash_tables()
+    st, h = _runner(lib, kv, idx, ratio)
+    assert st == L.OK
+    modes = [lib.csa2_runner_layer_mode(h, l) for l in range(40)]
+    names = {L.MODE_SWA: "swa", L.MODE_FULL: "full", L.MODE_REINDEX: "reindex", L.MODE_REUSE: "reuse"}
+    assert [names[m] for m in modes] == Lr.layer_modes(kv, idx)
+    assert lib.csa2_runner_layer_mode(h, 40) == -1
+    p = L.StepParams(64, 1, 131071, 64, 4096, 512, 128, 0, 512 ** -0.5, 1e-6, 1e4, 0.0)
+    assert lib.csa2_runner_workspace_size(h, C.byref(p), 2, 131072) > 64 * 131072 * 4
+    lib.csa2_runner_destroy(h)
+    for kv_, idx_ in ([[0, 1], [0, 0]], [[0, 2, 2], [0, 1, 2]], [[0, 1, 0], [0, 1, 1]],
+                      [[-1, 0], [-1, 0]], [[-1], [0]]):
+        st, h = _runner(lib, kv_, idx_, [1] * len(kv_))
+        assert st == L.ERR_INVALID_ARG, (kv_, idx_)
+    assert _runner(lib, [0], [0], [3])[0] == L.ERR_UNSUPPORTED
+    assert _runner(lib, [0], [0], [1], blk=48)[0] == L.ERR_UNSUPPORTED

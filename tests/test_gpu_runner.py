@@ -1,0 +1,150 @@
+"""Full / Reindex / Reuse runtime through csa2_runner_step vs the oracle's run_step,
+end to end from seeded hidden states (no value crosses from the GPU into the oracle)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import csa2_ref as R
+from oracle import layers as Lr
+
+import helpers as Hp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from compressed_sparse_attention_04_gb300 import build
+    build.build_all()
+
+
+def make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, n0_tokens, hidden, H, seed0, S_extra=0,
+               window=128):
+    """Per-layer inputs for both sides.  Full layers get hidden states for tokens
+    0..q_pos0+Tq-1: the prefix 0..n0_tokens-1 is compressed beforehand (GPU: by the
+    stage calls; oracle: by its own compressor), the rest is the step's input."""
+    from compressed_sparse_attention_04_gb300 import ops
+    gpu, orc = [], []
+    T_all = q_pos0 + Tq
+    swa_pos0 = max(0, q_pos0 - window + 1) - S_extra
+    swa_pos0 = max(0, swa_pos0)
+    S = T_all - swa_pos0
+    for l in range(len(kv_src)):
+        s = seed0 + l
+        q, q64 = Hp.bf16_input(s, 5, (B, Tq, H, 512), 1.28)
+        swa, swa64 = Hp.bf16_input(s, 8, (B, S, 512))
+        g = dict(q=q, swa_kv=swa, swa_len=S, swa_pos0=swa_pos0, out=torch.empty_like(q))
+        o = dict(q=q64, swa=swa64, swa_pos0=swa_pos0)
+        if kv_src[l] == l or idx_src[l] == l:
+            qi, qi64 = Hp.bf16_input(s, 6, (B, Tq, 32, 128), 1.28)
+            wi, wi64 = Hp.f32_input(s, 7, (B, Tq, 32), 1.28)
+            g.update(q_idx=qi, w_idx=wi, topk_out=None)
+            o.update(q_idx=qi64, w_idx=wi64)
+        if kv_src[l] == l:
+            m = ratio[l]
+            x, x64 = Hp.bf16_input(s, 1, (B, T_all, hidden))
+            wkv, wkv64 = Hp.bf16_input(s, 2, (512, hidden), 0.02)
+            wg, wg64 = Hp.bf16_input(s, 3, (512, hidden), 0.02) if m == 2 else (None, None)
+            wik, wik64 = Hp.bf16_input(s, 4, (128, 512), 0.02)
+            gam = torch.ones(512, dtype=torch.float32, device="cuda")
+            n0 = n0_tokens // m
+            n_cap = T_all // m + 1
+            cache = torch.zeros(B, n_cap, 512, dtype=torch.bfloat16, device="cuda")
+            codes = torch.zeros(B, n_cap, 64, dtype=torch.uint8, device="cuda")
+            scl = torch.zeros(B, n_cap, 4, dtype=torch.uint8, device="cuda")
+            if n0 > 0:
+                pre = ops.compress(x[:, : n0 * m].contiguous(), wkv, wg, gam, m, 0, cache)
+                ops.index_k_quant(pre, 0, m, wik, codes, scl)
+            xs = x[:, n0 * m:].contiguous()
+            g.update(x=xs, w_kv=wkv, w_gate=wg, norm_w=gam, w_ik=wik, kv_cache=cache,
+                     idx_codes=codes, idx_scales=scl, n_cap=n_cap, x_tokens=xs.shape[1],
+                     x_pos0=n0 * m)
+            kv_p, pre_p = R.compress(x64[:, : n0 * m], wkv64, wg64, np.ones(512), m)
+            pos = m * np.arange(n0)
+            c, sc = R.index_k_quant(R.index_k(pre_p, wik64, np.broadcast_to(pos, (B, n0))))
+            o.update(x=x64[:, n0 * m:], x_pos0=n0 * m, w_kv=wkv64, w_gate=wg64,
+                     gamma=np.ones(512), w_ik=wik64,
+                     prev_kv=R.bf16_to_f64(R.f64_to_bf16_bits(kv_p)), prev_codes=c,
+                     prev_scales=sc)
+        gpu.append(g)
+        orc.append(o)
+    return gpu, orc
+
+
+def run_gpu(kv_src, idx_src, ratio, gpu_layers, B, Tq, q_pos0, H, hidden, k, blk, nb,
+            window=128):
+    from compressed_sparse_attention_04_gb300 import ops
+    runner = ops.Runner(kv_src, idx_src, ratio, hsi_blk=blk, hsi_nb=nb)
+    p = runner.params(B, Tq, q_pos0, H, hidden, k, window)
+    topks, cands = {}, {}
+    ios = []
+    for l, g in enumerate(gpu_layers):
+        md = runner.mode(l)
+        if md in (1, 2):
+            topks[l] = torch.full((B, Tq, k), -7, dtype=torch.int32, device="cuda")
+            g["topk_out"] = topks[l]
+        if md == 1:
+            cands[l] = torch.full((B, Tq, nb), -7, dtype=torch.int32, device="cuda")
+            g["cand_out"] = cands[l]
+        ios.append(ops.layer_io(**g))
+    max_x = max([g.get("x_tokens", 0) for g in gpu_layers] + [0])
+    max_n = max([(g["x_pos0"] + g["x_tokens"]) // ratio[l]
+                 for l, g in enumerate(gpu_layers) if "x_tokens" in g] + [0])
+    ws = torch.empty(runner.workspace_size(p, max_x, max_n) + 256, dtype=torch.uint8, device="cuda")
+    runner.step(p, ios, ws)
+    torch.cuda.synchronize()
+    assert ops.last_device_status() == 0
+    return runner, topks, cands
+
+
+def compare(kv_src, idx_src, ratio, gpu_layers, orc_layers, B, Tq, q_pos0, k, blk, nb, topks,
+            cands):
+    outs, trace = Lr.run_step(kv_src, idx_src, ratio, orc_layers, B, Tq, q_pos0, k, hsi_blk=blk,
+                              hsi_nb=nb)
+    modes = Lr.layer_modes(kv_src, idx_src)
+    worst = 0.0
+    for l, md in enumerate(modes):
+        if md in (Lr.FULL, Lr.REINDEX):
+            got = topks[l].cpu().numpy()
+            for (b, i), sc in trace[l]["scores"].items():
+                Hp.check_topk_row(got[b, i], sc, trace[l]["valid"][b, i], k, f"layer {l} row {b},{i}")
+        if l in cands and "candidates" in trace[l]:
+            np.testing.assert_array_equal(cands[l].cpu().numpy(), trace[l]["candidates"])
+        mx, mean = Hp.check_attention(Hp.bf16_of(gpu_layers[l]["out"]), outs[l], f"layer {l}")
+        worst = max(worst, mx)
+    return worst
+
+
+def test_runner_prefill_full_and_reuse():
+    # one Full layer (m = 2) then two Reuse layers, causal prefill of 256 tokens
+    kv_src, idx_src, ratio = [0, 0, 0], [0, 0, 0], [2, 0, 0]
+    B, T, hidden, H, k = 1, 256, 256, 16, 32
+    g, o = make_stack(kv_src, idx_src, ratio, B, T, 0, 0, hidden, H, seed0=500)
+    runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, T, 0, H, hidden, k, 64, 64)
+    compare(kv_src, idx_src, ratio, g, o, B, T, 0, k, 64, 64, topks, cands)
+
+
+def test_runner_decode_mixed_pattern():
+    # SWA-only, encoder-style Full m=2 + Reuse, decoder-style Full m=1 + Reindex (HSI) + Reuse
+    kv_src = [-1, 1, 1, 1, 4, 4, 4, 4, 4, 4, 4]
+    idx_src = [-1, 1, 1, 1, 4, 4, 6, 6, 8, 8, 8]
+    ratio = [0, 2, 0, 0, 1, 0, 0, 0, 0, 0, 0]
+    B, Tq, hidden, H, k, blk, nb = 2, 1, 128, 8, 48, 16, 8
+    C = 1200                                   # context incl. the current token
+    q_pos0 = C - 1
+    g, o = make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, q_pos0 - 1, hidden, H, seed0=700)
+    runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, Tq, q_pos0, H, hidden, k, blk, nb)
+    compare(kv_src, idx_src, ratio, g, o, B, Tq, q_pos0, k, blk, nb, topks, cands)
+
+
+def test_runner_config1_single_full_layer():
+    """Config 1 at full size: one Full layer, prefill of 1024 tokens, hidden 4096,
+    m = 2 (512 entries), top-128, window 128, 16 heads, seed 0."""
+    kv_src, idx_src, ratio = [0], [0], [2]
+    B, T, hidden, H, k = 1, 1024, 4096, 16, 128
+    g, o = make_stack(kv_src, idx_src, ratio, B, T, 0, 0, hidden, H, seed0=0)
+    runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, T, 0, H, hidden, k, 64, 64)
+    compare(kv_src, idx_src, ratio, g, o, B, T, 0, k, 64, 64, topks, cands)
