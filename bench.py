@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Decode throughput of the CSA2 global-attention hot path on one GB300.
+
+Workload (default): the 40-layer attention-only stack of DeepSeek-V4.1-Flash, one
+decode step for 64 sequences at 131072 tokens of context: layers 0-1 window only,
+encoder Full layers 2/8/14 (m = 2, 65536 entries) with Reuse layers, decoder Full
+layer 20 (m = 1, 131072 entries) building an HSI pool (top-64 blocks of 64),
+Reindex layers 24/28/32/36 and Reuse layers; 64 heads x 512, top-512, window 128.
+Inputs are seeded synthetic (generator module ``synth``); caches are built through
+the library's own compressor before timing.  A step = one csa2_runner_step call
+(every stage of the path for every layer).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode tokens/s at 128K ctx (1 GB300); indexer+sparse-attn % HBM roofline"
+STAGE_NAMES = ["compress", "index_k", "indexer_scores", "topk_select", "hsi_pool", "sparse_attn"]
+
+WORKLOADS = {
+    # the headline configuration
+    "decode40": dict(B=64, C=131072, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
+    # a small stand-in for quick checks (not a bench line)
+    "small": dict(B=4, C=8192, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
+}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------- GPU setup
+def layer_tables():
+    """The 40-layer Full/Reindex/Reuse pattern (kv_source_layer_ids, index_source_layer_ids, m)."""
+    kv, idx, ratio = [], [], []
+    cur_kv = cur_idx = -1
+    for l in range(40):
+        if l < 2:
+            kv.append(-1); idx.append(-1); ratio.append(0)
+            continue
+        if l in (2, 8, 14, 20):
+            cur_kv = cur_idx = l
+            ratio.append(2 if l < 20 else 1)
+        else:
+            if l in (24, 28, 32, 36):
+                cur_idx = l
+            ratio.append(0)
+        kv.append(cur_kv); idx.append(cur_idx)
+    return kv, idx, ratio
+
+
+class Stack:
+    """Device-resident inputs, caches and outputs of the decode step."""
+
+    def __init__(self, wl, device, seed_base=5000, log=print):
+        import torch
+        from compressed_sparse_attention_04_gb300 import ops
+        from synth import gpu as sg
+        self.wl = wl
+        B, C, H, hid, W = wl["B"], wl["C"], wl["H"], wl["hidden"], wl["window"]
+        self.t = C - 1
+        self.kv_src, self.idx_src, self.ratio = layer_tables()
+        self.runner = ops.Runner(self.kv_src, self.idx_src, self.ratio, wl["blk"], wl["nb"])
+        self.modes = [self.runner.mode(l) for l in range(40)]
+        self.params = ops.Runner.params(B, 1, self.t, H, hid, wl["k"], W)
+        self.layers = []
+        dev = device
+        t0 = time.time()
+        Tc = 2048
+        xbuf = torch.empty(B * Tc * hid, dtype=torch.bfloat16, device=dev)
+        gemm_ws = torch.empty(ops.L.load().csa2_compress_workspace_size(B, Tc, hid, 2) + 256,
+                              dtype=torch.uint8, device=dev)
+        pre_buf = torch.empty(B * Tc * 512, dtype=torch.float32, device=dev)
+        for l in range(40):
+            s = seed_base + l
+            md = self.modes[l]
+            g = {}
+            g["q"] = sg.fill_normal(torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev), s, 5, 0, 1.28)
+            g["swa_kv"] = sg.fill_normal(torch.empty(B, W, 512, dtype=torch.bfloat16, device=dev), s, 8)
+            g["swa_len"], g["swa_pos0"] = W, self.t - W + 1
+            g["out"] = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
+            if md in (1, 2):
+                g["q_idx"] = sg.fill_normal(torch.empty(B, 1, 32, 128, dtype=torch.bfloat16, device=dev), s, 6, 0, 1.28)
+                g["w_idx"] = sg.fill_normal(torch.empty(B, 1, 32, dtype=torch.float32, device=dev), s, 7, 0, 1.28)
+            if md == 1:
+                m = self.ratio[l]
+                n_cap = C // m
+                g["w_kv"] = sg.fill_normal(torch.empty(512, hid, dtype=torch.bfloat16, device=dev), s, 2, 0, 0.02)
+                g["w_gate"] = (sg.fill_normal(torch.empty(512, hid, dtype=torch.bfloat16, device=dev), s, 3, 0, 0.02)
+                               if m == 2 else None)
+                g["w_ik"] = sg.fill_normal(torch.empty(128, 512, dtype=torch.bfloat16, device=dev), s, 4, 0, 0.02)
+                g["norm_w"] = torch.ones(512, dtype=torch.float32, device=dev)
+                g["kv_cache"] = torch.empty(B, n_cap, 512, dtype=torch.bfloat16, device=dev)
+                g["idx_codes"] = torch.empty(B, n_cap, 64, dtype=torch.uint8, device=dev)
+                g["idx_scales"] = torch.empty(B, n_cap, 4, dtype=torch.uint8, device=dev)
+                g["n_cap"] = n_cap
+                # prefix: tokens 0 .. C-m-1 through the library's compressor, in chunks
+                n_prefix = C - m
+                for p0 in range(0, n_prefix, Tc):
+                    tc = min(Tc, n_prefix - p0)
+                    x = xbuf[: B * tc * hid].view(B, tc, hid)
+                    for b in range(B):
+                        sg.fill_normal(x[b], s, 1, (b * C + p0) * hid)
+                    pre = pre_buf[: B * (tc // m) * 512].view(B, tc // m, 512)
+                    ops.compress(x, g["w_kv"], g["w_gate"], g["norm_w"], m, p0, g["kv_cache"],
+                                 kv_pre=pre, workspace=gemm_ws)
+                    ops.index_k_quant(pre, p0 // m, m, g["w_ik"], g["idx_codes"], g["idx_scales"])
+                xs = torch.empty(B, m, hid, dtype=torch.bfloat16, device=dev)
+                for b in range(B):
+                    sg.fill_normal(xs[b], s, 1, (b * C + n_prefix) * hid)
+                g["x"], g["x_tokens"], g["x_pos0"] = xs, m, n_prefix
+            self.layers.append(g)
+        torch.cuda.synchronize()
+        del xbuf, gemm_ws, pre_buf
+        log(f"[bench] caches built in {time.time() - t0:.1f}s")
+        self.ios = [ops.layer_io(**g) for g in self.layers]
+        max_n = max((g["x_pos0"] + g["x_tokens"]) // self.ratio[l]
+                    for l, g in enumerate(self.layers) if "x" in g)
+        nbytes = self.runner.workspace_size(self.params, 2, max_n)
+        self.ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+
+    def step(self, stream=None):
+        self.runner.step(self.params, self.ios, self.ws, stream)
+
+    # kernels launched per step (the library's own)
+    def launches(self):
+        n = 0
+        for l, md in enumerate(self.modes):
+            if md == 1:
+                n += 2 + 1 + 2 + 1 + (1 if any(self.modes[r] == 2 and self.kv_src[r] == l for r in range(40)) else 0)
+            elif md == 2:
+                n += 2 + 1
+            else:
+                n += 1
+        return n
+
+    def stage_bytes(self, l, stage):
+        """Algorithmic HBM bytes of one stage launch (each byte the method must move once)."""
+        wl = self.wl
+        B, H, k, W, hid = wl["B"], wl["H"], wl["k"], wl["window"], wl["hidden"]
+        md = self.modes[l]
+        if stage == 5:
+            rows = (k if md != 0 else 0) + W
+            return B * rows * 1024 + 2 * B * H * 512 * 2 + (B * k * 4 if md != 0 else 0)
+        if md == 1:
+            m = self.ratio[l]
+            N = wl["C"] // m
+            if stage == 0:
+                return (512 * hid * 2) * (2 if m == 2 else 1) + B * m * hid * 2 + B * 1024 + B * 2048
+            if stage == 1:
+                return 128 * 512 * 2 + B * 2048 + B * 68
+            if stage == 2:
+                return B * N * 68 + B * (32 * 128 * 2 + 32 * 4)
+            if stage == 3:
+                return B * N * 4 + B * k * 4
+            if stage == 4:
+                return B * (N // wl["blk"]) * 4 + B * wl["nb"] * 4
+        if md == 2:
+            pool = wl["nb"] * wl["blk"]
+            if stage == 2:
+                return B * pool * 68 + B * wl["nb"] * 4 + B * (32 * 128 * 2 + 32 * 4)
+            if stage == 3:
+                return B * pool * 4 + B * k * 4
+        return 0
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, n_seq=1, seed=77):
+    """Float64 oracle inputs for n_seq sequences of the workload (values from a fast
+    NumPy generator: this leg only times the oracle)."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    kv_src, idx_src, ratio = layer_tables()
+    C, H, hid, W = wl["C"], wl["H"], wl["hidden"], wl["window"]
+    t = C - 1
+    layers = []
+    for l in range(40):
+        d = {"q": rng.standard_normal((n_seq, 1, H, 512)) * 1.28,
+             "swa": rng.standard_normal((n_seq, W, 512)), "swa_pos0": t - W + 1}
+        if idx_src[l] == l:
+            d["q_idx"] = rng.standard_normal((n_seq, 1, 32, 128)) * 1.28
+            d["w_idx"] = rng.standard_normal((n_seq, 1, 32)) * 1.28
+        if kv_src[l] == l:
+            m = ratio[l]
+            n0 = (C - m) // m
+            d.update(x=rng.standard_normal((n_seq, m, hid)), x_pos0=C - m,
+                     w_kv=rng.standard_normal((512, hid)) * 0.02,
+                     w_gate=rng.standard_normal((512, hid)) * 0.02 if m == 2 else None,
+                     gamma=np.ones(512), w_ik=rng.standard_normal((128, 512)) * 0.02,
+                     prev_kv=rng.standard_normal((n_seq, n0, 512)),
+                     prev_codes=rng.integers(0, 256, (n_seq, n0, 64), dtype=np.uint8),
+                     prev_scales=rng.integers(0x18, 0x58, (n_seq, n0, 4), dtype=np.uint8))
+        layers.append(d)
+    return kv_src, idx_src, ratio, layers
+
+
+def time_oracle(wl, budget_s=12.0, max_reps=4, sample=None):
+    from oracle import layers as Lr
+    kv_src, idx_src, ratio, layers = sample or oracle_sample(wl)
+    t = wl["C"] - 1
+    reps, total = 0, 0.0
+    while reps < max_reps and (reps == 0 or total < budget_s):
+        t0 = time.perf_counter()
+        Lr.run_step(kv_src, idx_src, ratio, layers, 1, 1, t, wl["k"], hsi_blk=wl["blk"],
+                    hsi_nb=wl["nb"], window=wl["window"])
+        total += time.perf_counter() - t0
+        reps += 1
+    return reps, total
+
+
+# ----------------------------------------------------------------------------- main arms
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return 0
+    sample = oracle_sample(wl)
+    for _ in range(args.warmup):
+        time_oracle(wl, budget_s=0, max_reps=1, sample=sample)
+    reps, total = 0, 0.0
+    for _ in range(args.steps):
+        r, tt = time_oracle(wl, budget_s=0, max_reps=1, sample=sample)
+        reps += r
+        total += tt
+    v = reps / total
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / reps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"csa2_decode_40layer_b{wl['B']}_ctx{wl['C']}", "parallelism": "replicas"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "one sequence of the decode step per timed step (B=1 of the "
+                                       f"{wl['B']}-sequence batch, full-size caches)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    from compressed_sparse_attention_04_gb300 import build
+    if rank == 0:
+        build.build_all()
+    if world > 1:
+        torch.distributed.barrier()
+    log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
+    st = Stack(wl, dev, seed_base=5000 + 100 * rank, log=log)
+    stream = torch.cuda.current_stream(dev)
+    B = wl["B"]
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    from compressed_sparse_attention_04_gb300 import ops  # noqa: F401
+    assert ops.last_device_status() == 0, "device-side check fired during warm-up"
+
+    # per-stage timing events, one array per timed step
+    n_ev = 40 * 6 * 2
+    import ctypes as C
+    lib = ops.L.load()
+    ev_sets, handles = [], []
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+        for e in evs:
+            e.record(stream)            # creates the CUDA event
+        ev_sets.append(evs)
+        handles.append((C.c_void_p * n_ev)(*[e.cuda_event for e in evs]))
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        ops.L.check(lib.csa2_runner_set_timing(st.runner._h, handles[i], n_ev), "set_timing")
+        st.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ck = clocks.stop()
+    lib.csa2_runner_set_timing(st.runner._h, None, 0)
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert ops.last_device_status() == 0, "device-side check fired during the timed steps"
+
+    # per-stage totals over the timed steps
+    stage_ms = [0.0] * 6
+    stage_bytes = [0] * 6
+    stage_launches = [0] * 6
+    for i in range(args.steps):
+        evs = ev_sets[i]
+        for l in range(40):
+            for s in range(6):
+                a, b = evs[(l * 6 + s) * 2], evs[(l * 6 + s) * 2 + 1]
+                nb = st.stage_bytes(l, s)
+                if nb == 0:
+                    continue
+                stage_ms[s] += a.elapsed_time(b)
+                stage_bytes[s] += nb
+                stage_launches[s] += 1
+    dom = max(range(6), key=lambda s: stage_ms[s])
+    peak, peak_kind = peaks()
+    achieved = stage_bytes[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    hot = [2, 3, 4, 5]
+    hot_ms = sum(stage_ms[s] for s in hot)
+    hot_gbs = sum(stage_bytes[s] for s in hot) / (hot_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(st, args, stream)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        reps, total = time_oracle(wl)
+        cpu = {"value": reps / total, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{reps} x one sequence of the decode step (all 40 layers, full-size "
+                         "caches, cache building excluded as on the GPU); NumPy float64, BLAS threads "
+                         "= host cores"}
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": B * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"csa2_decode_40layer_b{B}_ctx{wl['C']}", "batch": B,
+                   "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
+                   "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
+                   "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "hbm", "kernel": STAGE_NAMES[dom], "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "launches_timed": stage_launches[dom]},
+        "hot_path_roofline": {"stages": [STAGE_NAMES[s] for s in hot], "achieved": hot_gbs,
+                              "frac": hot_gbs / peak, "unit": "GB/s"},
+        "stage_ms_per_step": {STAGE_NAMES[s]: stage_ms[s] / args.steps for s in range(6)},
+        "gpu_launches": st.launches() * args.steps,
+        "clocks": ck,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(st, args, stream):
+    """Same step measured through the C ABI with host inputs and outputs: each step
+    copies its inputs (queries, indexer queries/weights, new hidden states, newest
+    window row) from pinned host memory and reads every layer's output back."""
+    import torch
+    h2d, d2h, pairs_in, pairs_out = 0, 0, [], []
+    for g in st.layers:
+        for key in ("q", "q_idx", "w_idx", "x"):
+            if key in g and g[key] is not None:
+                h = torch.empty_like(g[key], device="cpu").pin_memory()
+                h.copy_(g[key])
+                pairs_in.append((g[key], h))
+                h2d += g[key].numel() * g[key].element_size()
+        row = g["swa_kv"][:, -1]
+        h = torch.empty(row.shape, dtype=row.dtype).pin_memory()
+        h.copy_(row)
+        pairs_in.append((row, h))
+        h2d += row.numel() * row.element_size()
+        ho = torch.empty_like(g["out"], device="cpu").pin_memory()
+        pairs_out.append((ho, g["out"]))
+        d2h += g["out"].numel() * g["out"].element_size()
+
+    def one():
+        for d, h in pairs_in:
+            d.copy_(h, non_blocking=True)
+        st.step()
+        for h, d in pairs_out:
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(args.steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
+    return {"value": st.wl["B"] / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode40")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("[bench] warm-up raised to 3 steps (minimum)", file=sys.stderr)
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        return run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

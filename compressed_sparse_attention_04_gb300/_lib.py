@@ -12,6 +12,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(7)
 MODE_SWA, MODE_FULL, MODE_REINDEX, MODE_REUSE = range(4)
+STAGES = 6   # compress, index_k, scores, top-k, HSI, attention
 
 vp, i32, f32, sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
 
@@ -59,6 +60,7 @@ SIGNATURES = {
     "csa2_runner_destroy": (None, [vp]),
     "csa2_runner_layer_mode": (i32, [vp, i32]),
     "csa2_runner_workspace_size": (sz, [vp, C.POINTER(StepParams), i32, i32]),
+    "csa2_runner_set_timing": (i32, [vp, vp, i32]),
     "csa2_runner_step": (i32, [vp, C.POINTER(StepParams), C.POINTER(LayerIO), vp, sz, vp]),
 }
 

@@ -225,6 +225,18 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
                             int m, const int32_t* cand, int nb, int blk, int k, int32_t* topk_out,
                             float* blockmax_out, float* scores_out, void* workspace,
                             size_t ws_bytes, void* stream) {
+  return csa2::indexer_impl(q_idx, w, B, Tq, q_pos0, codes, scales, n_cap, n_entries, m, cand, nb,
+                            blk, k, topk_out, blockmax_out, scores_out, workspace, ws_bytes, stream,
+                            nullptr, nullptr);
+}
+
+}  // extern "C"
+
+int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
+                       const uint8_t* codes, const uint8_t* scales, int n_cap, int n_entries,
+                       int m, const int32_t* cand, int nb, int blk, int k, int32_t* topk_out,
+                       float* blockmax_out, float* scores_out, void* workspace, size_t ws_bytes,
+                       void* stream, cudaEvent_t ev_score_end, cudaEvent_t ev_topk_begin) {
   if (!q_idx || !w || !codes || !scales || !topk_out)
     return fail(CSA2_ERR_INVALID_ARG, "indexer: null tensor pointer");
   if (B <= 0 || Tq <= 0 || q_pos0 < 0 || m < 1 || n_entries < 0 || n_cap < n_entries ||
@@ -261,6 +273,8 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
                  int((row_len + SC_CHUNK - 1) / SC_CHUNK)};
     score_kernel<<<unsigned(rows * sa.n_chunks), SC_T, 0, st>>>(sa);
   }
+  if (ev_score_end) cudaEventRecord(ev_score_end, st);
+  if (ev_topk_begin) cudaEventRecord(ev_topk_begin, st);
   TopkArgs ta{scores, int(row_len), Tq, q_pos0, m, n_entries, cand, nb, blk, k, topk_out};
   const int staged = int(row_len < TK_SMEM_KEYS ? row_len : TK_SMEM_KEYS);
   topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
@@ -268,6 +282,8 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
   if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
   return CSA2_OK;
 }
+
+extern "C" {
 
 int csa2_hsi_candidates(const float* blockmax, int B, int Tq, int q_pos0, int n_entries, int m,
                         int blk, int nb, int32_t* cand_out, void* stream) {

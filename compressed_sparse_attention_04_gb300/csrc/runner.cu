@@ -23,6 +23,8 @@ struct csa2_runner {
   std::vector<int> kv_src, idx_src, ratio, mode;
   std::vector<char> builds_pool;
   int hsi_blk = 64, hsi_nb = 64;
+  void* const* events = nullptr;   // optional per-stage timing events
+  int n_events = 0;
 };
 
 namespace csa2 {
@@ -48,6 +50,17 @@ WsLayout layout(const csa2_runner* r, const csa2_step_params* p, int max_x_token
   w.cand = take(rows * size_t(r->hsi_nb) * sizeof(int32_t));
   w.total = off;
   return w;
+}
+
+cudaEvent_t stage_event(const csa2_runner* r, int layer, int stage, int end) {
+  if (!r->events) return nullptr;
+  const int i = (layer * CSA2_STAGES + stage) * 2 + end;
+  return i < r->n_events ? static_cast<cudaEvent_t>(r->events[i]) : nullptr;
+}
+
+void mark(const csa2_runner* r, int layer, int stage, int end, void* stream) {
+  cudaEvent_t e = stage_event(r, layer, stage, end);
+  if (e) cudaEventRecord(e, static_cast<cudaStream_t>(stream));
 }
 
 int check_params(const csa2_step_params* p) {
@@ -114,6 +127,14 @@ int csa2_runner_create(int n_layers, const int32_t* kv_src, const int32_t* idx_s
 
 void csa2_runner_destroy(csa2_runner* r) { delete r; }
 
+int csa2_runner_set_timing(csa2_runner* r, void* const* events, int n_events) {
+  if (!r) return fail(CSA2_ERR_INVALID_ARG, "runner_set_timing: null runner");
+  if (events && n_events < 0) return fail(CSA2_ERR_INVALID_ARG, "runner_set_timing: n_events < 0");
+  r->events = events;
+  r->n_events = events ? n_events : 0;
+  return CSA2_OK;
+}
+
 int csa2_runner_layer_mode(const csa2_runner* r, int layer) {
   if (!r || layer < 0 || layer >= r->n_layers) return -1;
   return r->mode[layer];
@@ -159,14 +180,18 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
     if (md == CSA2_MODE_FULL) {
       const int m = r->ratio[l];
       if (L.x_tokens > 0) {
+        mark(r, l, 0, 0, stream);
         st = csa2_compress(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv, L.w_gate,
                            L.norm_w, p->eps, p->rope_base, L.kv_cache, L.n_cap,
                            reinterpret_cast<float*>(ws + w.kv_pre), ws + w.gemm, gemm_bytes, stream);
         if (st != CSA2_OK) return st;
+        mark(r, l, 0, 1, stream);
+        mark(r, l, 1, 0, stream);
         st = csa2_index_k_quant(reinterpret_cast<float*>(ws + w.kv_pre), p->B, L.x_tokens / m,
                                 L.x_pos0 / m, m, L.w_ik, p->rope_base, L.idx_codes, L.idx_scales,
                                 L.n_cap, nullptr, stream);
         if (st != CSA2_OK) return st;
+        mark(r, l, 1, 1, stream);
       }
       n_entries[l] = (L.x_pos0 + L.x_tokens) / m;
       slot_kv = l;
@@ -180,16 +205,20 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
       const int32_t* cand = (md == CSA2_MODE_REINDEX) ? slot_cand : nullptr;
       if (md == CSA2_MODE_REINDEX && (!cand || slot_kv != f))
         return fail(CSA2_ERR_INVALID_ARG, "layer %d: no candidate pool from Full layer %d", l, f);
-      st = csa2_indexer_score_topk(L.q_idx, L.w_idx, p->B, p->Tq, p->q_pos0, F.idx_codes,
-                                   F.idx_scales, F.n_cap, n_entries[f], r->ratio[f], cand,
-                                   r->hsi_nb, r->hsi_blk, p->k, topk, bmax, nullptr,
-                                   ws + w.scores, w.blockmax - w.scores, stream);
+      mark(r, l, 2, 0, stream);
+      st = indexer_impl(L.q_idx, L.w_idx, p->B, p->Tq, p->q_pos0, F.idx_codes, F.idx_scales,
+                        F.n_cap, n_entries[f], r->ratio[f], cand, r->hsi_nb, r->hsi_blk, p->k,
+                        topk, bmax, nullptr, ws + w.scores, w.blockmax - w.scores, stream,
+                        stage_event(r, l, 2, 1), stage_event(r, l, 3, 0));
       if (st != CSA2_OK) return st;
+      mark(r, l, 3, 1, stream);
       if (pool) {
         int32_t* c = L.cand_out ? L.cand_out : reinterpret_cast<int32_t*>(ws + w.cand);
+        mark(r, l, 4, 0, stream);
         st = csa2_hsi_candidates(bmax, p->B, p->Tq, p->q_pos0, n_entries[l], r->ratio[l],
                                  r->hsi_blk, r->hsi_nb, c, stream);
         if (st != CSA2_OK) return st;
+        mark(r, l, 4, 1, stream);
         slot_cand = c;
       }
       slot_topk = topk;
@@ -211,10 +240,12 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
                     "layer %d: shared slots do not hold KV source %d / index source %d", l, f,
                     r->idx_src[l]);
     }
+    mark(r, l, 5, 0, stream);
     st = csa2_sparse_attn(L.q, p->B, p->Tq, p->H, p->q_pos0, kv, n_cap, n_ent, topk, k, L.swa_kv,
                           L.swa_len, L.swa_pos0, p->window, L.sink, p->scale, L.out, nullptr,
                           nullptr, 0, stream);
     if (st != CSA2_OK) return st;
+    mark(r, l, 5, 1, stream);
   }
   return CSA2_OK;
 }

@@ -120,7 +120,9 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m,
  *   codes/scales: cache of n_cap rows per sequence, rows 0..n_entries-1 valid
  *   cand    NULL (Full layer: all visible entries compete) or i32 [B, Tq, nb]
  *           candidate block ids (Reindex: only visible entries of these blocks of
- *           `blk` entries compete; -1 entries ignored)
+ *           `blk` entries compete; -1 entries ignored).  Ids must be distinct and
+ *           ascending, as csa2_hsi_candidates writes them; a block id >= ceil(n_entries
+ *           / blk) is skipped and sets CSA2_ERR_DEVICE_CHECK.
  *   topk_out i32 [B, Tq, k], 1 <= k <= 2048
  *   blockmax_out NULL or f32 [B, Tq, ceil(n_entries/blk)]: per block of `blk`
  *           entries, the max score over its visible entries (-inf if none); Full only
@@ -244,6 +246,15 @@ int csa2_runner_layer_mode(const csa2_runner* r, int layer);
  * new tokens and hold at most max_entries entries after the step. */
 size_t csa2_runner_workspace_size(const csa2_runner* r, const csa2_step_params* p,
                                   int max_x_tokens, int max_entries);
+/* Optional per-launch timing.  `events` holds n_events = n_layers * CSA2_STAGES * 2
+ * cudaEvent_t handles (NULL entries are skipped).  Around stage s of layer l the
+ * runner records events[(l * CSA2_STAGES + s) * 2 + 0] before and ... + 1] after the
+ * stage's kernels, on the step's stream.  Stages: 0 compressor (projection GEMM +
+ * pooling epilogue), 1 indexer key + FP4, 2 indexer scores, 3 top-k selection, 4 HSI
+ * pool, 5 sparse attention.  NULL disables timing.  The runner keeps the pointer: the
+ * array must stay valid for the steps that use it. */
+#define CSA2_STAGES 6
+int csa2_runner_set_timing(csa2_runner* r, void* const* events, int n_events);
 /* Runs every layer in order on `stream`.  io[n_layers]. */
 int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer_io* io,
                      void* workspace, size_t ws_bytes, void* stream);
