@@ -52,6 +52,9 @@ SIGNATURES = {
     "csa2_indexer_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
     "csa2_indexer_score_topk": (i32, [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, vp, i32,
                                       i32, i32, vp, vp, vp, vp, sz, vp]),
+    "csa2_indexer_noalloc_max_scratch_bytes": (sz, []),
+    "csa2_indexer_score_topk_noalloc": (i32, [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, vp,
+                                              i32, i32, i32, vp, vp, vp]),
     "csa2_hsi_candidates": (i32, [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]),
     "csa2_sparse_attn_workspace_size": (sz, [i32, i32, i32, i32, i32]),
     "csa2_sparse_attn": (i32, [vp, i32, i32, i32, i32, vp, i32, i32, vp, i32, vp, i32, i32,

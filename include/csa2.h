@@ -141,6 +141,28 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
                             void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Stage 3 without allocation.  The pages have no counterpart: this is a library
+ * convenience.  Same computation, arguments and results as csa2_indexer_score_topk
+ * (no scores_out, no workspace), for callers that cannot allocate device memory --
+ * e.g. code running inside an allocator hook or under a framework that has reserved
+ * all device memory, or a plain C host with no GPU allocator of its own.  The score
+ * scratch lives in a fixed 16 MiB array inside the library (so B * Tq * row_len <=
+ * 4 Mi scores, row_len = n_entries, or nb * blk with cand); every GPU that loads the
+ * library holds that array until the process exits.  Larger calls return
+ * CSA2_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the one array: calls that overlap on the GPU (other streams,
+ * other host threads) race and must be serialised by the caller.  Nothing in the
+ * array needs to start at zero: each call writes every score it reads.
+ * ------------------------------------------------------------------------------- */
+size_t csa2_indexer_noalloc_max_scratch_bytes(void);
+int csa2_indexer_score_topk_noalloc(const void* q_idx, const float* w, int B, int Tq,
+                                    int q_pos0, const uint8_t* codes, const uint8_t* scales,
+                                    int n_cap, int n_entries, int m, const int32_t* cand, int nb,
+                                    int blk, int k, int32_t* topk_out, float* blockmax_out,
+                                    void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Stage 3b -- hierarchical candidate pool.  [P2 §CSA2-ReIndex], [P3 §五 HSI]: the
  * blocks of `blk` entries are ranked by their block max; the block that holds the
  * newest visible entry is always taken (score +inf); the top-nb blocks by (score
