@@ -31,7 +31,7 @@ namespace csa2 {
 namespace {
 
 struct WsLayout {
-  size_t gemm, kv_pre, scores, blockmax, topk, cand, total;
+  size_t gemm, kv_pre, scores, blockmax, topk, cand, attn, total;
 };
 
 WsLayout layout(const csa2_runner* r, const csa2_step_params* p, int max_x_tokens, int max_entries) {
@@ -48,6 +48,7 @@ WsLayout layout(const csa2_runner* r, const csa2_step_params* p, int max_x_token
   w.blockmax = take(rows * size_t(ceil_div(max_entries, r->hsi_blk)) * sizeof(float));
   w.topk = take(rows * size_t(p->k) * sizeof(int32_t));
   w.cand = take(rows * size_t(r->hsi_nb) * sizeof(int32_t));
+  w.attn = take(csa2_sparse_attn_workspace_size(p->B, p->Tq, p->H, p->k, p->window));
   w.total = off;
   return w;
 }
@@ -243,7 +244,7 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
     mark(r, l, 5, 0, stream);
     st = csa2_sparse_attn(L.q, p->B, p->Tq, p->H, p->q_pos0, kv, n_cap, n_ent, topk, k, L.swa_kv,
                           L.swa_len, L.swa_pos0, p->window, L.sink, p->scale, L.out, nullptr,
-                          nullptr, 0, stream);
+                          ws + w.attn, w.total - w.attn, stream);
     if (st != CSA2_OK) return st;
     mark(r, l, 5, 1, stream);
   }

@@ -315,6 +315,11 @@ def _topk_input(seed, B, Tq, k, n_entries, holes=True):
     (1, 40, 16, 0, 20, 128, 40, 0, False),                      # prefill, window clipped at 0
     (3, 2, 12, 500, 700, 64, 200, 370, True),                   # H not a multiple of 8, sink
     (2, 1, 8, 300, 0, 0, 128, 173, False),                      # window only (k = 0)
+    # 64 heads (tensor-core path): holes + clipped window + empty tiles + sink, ragged k,
+    # window only
+    (1, 40, 64, 0, 20, 128, 40, 0, True),
+    (2, 3, 64, 500, 700, 300, 200, 370, False),
+    (2, 1, 64, 300, 0, 0, 128, 173, True),
 ])
 def test_sparse_attn_parity(B, Tq, H, q_pos0, n_entries, k, S, swa_pos0, sink):
     ops = _ops()
