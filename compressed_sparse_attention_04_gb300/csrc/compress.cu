@@ -9,10 +9,16 @@
 // [P2] "DeepSeek v4.1 Flash技术剖析——架构篇" (myhz0606.com) §Compressor.
 //
 // Kernels
-//   proj_gemm_kernel   P[M, Nout] = X[M, K] . [W_kv; W_gate]^T (bf16 in, fp32 accumulate)
+//   proj_umma_kernel   P[split][M, Nout] = X[M, K-range] . [W_kv; W_gate]^T on tcgen05: one CTA
+//                      per (128 channels, 128 rows, K-range); D^T = W X^T in TMEM; a 4-stage
+//                      cp.async pipeline feeds 128B-swizzled tiles; the K-ranges (split-K,
+//                      used when there are few rows, as in decode) are summed in fixed order
+//                      by the epilogue, so results do not depend on scheduling.
+//   proj_gemm_kernel   SIMT fallback of the same product
 //   compress_epilogue  per entry: softmax-pool over the group, RMSNorm, RoPE, stores
 //   index_k_kernel     per entry: 512 -> 128 projection, RoPE, FP4 quantisation
 #include "common.cuh"
+#include "umma.cuh"
 
 CSA2_DEFINE_ERR_WORD(d_err_compress)
 
@@ -79,9 +85,127 @@ __global__ void __launch_bounds__(GT) proj_gemm_kernel(const uint16_t* __restric
   }
 }
 
-// One block of 128 threads per entry (b, g); thread owns channels 4t..4t+3.
+
+constexpr int PU_T = 128;
+constexpr int PU_TILE = 128;                 // channels (M of the MMA) and rows (N)
+constexpr int PU_KC = 64;                    // K per stage (one 128-byte atom column)
+constexpr int PU_STAGES = 4;
+constexpr uint32_t PU_STAGE_BYTES = 2 * PU_TILE * PU_KC * 2;   // 32 KB (W tile + X tile)
+constexpr uint32_t PU_SMEM = PU_STAGES * PU_STAGE_BYTES + 1024;
+
+__global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __restrict__ X,
+                                                            const uint16_t* __restrict__ W0,
+                                                            const uint16_t* __restrict__ W1, int M,
+                                                            int K, int Nout, int k_per_split,
+                                                            float* __restrict__ P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t empty_bar[PU_STAGES], done_bar;
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * PU_TILE;            // channel tile
+  const int m0 = blockIdx.y * PU_TILE;            // row tile
+  const int split = blockIdx.z;
+  const int k_begin = split * k_per_split;
+  const int n_iter = k_per_split / PU_KC;
+  if (tid == 0) {
+    for (int s = 0; s < PU_STAGES; ++s) umma::mbar_init(&empty_bar[s], 1);
+    umma::mbar_init(&done_bar, 1);
+    umma::mbar_fence_init();
+  }
+  if (warp == 0) umma::tmem_alloc(&tmem_slot, 128);
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint16_t* wsrc[PU_TILE / 32];             // this thread's 4 channel rows
+  (void)wsrc;
+
+  auto load_stage = [&](int it) {
+    const int s = it % PU_STAGES;
+    uint8_t* Ws = base + s * PU_STAGE_BYTES;
+    uint8_t* Xs = Ws + PU_TILE * PU_KC * 2;
+    const int k0 = k_begin + it * PU_KC;
+    for (int c = tid; c < PU_TILE * 8; c += PU_T) {
+      const int r = c >> 3, ch = c & 7;
+      const int n = n0 + r;
+      const uint16_t* wrow = (n < 512) ? (W0 + size_t(n) * K) : (W1 + size_t(n - 512) * K);
+      umma::cp_async16(Ws + umma::kmajor_sw128_offset(r, ch * 8, PU_TILE), wrow + k0 + ch * 8, 16u);
+      const int m = m0 + r;
+      const uint16_t* xrow = X + size_t(m < M ? m : 0) * K;
+      umma::cp_async16(Xs + umma::kmajor_sw128_offset(r, ch * 8, PU_TILE), xrow + k0 + ch * 8,
+                       m < M ? 16u : 0u);
+    }
+  };
+  constexpr uint32_t idesc = umma::idesc_f16(PU_TILE, PU_TILE, 1, 0, 0);
+  bool ok = true;
+  // prologue: PU_STAGES - 1 stages in flight
+  for (int it = 0; it < PU_STAGES - 1; ++it) {
+    if (it < n_iter) load_stage(it);
+    umma::cp_async_commit();
+  }
+  for (int it = 0; it < n_iter; ++it) {
+    const int nxt = it + PU_STAGES - 1;
+    if (nxt < n_iter) {
+      // the stage being refilled was last read by the MMAs of iteration nxt - PU_STAGES
+      if (nxt >= PU_STAGES)
+        ok = ok && umma::mbar_wait(&empty_bar[nxt % PU_STAGES], ((nxt / PU_STAGES) - 1) & 1, &d_err_compress);
+      load_stage(nxt);
+    }
+    umma::cp_async_commit();
+    umma::cp_async_wait_pending(PU_STAGES - 1);   // stage `it` landed for this thread
+    umma::fence_proxy_async();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    if (tid == 0 && ok) {
+      const int s = it % PU_STAGES;
+      const uint32_t wb = umma::smem_u32(base + s * PU_STAGE_BYTES);
+      const uint32_t xb = wb + PU_TILE * PU_KC * 2;
+#pragma unroll
+      for (int kk = 0; kk < PU_KC / 16; ++kk)
+        umma::mma_f16(tmem, umma::desc_sw128(wb + kk * 32, 16, 1024),
+                      umma::desc_sw128(xb + kk * 32, 16, 1024), idesc, (it | kk) != 0);
+      umma::commit(&empty_bar[s]);
+      if (it == n_iter - 1) umma::commit(&done_bar);
+    }
+  }
+  umma::cp_async_wait_all();
+  if (ok) ok = umma::mbar_wait(&done_bar, 0, &d_err_compress);
+  umma::fence_after();
+  if (ok) {
+    // D^T: lane = channel n0 + 32*warp + lane, column = row m0 + c
+    const int n = n0 + warp * 32 + lane;
+    float* Pd = P + size_t(split) * size_t(M) * Nout;
+#pragma unroll 1
+    for (int c0 = 0; c0 < PU_TILE; c0 += 32) {
+      uint32_t v[32];
+      umma::tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c0), v);
+      umma::tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int m = m0 + c0 + c;
+        if (m < M) Pd[size_t(m) * Nout + n] = __uint_as_float(v[c]);
+      }
+    }
+  }
+  umma::fence_before();
+  __syncthreads();
+  if (warp == 0) umma::tmem_free(tmem, 128);
+}
+
+int proj_splits(int M, int K, int Nout) {
+  const int tiles = (Nout / PU_TILE) * ((M + PU_TILE - 1) / PU_TILE);
+  int s = 1;
+  while (s * 2 <= K / 256 && tiles * s * 2 <= 2 * 152 && (K / PU_KC) % (s * 2) == 0) s *= 2;
+  return s;
+}
+
+// One block of 128 threads per entry (b, g); thread owns channels 4t..4t+3.  P holds
+// n_split partial products (split-K) summed here in order.
 __global__ void __launch_bounds__(128) compress_epilogue_kernel(
-    const float* __restrict__ P, int Nout, int B, int T, int m, int pos0, int G,
+    const float* __restrict__ P, int n_split, size_t split_stride, int Nout, int B, int T, int m,
+    int pos0, int G,
     const float* __restrict__ norm_w, float eps, float rope_base, uint16_t* __restrict__ kv_cache,
     int n_cap, float* __restrict__ kv_pre) {
   const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x;
@@ -90,16 +214,26 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int c = 4 * t + u;
+    auto proj = [&](size_t idx) {
+      float acc = P[idx];
+      for (int sp = 1; sp < n_split; ++sp) acc += P[idx + sp * split_stride];
+      return acc;
+    };
     if (m == 1) {
-      pooled[u] = P[row0 * Nout + c];
+      pooled[u] = proj(row0 * Nout + c);
     } else {
+      float kvv[2], zz[2];
       float mx = -INFINITY;
-      for (int i = 0; i < m; ++i) mx = fmaxf(mx, P[(row0 + i) * Nout + 512 + c]);
+      for (int i = 0; i < m; ++i) {
+        zz[i] = proj((row0 + i) * Nout + 512 + c);
+        kvv[i] = proj((row0 + i) * Nout + c);
+        mx = fmaxf(mx, zz[i]);
+      }
       float num = 0.f, den = 0.f;
       for (int i = 0; i < m; ++i) {
-        const float w = expf(P[(row0 + i) * Nout + 512 + c] - mx);
+        const float w = expf(zz[i] - mx);
         den += w;
-        num = fmaf(w, P[(row0 + i) * Nout + c], num);
+        num = fmaf(w, kvv[i], num);
       }
       pooled[u] = num / den;
     }
@@ -206,10 +340,11 @@ using namespace csa2;
 extern "C" {
 
 size_t csa2_compress_workspace_size(int B, int T, int hidden, int m) {
-  (void)hidden;
-  if (B <= 0 || T <= 0 || (m != 1 && m != 2)) return 0;
+  if (B <= 0 || T <= 0 || (m != 1 && m != 2) || hidden <= 0) return 0;
   const int nout = (m == 1) ? 512 : 1024;
-  return align_up(size_t(B) * T * nout * sizeof(float), 256);
+  const long long M = (long long)B * T;
+  const int splits = (hidden % 256 == 0 && M <= (1ll << 30)) ? proj_splits(int(M), hidden, nout) : 1;
+  return align_up(size_t(splits) * size_t(M) * nout * sizeof(float), 256);
 }
 
 int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, const void* w_kv,
@@ -243,11 +378,24 @@ int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, cons
   cudaStream_t st = (cudaStream_t)stream;
   const int M = B * T, nout = (m == 1) ? 512 : 1024;
   float* P = static_cast<float*>(workspace);
-  dim3 grid(nout / GN, ceil_div(M, GM));
-  proj_gemm_kernel<<<grid, GT, 0, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
-                                        (const uint16_t*)w_gate, M, hidden, nout, P);
-  compress_epilogue_kernel<<<B * G, 128, 0, st>>>(P, nout, B, T, m, pos0, G, norm_w, eps,
-                                                   rope_base, (uint16_t*)kv_cache, n_cap, kv_pre);
+  int splits = 1;
+  if (hidden % 256 == 0) {
+    splits = proj_splits(M, hidden, nout);
+    cudaError_t e0 = cudaFuncSetAttribute(proj_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(PU_SMEM));
+    if (e0 != cudaSuccess) return cuda_fail(e0, "compress: shared memory attribute");
+    dim3 grid(nout / PU_TILE, ceil_div(M, PU_TILE), splits);
+    proj_umma_kernel<<<grid, PU_T, PU_SMEM, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
+                                                  (const uint16_t*)w_gate, M, hidden, nout,
+                                                  hidden / splits, P);
+  } else {
+    dim3 grid(nout / GN, ceil_div(M, GM));
+    proj_gemm_kernel<<<grid, GT, 0, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
+                                          (const uint16_t*)w_gate, M, hidden, nout, P);
+  }
+  compress_epilogue_kernel<<<B * G, 128, 0, st>>>(P, splits, size_t(M) * nout, nout, B, T, m, pos0,
+                                                   G, norm_w, eps, rope_base, (uint16_t*)kv_cache,
+                                                   n_cap, kv_pre);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return CSA2_OK;

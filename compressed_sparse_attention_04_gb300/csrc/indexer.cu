@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_umma_kernel(ScoreArgs a) {
 }
 
 constexpr int TK_T = 512;
-constexpr int TK_SMEM_KEYS = 11264;   // rows up to this length are staged in shared memory
+constexpr int TK_SMEM_KEYS = 32768;   // rows up to this length are staged in shared memory
 
 struct TopkArgs {
   const float* scores;
@@ -406,6 +406,71 @@ __global__ void __launch_bounds__(TK_T) topk_kernel(TopkArgs a) {
   radix_topk<TK_T>(n, a.k, key_of, emit, sm);
 }
 
+// Long rows: each (row, chunk of TK_CHUNK slots) CTA selects its local top-k into a
+// candidate list (keys + slot positions, in position order); a per-row merge then
+// selects the top-k of the concatenated lists.  Both use the same ordering, so the
+// result equals the single-pass selection.
+constexpr int TK_CHUNK = 16384;
+
+struct TopkChunkArgs {
+  TopkArgs a;
+  int n_chunks;
+  unsigned* cand_keys;   // [rows][n_chunks][k]
+  int32_t* cand_pos;     // [rows][n_chunks][k]
+};
+
+__global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
+  extern __shared__ unsigned keys_sm[];
+  __shared__ SelectSmem sm;
+  const TopkArgs& a = c.a;
+  const int row = blockIdx.x / c.n_chunks, ch = blockIdx.x % c.n_chunks, i = row % a.Tq;
+  const long long t = (long long)a.q_pos0 + i;
+  const int n_row = a.cand ? a.row_len : n_visible(t, a.m, a.n_entries);
+  const int p0 = ch * TK_CHUNK;
+  const int n = max(0, min(TK_CHUNK, n_row - p0));
+  const float* srow = a.scores + size_t(row) * a.row_len + p0;
+  for (int j = threadIdx.x; j < n; j += TK_T) {
+    const float f = srow[j];
+    keys_sm[j] = (f == -INFINITY) ? 0u : f32_key(f);
+  }
+  __syncthreads();
+  unsigned* ck = c.cand_keys + (size_t(row) * c.n_chunks + ch) * a.k;
+  int32_t* cp = c.cand_pos + (size_t(row) * c.n_chunks + ch) * a.k;
+  auto key_of = [&](int j) -> unsigned { return keys_sm[j]; };
+  auto emit = [&](int pos, int j) {
+    ck[pos] = j >= 0 ? keys_sm[j] : 0u;
+    cp[pos] = j >= 0 ? p0 + j : -1;
+  };
+  radix_topk<TK_T>(n, a.k, key_of, emit, sm);
+}
+
+__global__ void __launch_bounds__(TK_T) topk_merge_kernel(TopkChunkArgs c) {
+  extern __shared__ unsigned keys_sm[];
+  __shared__ SelectSmem sm;
+  const TopkArgs& a = c.a;
+  const int row = blockIdx.x;
+  const int n = c.n_chunks * a.k;
+  const unsigned* ck = c.cand_keys + size_t(row) * n;
+  const int32_t* cp = c.cand_pos + size_t(row) * n;
+  const bool staged = n <= TK_SMEM_KEYS;
+  if (staged) {
+    for (int j = threadIdx.x; j < n; j += TK_T) keys_sm[j] = ck[j];
+    __syncthreads();
+  }
+  auto key_of = [&](int j) -> unsigned { return staged ? keys_sm[j] : ck[j]; };
+  int32_t* orow = a.out + size_t(row) * a.k;
+  const int32_t* crow = a.cand ? a.cand + size_t(row) * a.nb : nullptr;
+  auto emit = [&](int pos, int j) {
+    int32_t v = -1;
+    if (j >= 0) {
+      const int p = cp[j];
+      v = crow ? crow[p / a.blk] * a.blk + (p % a.blk) : p;
+    }
+    orow[pos] = v;
+  };
+  radix_topk<TK_T>(n, a.k, key_of, emit, sm);
+}
+
 struct HsiArgs {
   const float* blockmax;
   int n_blocks, Tq, q_pos0, m, n_entries, blk, nb;
@@ -441,7 +506,12 @@ size_t csa2_indexer_workspace_size(int B, int Tq, int n_entries, int nb, int blk
   if (B <= 0 || Tq <= 0) return 0;
   const long long row_len = with_cand ? (long long)nb * blk : n_entries;
   if (row_len <= 0) return 0;
-  return align_up(size_t(B) * Tq * size_t(row_len) * sizeof(float), 256);
+  size_t bytes = align_up(size_t(B) * Tq * size_t(row_len) * sizeof(float), 256);
+  if (row_len > TK_SMEM_KEYS) {   // candidate lists of the chunked selection
+    const size_t n_chunks = size_t((row_len + TK_CHUNK - 1) / TK_CHUNK);
+    bytes += 2 * align_up(size_t(B) * Tq * n_chunks * CSA2_MAX_TOPK * 4, 256);
+  }
+  return bytes;
 }
 
 int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
@@ -482,13 +552,16 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   const long long row_len = cand ? (long long)nb * blk : n_entries;
   if (rows * ((row_len + SC_CHUNK - 1) / SC_CHUNK) > (1ll << 31) - 1 || row_len > (1ll << 30))
     return fail(CSA2_ERR_UNSUPPORTED, "indexer: problem too large for one call");
-  float* scores = scores_out;
-  if (!scores) {
-    const size_t need = csa2_indexer_workspace_size(B, Tq, n_entries, nb, blk, cand != nullptr);
-    if (need && (!workspace || ws_bytes < need || !aligned256(workspace)))
-      return fail(CSA2_ERR_WORKSPACE, "indexer: workspace needs %zu bytes, 256-aligned", need);
-    scores = static_cast<float*>(workspace);
-  }
+  // workspace: [scores unless scores_out is given][candidate lists for long rows]
+  const size_t scores_bytes = align_up(size_t(rows) * size_t(row_len) * sizeof(float), 256);
+  const bool chunked = row_len > TK_SMEM_KEYS;
+  const size_t n_chunks_tk = chunked ? size_t((row_len + TK_CHUNK - 1) / TK_CHUNK) : 0;
+  const size_t cand_bytes = chunked ? align_up(size_t(rows) * n_chunks_tk * CSA2_MAX_TOPK * 4, 256) : 0;
+  const size_t need = (scores_out ? 0 : scores_bytes) + 2 * cand_bytes;
+  if (need && (!workspace || ws_bytes < need || !aligned256(workspace)))
+    return fail(CSA2_ERR_WORKSPACE, "indexer: workspace needs %zu bytes, 256-aligned", need);
+  float* scores = scores_out ? scores_out : static_cast<float*>(workspace);
+  char* cand_area = static_cast<char*>(workspace) + (scores_out ? 0 : scores_bytes);
   cudaStream_t st = (cudaStream_t)stream;
   const int n_blocks = (cand || blockmax_out) ? ceil_div(n_entries, blk) : 0;
   if (row_len > 0) {
@@ -509,8 +582,26 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   if (ev_score_end) cudaEventRecord(ev_score_end, st);
   if (ev_topk_begin) cudaEventRecord(ev_topk_begin, st);
   TopkArgs ta{scores, int(row_len), Tq, q_pos0, m, n_entries, cand, nb, blk, k, topk_out};
-  const int staged = int(row_len < TK_SMEM_KEYS ? row_len : TK_SMEM_KEYS);
-  topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
+  if (!chunked) {
+    const int staged = int(row_len < TK_SMEM_KEYS ? row_len : TK_SMEM_KEYS);
+    cudaError_t e0 = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          TK_SMEM_KEYS * 4);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
+    topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
+  } else {
+    TopkChunkArgs tc{ta, int(n_chunks_tk), reinterpret_cast<unsigned*>(cand_area),
+                     reinterpret_cast<int32_t*>(cand_area + cand_bytes)};
+    cudaError_t e0 = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          TK_SMEM_KEYS * 4);
+    if (e0 == cudaSuccess)
+      e0 = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TK_SMEM_KEYS * 4);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
+    if (rows * (long long)n_chunks_tk > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "indexer: too many rows");
+    topk_chunk_kernel<<<unsigned(rows * n_chunks_tk), TK_T, size_t(TK_CHUNK) * 4, st>>>(tc);
+    const long long n_merge = (long long)n_chunks_tk * k;
+    topk_merge_kernel<<<unsigned(rows), TK_T, size_t(n_merge <= TK_SMEM_KEYS ? n_merge : 0) * 4, st>>>(tc);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
   return CSA2_OK;

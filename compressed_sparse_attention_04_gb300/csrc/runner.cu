@@ -42,9 +42,12 @@ WsLayout layout(const csa2_runner* r, const csa2_step_params* p, int max_x_token
   const size_t gemm_bytes = csa2_compress_workspace_size(p->B, max_x_tokens > 0 ? max_x_tokens : 1, p->hidden, 2);
   w.gemm = take(gemm_bytes);
   w.kv_pre = take(size_t(p->B) * (max_x_tokens > 0 ? max_x_tokens : 1) * 512 * sizeof(float));
-  const size_t pool_len = size_t(r->hsi_nb) * r->hsi_blk;
-  const size_t row_len = size_t(max_entries) > pool_len ? size_t(max_entries) : pool_len;
-  w.scores = take(rows * row_len * sizeof(float));
+  // indexer scratch (scores + top-k candidate lists): the larger of a Full call over
+  // max_entries and a Reindex call over the candidate pool
+  const size_t full_ws = csa2_indexer_workspace_size(p->B, p->Tq, max_entries, 0, r->hsi_blk, 0);
+  const size_t pool_ws = csa2_indexer_workspace_size(p->B, p->Tq, max_entries, r->hsi_nb, r->hsi_blk, 1);
+  (void)rows;
+  w.scores = take(full_ws > pool_ws ? full_ws : pool_ws);
   w.blockmax = take(rows * size_t(ceil_div(max_entries, r->hsi_blk)) * sizeof(float));
   w.topk = take(rows * size_t(p->k) * sizeof(int32_t));
   w.cand = take(rows * size_t(r->hsi_nb) * sizeof(int32_t));

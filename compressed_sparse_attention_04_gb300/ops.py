@@ -107,7 +107,7 @@ def indexer_score_topk(q_idx, w, q_pos0, codes, scales, n_entries, m, k, cand=No
         row = nb * blk if cand is not None else n_entries
         _req(scores_out, torch.float32, (B, Tq, row), "scores_out")
     need = lib.csa2_indexer_workspace_size(B, Tq, n_entries, nb, blk, int(cand is not None))
-    buf = workspace if workspace is not None else (_ws(need, q_idx.device) if scores_out is None else None)
+    buf = workspace if workspace is not None else _ws(need, q_idx.device)
     L.check(lib.csa2_indexer_score_topk(_p(q_idx), _p(w), B, Tq, q_pos0, _p(codes), _p(scales),
                                         n_cap, n_entries, m, _p(cand), nb, blk, k, _p(topk_out),
                                         _p(blockmax_out), _p(scores_out), _ws_ptr(buf),
