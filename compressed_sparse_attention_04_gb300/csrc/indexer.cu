@@ -14,14 +14,18 @@
 //                  quantises its query to FP4 (same rule as the keys), then each thread
 //                  scores one entry per pass: 32 heads x 4 blocks of 32 dims; the block
 //                  partial sums are exact in float32 and are scaled once by the key scale.
-//   score_umma_kernel  tensor-core version of score_kernel (block <= 128): keys on M = 128,
-//                  the 32 heads on N, K = 128.  Converter warps turn FP4 codes into
-//                  f16 (code value times the key's block scale, exact in f16) in a
-//                  128-byte-swizzled tile; one thread issues 8 tcgen05 MMAs per tile into
-//                  a double-buffered TMEM accumulator; epilogue warps apply ReLU and the
-//                  head weights.  All products are exact; only float32 accumulation rounds.
+//   score_fp4_kernel  tensor-core version of score_kernel (block <= 128): keys on M = 128,
+//                  the 32 heads on N, K = 128, block-scaled FP4 MMA.  Producer warps copy
+//                  the keys' packed codes straight into the operand image and put the block
+//                  scales into TMEM; one thread issues two MMAs per tile into a
+//                  double-buffered TMEM accumulator; epilogue warps apply ReLU and the head
+//                  weights.  The 16-value block products are exact; only float32
+//                  accumulation rounds.
 //   topk_kernel    one CTA per query row: radix select (select.cuh).
 //   hsi_kernel     one CTA per query row: top-nb blocks with the newest block forced.
+#include <cuda.h>
+#include <cstring>
+
 #include "common.cuh"
 #include "select.cuh"
 #include "umma.cuh"
@@ -47,6 +51,7 @@ struct ScoreArgs {
   int row_len;
   float* blockmax;         // [rows, n_blocks] or null
   int n_chunks;
+  int use_tma;             // codes through the tensor map (n_cap % 64 == 0, pool blk == 64)
 };
 
 __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
@@ -149,45 +154,101 @@ __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
 
 
 // ---------------------------------------------------------------- tensor-core scoring
-constexpr int SU_TILE = 128;                 // keys per tile (M)
-constexpr int SU_TILES = 16;                 // tiles per CTA
-constexpr int SU_STAGES = 2;                 // f16 A-tile ring
-constexpr int SU_RAW = 3;                    // raw FP4 prefetch depth (tiles)
-constexpr int SU_T = 288;                    // 4 converter + 4 epilogue + 1 MMA warp
-constexpr uint32_t SU_A_BYTES = SU_TILE * 128 * 2;     // 32 KB
-constexpr uint32_t SU_Q_BYTES = 32 * 128 * 2;          // 8 KB
-constexpr uint32_t SU_RAW_STRIDE = 80;                 // bytes per key row (64 used; padded)
-constexpr uint32_t SU_RAW_BYTES = SU_TILE * SU_RAW_STRIDE;   // 10 KB per stage
-constexpr uint32_t SU_SMEM = SU_STAGES * SU_A_BYTES + SU_Q_BYTES + SU_RAW * SU_RAW_BYTES +
-                             SU_RAW * SU_TILE * 4 + 1024;
+// Block-scaled FP4 MMA (kind::mxf4nvf4, scale_vec::4X): the packed E2M1 key codes are the
+// A operand as stored (128 keys x 64 bytes per tile, K-major, no swizzle: 8-row x 16-byte
+// core matrices, LBO = 128, SBO = 512), the query's FP4 codes the B operand, and the
+// E4M3 scales (one per 32 dims, given to the MMA once per 16) sit in TMEM in the
+// replicated chunk layout: word g of lane i holds the four block scales of row i + 32 g.
+// The MMA yields sum_blocks s_q s_k sum(e2m1 products) per (key, head) = q_hat . k_hat.
+constexpr int SU_TILE = 128;                 // keys per MMA tile (M)
+constexpr int SU_STEP = 256;                 // keys per pipeline step: two MMA tiles
+constexpr int SU_STEPS = 32;                 // steps per CTA (8192 keys)
+constexpr int SU_STAGES = 6;                 // code / scale ring (in steps)
+constexpr int SU_ND = 2;                     // TMEM accumulator buffers (in steps)
+constexpr int SU_T = 320;                    // 4 producer + 4 epilogue + 1 MMA + 1 copy warp
+constexpr uint32_t SU_A_BYTES = SU_TILE * 64;          // 8 KB of codes per tile
+constexpr uint32_t SU_STAGE_BYTES = 2 * SU_A_BYTES;    // 16 KB of codes per step
+constexpr uint32_t SU_Q_BYTES = 32 * 64;               // 2 KB of query codes
+constexpr uint32_t SU_SMEM = SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4) + SU_Q_BYTES + 1024;
+constexpr uint32_t SU_TMEM_COLS = 256;       // D 2 x 64 | SFA 6 x 16 | SFB 8
+constexpr uint32_t SU_SFA_COL = 128, SU_SFB_COL = 224;
+constexpr uint32_t SU_IDESC = (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
 
-__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
-  return r;
+// byte offset of 16-byte chunk c (0..3) of row r in the no-swizzle K-major FP4 image
+__device__ __forceinline__ uint32_t fp4_chunk_off(int r, int c) {
+  return uint32_t((r >> 3) * 512 + c * 128 + (r & 7) * 16);
 }
-__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(two_bytes));
-  return r;
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(128u >> 4) << 16;   // LBO: next 16-byte column of core matrices (K)
+  d |= uint64_t(512u >> 4) << 32;   // SBO: next group of 8 rows (M / N)
+  d |= uint64_t(1) << 46;
+  return d;
 }
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
+__device__ __forceinline__ void mma_fp4(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t sfa,
+                                        uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :: "r"(tmem_d), "l"(da), "l"(db), "r"(SU_IDESC), "r"(sfa), "r"(sfb), "r"(accumulate));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                  "r"(v[6]), "r"(v[7]) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// per-16 scale words for the two K = 64 halves from four per-32 E4M3 bytes: (s0 s0 s1 s1),
+// (s2 s2 s3 s3)
+__device__ __forceinline__ uint32_t sf_lo(uint32_t s4) { return __byte_perm(s4, 0u, 0x1100); }
+__device__ __forceinline__ uint32_t sf_hi(uint32_t s4) { return __byte_perm(s4, 0u, 0x3322); }
+
+// Placement of the 256 keys of a step in the two 128-row MMA tiles: step key 64 q + l
+// (l < 32) goes to row 32 q + l of tile 0, step key 64 q + 32 + l to row 32 q + l of
+// tile 1.  Epilogue warp q (TMEM lanes 32 q ..) then holds step keys 64 q .. 64 q + 63,
+// a whole 64-key block, so block maxima need no exchange between warps.
+__device__ __forceinline__ void step_slot(int kk, int& tile, int& r) {
+  const int q = kk >> 6, w = kk & 63;
+  tile = w >> 5;
+  r = q * 32 + (w & 31);
 }
 
-__global__ void __launch_bounds__(SU_T, 2) score_umma_kernel(ScoreArgs a) {
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(512u >> 4) << 32;   // SBO: next group of 8 rows of 64 bytes
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(4) << 61;           // SWIZZLE_64B
+  return d;
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, void* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+      :: "r"(umma::smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+         "r"(umma::smem_u32(mbar)) : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, void* mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(umma::smem_u32(dst)), "l"(src), "r"(bytes), "r"(umma::smem_u32(mbar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(void* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(umma::smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap codes_map) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* As = base;                                  // SU_STAGES x 32 KB
-  uint8_t* Qs = base + SU_STAGES * SU_A_BYTES;         // 8 KB
-  uint8_t* raw = Qs + SU_Q_BYTES;                      // SU_RAW x 10 KB of codes
-  uint32_t* raw_sc = reinterpret_cast<uint32_t*>(raw + SU_RAW * SU_RAW_BYTES);   // SU_RAW x 128
-  __shared__ __align__(8) uint64_t a_full[SU_STAGES], a_empty[SU_STAGES], d_full[2], d_empty[2];
-  __shared__ __align__(8) uint64_t epi_bar[2];
+  uint8_t* As = base;                                              // SU_STAGES x 2 tiles x 8 KB
+  uint32_t* Ss = reinterpret_cast<uint32_t*>(base + SU_STAGES * SU_STAGE_BYTES);   // SU_STAGES x 2 x 128
+  uint8_t* Qs = base + SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4);  // 2 KB query codes
+  __shared__ __align__(8) uint64_t a_empty[SU_STAGES], land[SU_STAGES], sf_ready[SU_STAGES];
+  __shared__ __align__(8) uint64_t d_full[SU_ND], d_empty[SU_ND];
   __shared__ uint32_t tmem_slot;
-  __shared__ float wmax[2][4];
+  __shared__ uint32_t qscale[32];                                  // 4 E4M3 bytes per head
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = blockIdx.x / a.n_chunks, chunk = blockIdx.x % a.n_chunks;
   const int b = row / a.Tq, i = row % a.Tq;
@@ -195,35 +256,53 @@ __global__ void __launch_bounds__(SU_T, 2) score_umma_kernel(ScoreArgs a) {
   const int n_vis = n_visible(t, a.m, a.n_entries);
   const bool pool = a.cand != nullptr;
   const int limit = pool ? a.row_len : n_vis;
-  const int c0 = chunk * SU_TILE * SU_TILES;
+  const int c0 = chunk * SU_STEP * SU_STEPS;
   if (c0 >= limit && a.blockmax == nullptr) return;   // uniform
-  int n_tiles = SU_TILES;
+  int n_steps = SU_STEPS;
   {
-    const int span = (a.blockmax ? a.row_len : limit) - c0;   // slots this CTA must cover
-    const int need = span <= 0 ? 1 : (span + SU_TILE - 1) / SU_TILE;
-    n_tiles = need < SU_TILES ? need : SU_TILES;
+    const int span = (a.blockmax ? a.row_len : limit) - c0;
+    const int need = span <= 0 ? 1 : (span + SU_STEP - 1) / SU_STEP;
+    n_steps = need < SU_STEPS ? need : SU_STEPS;
   }
 
-  // query -> FP4 (same rule as the keys) -> f16 B operand (32 heads x 128, K-major)
+  // query -> FP4 codes (B operand image) + per-head scale bytes
   const uint16_t* qrow = a.q_idx + size_t(row) * 32 * 128;
-  for (int pb = warp; pb < 128; pb += SU_T / 32) {
+  // all loads first (independent), then the quantisation
+  constexpr int QW = SU_T / 32, QIT = (128 + QW - 1) / QW;
+  float qv[QIT];
+#pragma unroll
+  for (int j = 0; j < QIT; ++j) {
+    const int pb = warp + j * QW;
+    qv[j] = pb < 128 ? bf16_to_f32(qrow[(pb >> 2) * 128 + (pb & 3) * 32 + lane]) : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < QIT; ++j) {
+    const int pb = warp + j * QW;
+    if (pb >= 128) break;
     const int h = pb >> 2, blk4 = pb & 3;
-    const float v = bf16_to_f32(qrow[h * 128 + blk4 * 32 + lane]);
+    const float v = qv[j];
     uint32_t sb;
     const uint32_t code = fp4_quant_lane(v, sb);
-    const __half qv = __float2half_rn(e2m1_value(code) * e4m3_value(sb));   // exact
-    *reinterpret_cast<__half*>(Qs + umma::kmajor_sw128_offset(h, blk4 * 32 + lane, 32)) = qv;
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+    if ((lane & 1) == 0) {
+      const int byte = blk4 * 16 + (lane >> 1);        // byte index within the head's 64
+      Qs[fp4_chunk_off(h, byte >> 4) + (byte & 15)] = uint8_t(code | (hi << 4));
+    }
+    if (lane == 0) reinterpret_cast<uint8_t*>(qscale)[h * 4 + blk4] = uint8_t(sb);
   }
   if (tid == 0) {
-    for (int s2 = 0; s2 < SU_STAGES; ++s2) { umma::mbar_init(&a_full[s2], 4); umma::mbar_init(&a_empty[s2], 1); }
-    for (int d = 0; d < 2; ++d) {
+    for (int s2 = 0; s2 < SU_STAGES; ++s2) {
+      umma::mbar_init(&a_empty[s2], 1);
+      umma::mbar_init(&land[s2], a.use_tma ? 1 : 128);   // TMA: one arrive with the byte count
+      umma::mbar_init(&sf_ready[s2], 4);
+    }
+    for (int d = 0; d < SU_ND; ++d) {
       umma::mbar_init(&d_full[d], 1);
       umma::mbar_init(&d_empty[d], 4);
-      umma::mbar_init(&epi_bar[d], 4);
     }
     umma::mbar_fence_init();
   }
-  if (warp == 0) umma::tmem_alloc(&tmem_slot, 64);
+  if (warp == 0) umma::tmem_alloc(&tmem_slot, SU_TMEM_COLS);
   umma::fence_proxy_async();
   umma::fence_before();
   __syncthreads();
@@ -232,136 +311,213 @@ __global__ void __launch_bounds__(SU_T, 2) score_umma_kernel(ScoreArgs a) {
   const size_t cache_row0 = size_t(b) * a.n_cap;
 
   if (warp < 4) {
-    // ---------------- converters: thread = key of the tile.  Each thread prefetches
-    // its own key's 64 code bytes and 4 scale bytes SU_RAW - 1 tiles ahead with
-    // asynchronous copies, then writes the f16 row into the swizzled A tile.
-    auto key_of = [&](int j) -> long long {
-      const int p = c0 + j * SU_TILE + tid;
-      if (j >= n_tiles || p >= limit) return -1;
+    // ---------------- producers: raw codes straight into the operand images, raw scale
+    // bytes beside them; then this warp's quadrant of the scale factors into TMEM.
+    const uint32_t lane_addr = uint32_t(warp * 32) << 16;
+    {   // query scale factors (columns SFB .. SFB+7): heads 0..31 in word 0 of each group
+      const uint32_t qs = qscale[lane];
+      const uint32_t v[8] = {sf_lo(qs), 0u, 0u, 0u, sf_hi(qs), 0u, 0u, 0u};
+      tmem_st8(tmem + lane_addr + SU_SFB_COL, v);
+      tmem_st_wait();
+    }
+    auto key_at = [&](int st, int kk) -> long long {   // entry of step st, step key kk (or -1)
+      const int p = c0 + st * SU_STEP + kk;
+      if (st >= n_steps || p >= limit) return -1;
       if (!pool) return p;
       const int cb = a.cand[size_t(row) * a.nb + p / a.blk];
       if (cb < 0 || cb >= a.n_blocks) return -1;
       const long long ee = (long long)cb * a.blk + (p % a.blk);
       return ee < n_vis ? ee : -1;
     };
-    auto issue = [&](int j) {
-      const long long e = key_of(j);
-      if (e >= 0) {
-        const uint8_t* src = a.codes + (cache_row0 + size_t(e)) * 64;
-        uint8_t* dst = raw + (j % SU_RAW) * SU_RAW_BYTES + tid * SU_RAW_STRIDE;
+    // 16-byte unit u = 4 * key + chunk of the step: consecutive threads copy consecutive
+    // units, so a warp reads 512 contiguous bytes whenever the keys are contiguous.
+    auto issue = [&](int st) {
+      if (st < n_steps) {
+        const int s2 = st % SU_STAGES;
+        if (st >= SU_STAGES &&
+            !umma::mbar_wait(&a_empty[s2], ((st / SU_STAGES) - 1) & 1, &d_err_indexer)) return false;
+        uint8_t* dst = As + s2 * SU_STAGE_BYTES;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) umma::cp_async16(dst + 16 * u, src + 16 * u, 16u);
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
-                     :: "r"(umma::smem_u32(raw_sc + (j % SU_RAW) * SU_TILE + tid)),
-                        "l"(a.scales + (cache_row0 + size_t(e)) * 4) : "memory");
-      }
-      umma::cp_async_commit();
-    };
-    for (int j = 0; j < SU_RAW - 1; ++j) issue(j);
-    for (int j = 0; j < n_tiles; ++j) {
-      issue(j + SU_RAW - 1);
-      umma::cp_async_wait_pending(SU_RAW - 1);   // this thread's tile-j copies landed
-      const int s2 = j % SU_STAGES;
-      if (!umma::mbar_wait(&a_empty[s2], ((j / SU_STAGES) & 1) ^ 1, &d_err_indexer)) break;
-      uint8_t* arow = As + s2 * SU_A_BYTES;
-      if (key_of(j) >= 0) {
-        const uint8_t* rsrc = raw + (j % SU_RAW) * SU_RAW_BYTES + tid * SU_RAW_STRIDE;
-        const uint32_t sc4 = raw_sc[(j % SU_RAW) * SU_TILE + tid];
+        for (int rep = 0; rep < 8; ++rep) {
+          const int u = rep * 128 + tid, kk = u >> 2, c = u & 3;
+          int tile, r;
+          step_slot(kk, tile, r);
+          const long long e = key_at(st, kk);
+          umma::cp_async16(dst + tile * SU_A_BYTES + fp4_chunk_off(r, c),
+                           a.codes + (cache_row0 + size_t(e >= 0 ? e : 0)) * 64 + 16 * c,
+                           e >= 0 ? 16u : 0u);
+        }
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          const uint4 cvv = *reinterpret_cast<const uint4*>(rsrc + 16 * kb);
-          const uint32_t sbyte = (sc4 >> (8 * kb)) & 0xFFu;
-          const uint32_t s2h = cvt_e4m3x2_f16x2(sbyte | (sbyte << 8));
-          const uint32_t w4[4] = {cvv.x, cvv.y, cvv.z, cvv.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {      // 8 codes -> 8 f16 -> one 16-byte chunk
-            uint32_t o[4];
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) o[bb] = hmul2(cvt_e2m1x2_f16x2((w4[u] >> (8 * bb)) & 0xFFu), s2h);
-            const int k = kb * 32 + u * 8;
-            *reinterpret_cast<uint4*>(arow + umma::kmajor_sw128_offset(tid, k, SU_TILE)) =
-                make_uint4(o[0], o[1], o[2], o[3]);
-          }
+        for (int rep = 0; rep < 2; ++rep) {
+          const int kk = rep * 128 + tid;
+          int tile, r;
+          step_slot(kk, tile, r);
+          const long long e = key_at(st, kk);
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
+                       :: "r"(umma::smem_u32(Ss + (s2 * 2 + tile) * SU_TILE + r)),
+                          "l"(a.scales + (cache_row0 + size_t(e >= 0 ? e : 0)) * 4),
+                          "r"(e >= 0 ? 4u : 0u) : "memory");
         }
       }
-      umma::fence_proxy_async();
+      umma::cp_async_commit();
+      return true;
+    };
+    // prefetch distance SU_STAGES - 2: the stage being refilled was read by the MMAs two
+    // steps back, which have normally finished, so the producers rarely wait on them
+    constexpr int PF = SU_STAGES - 2;
+    bool ok = true;
+    if (!a.use_tma)
+      for (int st = 0; st < PF && ok; ++st) ok = issue(st);
+    for (int st = 0; st < n_steps && ok; ++st) {
+      const int s2 = st % SU_STAGES;
+      if (!a.use_tma) {   // (with the tensor map the copy warp fills the ring)
+        ok = issue(st + PF);
+        umma::cp_async_wait_pending(PF);    // this thread's copies for step st landed
+        umma::fence_proxy_async();
+        umma::mbar_arrive(&land[s2]);
+      }
+      if (!umma::mbar_wait(&land[s2], (st / SU_STAGES) & 1, &d_err_indexer)) { ok = false; break; }
+      // scale factors of rows lane, lane + 32, lane + 64, lane + 96 of both tiles
+#pragma unroll
+      for (int tile = 0; tile < 2; ++tile) {
+        uint32_t v[8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          // row 32 g + lane of `tile` holds step key 64 g + 32 tile + lane
+          const uint32_t s4 = a.use_tma ? Ss[s2 * SU_STEP + 64 * g + 32 * tile + lane]
+                                        : Ss[(s2 * 2 + tile) * SU_TILE + g * 32 + lane];
+          v[g] = sf_lo(s4);
+          v[4 + g] = sf_hi(s4);
+        }
+        tmem_st8(tmem + lane_addr + SU_SFA_COL + 16 * s2 + 8 * tile, v);
+      }
+      tmem_st_wait();
+      umma::fence_before();
       __syncwarp();
-      if (lane == 0) umma::mbar_arrive(&a_full[s2]);
+      if (lane == 0) umma::mbar_arrive(&sf_ready[s2]);
     }
-    umma::cp_async_wait_all();
+    if (!a.use_tma) umma::cp_async_wait_all();
   } else if (warp < 8) {
-    // ---------------- epilogue: thread = key of the tile (lane quadrant warp % 4)
+    // ---------------- epilogue: warp q holds step keys 64 q .. 64 q + 63 (two tiles)
     const int q = warp & 3;
     float wv[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) wv[h] = a.w[size_t(row) * 32 + h];
-    for (int j = 0; j < n_tiles; ++j) {
-      const int d = j & 1;
-      if (!umma::mbar_wait(&d_full[d], (j >> 1) & 1, &d_err_indexer)) break;
+    for (int st = 0; st < n_steps; ++st) {
+      const int d = st % SU_ND;
+      if (!umma::mbar_wait(&d_full[d], (st / SU_ND) & 1, &d_err_indexer)) break;
       umma::fence_after();
-      uint32_t v[32];
-      umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(32 * d), v);
+      uint32_t v0[32], v1[32];
+      umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(64 * d), v0);
+      umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(64 * d + 32), v1);
       umma::tmem_ld_wait();
       umma::fence_before();
-      const int p = c0 + j * SU_TILE + q * 32 + lane;
-      bool valid = p < limit;
-      if (valid && pool) {
-        const int cb = a.cand[size_t(row) * a.nb + p / a.blk];
-        valid = cb >= 0 && cb < a.n_blocks && (long long)cb * a.blk + (p % a.blk) < n_vis;
-        if (cb >= a.n_blocks) atomicOr(&d_err_indexer, ERR_BOUNDS);
-      }
-      float sc = 0.f;
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&d_empty[d]);      // accumulators copied out
+      const int pbase = c0 + st * SU_STEP + 64 * q + lane;
+      float sc0 = 0.f, sc1 = 0.f;
 #pragma unroll
-      for (int h = 0; h < 32; ++h) sc = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.f), sc);
-      const float score = valid ? sc : -INFINITY;
-      if (p < a.row_len && (pool || p < n_vis)) a.scores[size_t(row) * a.row_len + p] = score;
+      for (int h = 0; h < 32; ++h) {
+        sc0 = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.f), sc0);
+        sc1 = fmaf(wv[h], fmaxf(__uint_as_float(v1[h]), 0.f), sc1);
+      }
+      float score[2] = {sc0, sc1};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int p = pbase + 32 * half;
+        bool valid = p < limit;
+        if (valid && pool) {
+          const int cb = a.cand[size_t(row) * a.nb + p / a.blk];
+          valid = cb >= 0 && cb < a.n_blocks && (long long)cb * a.blk + (p % a.blk) < n_vis;
+          if (cb >= a.n_blocks) atomicOr(&d_err_indexer, ERR_BOUNDS);
+        }
+        if (!valid) score[half] = -INFINITY;
+        if (p < a.row_len && (pool || p < n_vis)) a.scores[size_t(row) * a.row_len + p] = score[half];
+      }
       if (a.blockmax) {
-        // blocks of a.blk keys (power of two <= 128) never straddle a 128-key tile
-        float mx = score;
-        const int gl = a.blk < 32 ? a.blk : 32;
-        for (int o = 1; o < gl; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        // blocks of a.blk <= 64 keys lie inside one warp's 64 step keys
         if (a.blk <= 32) {
-          const int bi = p / a.blk;
-          if ((lane % a.blk) == 0 && bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = mx;
-        } else {
-          if (lane == 0) wmax[d][q] = mx;
-          __syncwarp();
-          if (lane == 0) umma::mbar_arrive(&epi_bar[d]);
-          if (!umma::mbar_wait(&epi_bar[d], (j >> 1) & 1, &d_err_indexer)) break;
-          if (lane == 0 && (q % (a.blk / 32)) == 0) {
-            float m2 = mx;
-            for (int u = 1; u < a.blk / 32; ++u) m2 = fmaxf(m2, wmax[d][q + u]);
-            const int bi = p / a.blk;
-            if (bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = m2;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float mx = score[half];
+            for (int o = 1; o < a.blk; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const int p = pbase + 32 * half, bi = p / a.blk;
+            if ((lane % a.blk) == 0 && bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = mx;
           }
+        } else {
+          float mx = fmaxf(score[0], score[1]);
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const int bi = (c0 + st * SU_STEP + 64 * q) / 64;
+          if (lane == 0 && bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = mx;
         }
       }
-      // the TMEM buffer and wmax[d] are reused two tiles later: release both now
-      __syncwarp();
-      if (lane == 0) umma::mbar_arrive(&d_empty[d]);
     }
-  } else if (lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = umma::idesc_f16(SU_TILE, 32, 0, 0, 0);
+  } else if (warp == 8 && lane == 0) {
+    // ---------------- MMA issuer: per step two tiles x two K = 64 block-scaled MMAs
     const uint32_t a0 = umma::smem_u32(As), q0 = umma::smem_u32(Qs);
-    for (int j = 0; j < n_tiles; ++j) {
-      const int s2 = j % SU_STAGES, d = j & 1;
-      if (!umma::mbar_wait(&a_full[s2], (j / SU_STAGES) & 1, &d_err_indexer)) break;
-      if (!umma::mbar_wait(&d_empty[d], ((j >> 1) & 1) ^ 1, &d_err_indexer)) break;
+    for (int st = 0; st < n_steps; ++st) {
+      const int s2 = st % SU_STAGES, d = st % SU_ND;
+      if (!umma::mbar_wait(&sf_ready[s2], (st / SU_STAGES) & 1, &d_err_indexer)) break;
+      if (!umma::mbar_wait(&d_empty[d], ((st / SU_ND) & 1) ^ 1, &d_err_indexer)) break;
       umma::fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t da = umma::desc_sw128(a0 + s2 * SU_A_BYTES + (kk >> 2) * (SU_TILE * 128) + (kk & 3) * 32, 16, 1024);
-        const uint64_t db = umma::desc_sw128(q0 + (kk >> 2) * (32 * 128) + (kk & 3) * 32, 16, 1024);
-        umma::mma_f16(tmem + 32 * d, da, db, idesc, kk > 0);
-      }
+      for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_fp4(tmem + 64 * d + 32 * tile,
+                  a.use_tma ? desc_sw64(a0 + s2 * SU_STAGE_BYTES + tile * SU_A_BYTES + ks * 32)
+                            : desc_noswz(a0 + s2 * SU_STAGE_BYTES + tile * SU_A_BYTES + ks * 256),
+                  desc_noswz(q0 + ks * 256), tmem + SU_SFA_COL + 16 * s2 + 8 * tile + 4 * ks,
+                  tmem + SU_SFB_COL + 4 * ks, ks);
       umma::commit(&a_empty[s2]);
       umma::commit(&d_full[d]);
     }
+  } else if (warp == 9 && lane == 0 && a.use_tma) {
+    // ---------------- copy thread: each step as eight 2 KB tensor copies (one per 64-key
+    // block and half) plus the scale bytes, counted in bytes on land[stage]; it runs as
+    // far ahead as the ring allows, apart from the producers that read the scales.
+    const long long total_keys = (long long)a.rows / a.Tq * a.n_cap;   // B * n_cap
+    auto issue_tma = [&](int st) {
+      if (st >= n_steps) return true;
+      const int s2 = st % SU_STAGES;
+      if (st >= SU_STAGES &&
+          !umma::mbar_wait(&a_empty[s2], ((st / SU_STAGES) - 1) & 1, &d_err_indexer)) return false;
+      const int p0 = c0 + st * SU_STEP;                // first slot of the step (64-aligned)
+      long long blk_key[4];
+      uint32_t bytes = 0;
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        long long k0 = -1;
+        if (p0 + 64 * qq < limit) {
+          if (!pool) k0 = (long long)cache_row0 + p0 + 64 * qq;
+          else {
+            const int cb = a.cand[size_t(row) * a.nb + (p0 >> 6) + qq];
+            if (cb >= 0 && cb < a.n_blocks) k0 = (long long)cache_row0 + 64ll * cb;
+          }
+        }
+        blk_key[qq] = k0;
+        if (k0 >= 0) bytes += 2 * 2048 + uint32_t(min(64ll, total_keys - k0)) * 4;
+      }
+      mbar_arrive_expect_tx(&land[s2], bytes);
+      uint8_t* dst = As + s2 * SU_STAGE_BYTES;
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        if (blk_key[qq] < 0) continue;
+        const int blk_id = int(blk_key[qq] >> 6);
+        tma_load_4d(dst + qq * 2048, &codes_map, 0, 0, 0, blk_id, &land[s2]);
+        tma_load_4d(dst + SU_A_BYTES + qq * 2048, &codes_map, 0, 0, 1, blk_id, &land[s2]);
+        bulk_load(Ss + s2 * SU_STEP + 64 * qq, a.scales + blk_key[qq] * 4,
+                  uint32_t(min(64ll, total_keys - blk_key[qq])) * 4, &land[s2]);
+      }
+      return true;
+    };
+    for (int st = 0; st < n_steps; ++st)
+      if (!issue_tma(st)) break;
   }
   umma::fence_before();
   __syncthreads();
-  if (warp == 0) umma::tmem_free(tmem, 64);
+  if (warp == 0) umma::tmem_free(tmem, SU_TMEM_COLS);
 }
 
 constexpr int TK_T = 512;
@@ -526,6 +682,40 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
 
 }  // extern "C"
 
+namespace {
+// 4-D view of the indexer-code cache for the TMA: (64 bytes of a key) x (32 keys) x
+// (2 halves) x (64-key blocks over all sequences); a box of {64, 32, 1, 1} lands one half
+// block as 32 rows of 64 bytes with the 64-byte swizzle.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || total_keys % 64 != 0 || total_keys / 64 > (1ll << 31) - 1) return false;
+  const cuuint64_t dims[4] = {64, 32, 2, cuuint64_t(total_keys / 64)};
+  const cuuint64_t strides[3] = {64, 64 * 32, 64 * 64};
+  const cuuint32_t box[4] = {64, 32, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(codes), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
                        const uint8_t* codes, const uint8_t* scales, int n_cap, int n_entries,
                        int m, const int32_t* cand, int nb, int blk, int k, int32_t* topk_out,
@@ -567,14 +757,20 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   if (row_len > 0) {
     ScoreArgs sa{(const uint16_t*)q_idx, w, int(rows), Tq, q_pos0, codes, scales, n_cap,
                  n_entries, m, cand, nb, blk, n_blocks, scores, int(row_len), blockmax_out,
-                 int((row_len + SC_CHUNK - 1) / SC_CHUNK)};
-    const bool umma_ok = !(cand || blockmax_out) || blk <= 128;
+                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0};
+    const bool umma_ok = !(cand || blockmax_out) || blk <= 64;
     if (umma_ok) {
-      sa.n_chunks = int((row_len + SU_TILE * SU_TILES - 1) / (SU_TILE * SU_TILES));
-      cudaError_t e0 = cudaFuncSetAttribute(score_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      sa.n_chunks = int((row_len + SU_STEP * SU_STEPS - 1) / (SU_STEP * SU_STEPS));
+      cudaError_t e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             int(SU_SMEM));
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: shared memory attribute");
-      score_umma_kernel<<<unsigned(rows * sa.n_chunks), SU_T, SU_SMEM, st>>>(sa);
+      CUtensorMap map;
+      memset(&map, 0, sizeof(map));
+      sa.use_tma = (n_cap % 64 == 0) && (!cand || blk == 64) &&
+                   make_codes_map(&map, codes, (long long)B * n_cap);
+      score_fp4_kernel<<<unsigned(rows * sa.n_chunks), SU_T, SU_SMEM, st>>>(sa, map);
     } else {
       score_kernel<<<unsigned(rows * sa.n_chunks), SC_T, 0, st>>>(sa);
     }

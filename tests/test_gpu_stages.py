@@ -161,6 +161,7 @@ def test_index_k_quant_parity(B, G, entry0, m):
 
 # ---------------------------------------------------------------- stage 3
 def _indexer_inputs(seed, B, Tq, n_cap, plant_ties=True):
+    """Query, weights and a random FP4 cache of n_cap rows per sequence (ties planted)."""
     qi, qi64 = Hp.bf16_input(seed, 1, (B, Tq, 32, 128), 1.28)
     w, w64 = Hp.f32_input(seed, 2, (B, Tq, 32), 1.28)
     codes, scales = Hp.index_cache_input(seed, 3, B, n_cap)
@@ -190,7 +191,8 @@ def _oracle_scores(qi64, w64, codes, scales, n):
 def test_indexer_full_parity(B, Tq, q_pos0, n_entries, m, k):
     ops = _ops()
     seed = 70 + n_entries + Tq
-    n_cap = n_entries + 3
+    # capacities that are a multiple of 64 take the TMA path, others the per-thread copies
+    n_cap = n_entries + 3 if n_entries % 2 else -(-n_entries // 64) * 64 + 64
     qi, qi64, w, w64, codes, scales = _indexer_inputs(seed, B, Tq, n_cap)
     blk = 64
     nblk = -(-n_entries // blk)
