@@ -52,6 +52,9 @@ struct ScoreArgs {
   float* blockmax;         // [rows, n_blocks] or null
   int n_chunks;
   int use_tma;             // codes through the tensor map (n_cap % 64 == 0, pool blk == 64)
+  const uint8_t* qprep;    // [rows][SU_QROW_BYTES] FP4 query images (tensor-core path)
+  const int* prefix;       // [Tq + 1] exclusive prefix of the steps per query index
+  long long total_steps;   // B * prefix[Tq]
 };
 
 __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
@@ -169,8 +172,10 @@ constexpr int SU_T = 320;                    // 4 producer + 4 epilogue + 1 MMA 
 constexpr uint32_t SU_A_BYTES = SU_TILE * 64;          // 8 KB of codes per tile
 constexpr uint32_t SU_STAGE_BYTES = 2 * SU_A_BYTES;    // 16 KB of codes per step
 constexpr uint32_t SU_Q_BYTES = 32 * 64;               // 2 KB of query codes
-constexpr uint32_t SU_SMEM = SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4) + SU_Q_BYTES + 1024;
-constexpr uint32_t SU_TMEM_COLS = 256;       // D 2 x 64 | SFA 6 x 16 | SFB 8
+constexpr uint32_t SU_QROW_BYTES = SU_Q_BYTES + 128;   // + 32 per-head scale words
+// code / scale ring, two query buffers (rows change inside a CTA's step range), alignment
+constexpr uint32_t SU_SMEM = SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4) + 2 * SU_QROW_BYTES + 1024;
+constexpr uint32_t SU_TMEM_COLS = 256;       // D 2 x 64 | SFA 6 x 16 | SFB 2 x 8
 constexpr uint32_t SU_SFA_COL = 128, SU_SFB_COL = 224;
 constexpr uint32_t SU_IDESC = (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
 
@@ -239,110 +244,160 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(void* bar, uint32_t bytes)
                :: "r"(umma::smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-__global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap codes_map) {
+// ---- persistent schedule: the steps of all rows, in row order, split evenly over the CTAs.
+// A row (query) has ceil(span / SU_STEP) steps, span = the pool length, or the visible
+// entries, or (when block maxima are produced) the whole row.  The steps of a row depend
+// only on the query index i, so one prefix table over i serves all sequences.
+__host__ __device__ inline int row_steps(int i, int q_pos0, int m, int n_entries, int row_len,
+                                         bool pool, bool blockmax) {
+  const int limit = pool ? row_len : n_visible((long long)q_pos0 + i, m, n_entries);
+  const int span = blockmax ? row_len : limit;
+  return (span + SU_STEP - 1) / SU_STEP;
+}
+
+// Walks the (sequence, query index, step) triples from a flat step number.
+struct StepCursor {
+  int b, i, st, n, k;   // sequence, query index, step within the row, steps in the row,
+                        // rows entered so far by this CTA minus one
+  __device__ void init(const ScoreArgs& a, long long s) {
+    const int T = a.prefix[a.Tq];
+    b = int(s / T);
+    const int r = int(s % T);
+    int lo = 0, hi = a.Tq - 1;   // largest i with prefix[i] <= r (that row has steps)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.prefix[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    i = lo;
+    st = r - a.prefix[i];
+    n = a.prefix[i + 1] - a.prefix[i];
+    k = 0;
+  }
+  // Advance one step; true when it enters a new row.  Only called while steps remain.
+  __device__ bool next(const ScoreArgs& a) {
+    if (++st < n) return false;
+    do {
+      if (++i == a.Tq) { i = 0; ++b; }
+      n = a.prefix[i + 1] - a.prefix[i];
+    } while (n == 0);
+    st = 0;
+    ++k;
+    return true;
+  }
+  __device__ int row(const ScoreArgs& a) const { return b * a.Tq + i; }
+};
+
+// One CTA per (query row, head), one warp per 32-dimension block: the FP4 query as the
+// MMA's B operand image (32 heads x 64 bytes, K-major, no swizzle) followed by its E4M3
+// block scales (4 bytes per head).  CTA 0 also writes the step prefix table.
+__global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep, int* prefix) {
+  __shared__ int scan[32];
+  const int tid = threadIdx.x, blk4 = tid >> 5, lane = tid & 31;
+  const long long row = blockIdx.x >> 5;
+  const int h = blockIdx.x & 31;
+  const float v = bf16_to_f32(a.q_idx[size_t(row) * 32 * 128 + h * 128 + blk4 * 32 + lane]);
+  uint32_t sb;
+  const uint32_t code = fp4_quant_lane(v, sb);
+  // eight codes per 32-bit word (element 8 j + i in nibble i), words j = 0..3 -> 16 bytes
+  uint32_t word = code << (4 * (lane & 7));
+  word |= __shfl_xor_sync(0xffffffffu, word, 1);
+  word |= __shfl_xor_sync(0xffffffffu, word, 2);
+  word |= __shfl_xor_sync(0xffffffffu, word, 4);
+  const uint32_t w1 = __shfl_sync(0xffffffffu, word, 8), w2 = __shfl_sync(0xffffffffu, word, 16),
+                 w3 = __shfl_sync(0xffffffffu, word, 24);
+  uint8_t* out = qprep + size_t(row) * SU_QROW_BYTES;
+  if (lane == 0) {
+    *reinterpret_cast<uint4*>(out + fp4_chunk_off(h, blk4)) = make_uint4(word, w1, w2, w3);
+    out[SU_Q_BYTES + h * 4 + blk4] = uint8_t(sb);
+  }
+  if (blockIdx.x == 0) {
+    const bool pool = a.cand != nullptr, bm = a.blockmax != nullptr;
+    int carry = 0;
+    for (int base = 0; base < a.Tq; base += 128) {
+      const int i = base + tid;
+      const int c = i < a.Tq ? row_steps(i, a.q_pos0, a.m, a.n_entries, a.row_len, pool, bm) : 0;
+      int tot;
+      const int ex = block_excl_scan<128>(c, scan, tot);
+      if (i < a.Tq) prefix[i] = carry + ex;
+      carry += tot;
+    }
+    if (tid == 0) prefix[a.Tq] = carry;
+  }
+}
+
+__global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap codes_map,
+                                                          const __grid_constant__ CUtensorMap codes_map4) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* As = base;                                              // SU_STAGES x 2 tiles x 8 KB
-  uint32_t* Ss = reinterpret_cast<uint32_t*>(base + SU_STAGES * SU_STAGE_BYTES);   // SU_STAGES x 2 x 128
-  uint8_t* Qs = base + SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4);  // 2 KB query codes
+  uint32_t* Ss = reinterpret_cast<uint32_t*>(base + SU_STAGES * SU_STAGE_BYTES);   // SU_STAGES x 256
+  uint8_t* Qb = base + SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4);  // 2 x query image + scales
   __shared__ __align__(8) uint64_t a_empty[SU_STAGES], land[SU_STAGES], sf_ready[SU_STAGES];
-  __shared__ __align__(8) uint64_t d_full[SU_ND], d_empty[SU_ND];
+  __shared__ __align__(8) uint64_t d_full[SU_ND], d_empty[SU_ND], q_empty[2];
   __shared__ uint32_t tmem_slot;
-  __shared__ uint32_t qscale[32];                                  // 4 E4M3 bytes per head
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = blockIdx.x / a.n_chunks, chunk = blockIdx.x % a.n_chunks;
-  const int b = row / a.Tq, i = row % a.Tq;
-  const long long t = (long long)a.q_pos0 + i;
-  const int n_vis = n_visible(t, a.m, a.n_entries);
+  const long long S = a.total_steps;
+  const long long s_begin = S * blockIdx.x / gridDim.x, s_end = S * (blockIdx.x + 1) / gridDim.x;
+  const int L = int(s_end - s_begin);
+  if (L <= 0) return;   // uniform
   const bool pool = a.cand != nullptr;
-  const int limit = pool ? a.row_len : n_vis;
-  const int c0 = chunk * SU_STEP * SU_STEPS;
-  if (c0 >= limit && a.blockmax == nullptr) return;   // uniform
-  int n_steps = SU_STEPS;
-  {
-    const int span = (a.blockmax ? a.row_len : limit) - c0;
-    const int need = span <= 0 ? 1 : (span + SU_STEP - 1) / SU_STEP;
-    n_steps = need < SU_STEPS ? need : SU_STEPS;
-  }
 
-  // query -> FP4 codes (B operand image) + per-head scale bytes
-  const uint16_t* qrow = a.q_idx + size_t(row) * 32 * 128;
-  // all loads first (independent), then the quantisation
-  constexpr int QW = SU_T / 32, QIT = (128 + QW - 1) / QW;
-  float qv[QIT];
-#pragma unroll
-  for (int j = 0; j < QIT; ++j) {
-    const int pb = warp + j * QW;
-    qv[j] = pb < 128 ? bf16_to_f32(qrow[(pb >> 2) * 128 + (pb & 3) * 32 + lane]) : 0.f;
-  }
-#pragma unroll
-  for (int j = 0; j < QIT; ++j) {
-    const int pb = warp + j * QW;
-    if (pb >= 128) break;
-    const int h = pb >> 2, blk4 = pb & 3;
-    const float v = qv[j];
-    uint32_t sb;
-    const uint32_t code = fp4_quant_lane(v, sb);
-    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
-    if ((lane & 1) == 0) {
-      const int byte = blk4 * 16 + (lane >> 1);        // byte index within the head's 64
-      Qs[fp4_chunk_off(h, byte >> 4) + (byte & 15)] = uint8_t(code | (hi << 4));
-    }
-    if (lane == 0) reinterpret_cast<uint8_t*>(qscale)[h * 4 + blk4] = uint8_t(sb);
-  }
   if (tid == 0) {
     for (int s2 = 0; s2 < SU_STAGES; ++s2) {
       umma::mbar_init(&a_empty[s2], 1);
-      umma::mbar_init(&land[s2], a.use_tma ? 1 : 128);   // TMA: one arrive with the byte count
+      // TMA: the copy thread's arrive with the byte count; otherwise also the producers'
+      umma::mbar_init(&land[s2], a.use_tma ? 1 : 129);
       umma::mbar_init(&sf_ready[s2], 4);
     }
     for (int d = 0; d < SU_ND; ++d) {
       umma::mbar_init(&d_full[d], 1);
       umma::mbar_init(&d_empty[d], 4);
     }
+    umma::mbar_init(&q_empty[0], 1);
+    umma::mbar_init(&q_empty[1], 1);
     umma::mbar_fence_init();
   }
   if (warp == 0) umma::tmem_alloc(&tmem_slot, SU_TMEM_COLS);
-  umma::fence_proxy_async();
   umma::fence_before();
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
-  const size_t cache_row0 = size_t(b) * a.n_cap;
 
   if (warp < 4) {
-    // ---------------- producers: raw codes straight into the operand images, raw scale
-    // bytes beside them; then this warp's quadrant of the scale factors into TMEM.
+    // ---------------- producers: (without the tensor map) the codes and scale bytes by
+    // cp.async; then this warp's quadrant of the scale factors into TMEM.
     const uint32_t lane_addr = uint32_t(warp * 32) << 16;
-    {   // query scale factors (columns SFB .. SFB+7): heads 0..31 in word 0 of each group
-      const uint32_t qs = qscale[lane];
-      const uint32_t v[8] = {sf_lo(qs), 0u, 0u, 0u, sf_hi(qs), 0u, 0u, 0u};
-      tmem_st8(tmem + lane_addr + SU_SFB_COL, v);
-      tmem_st_wait();
-    }
-    auto key_at = [&](int st, int kk) -> long long {   // entry of step st, step key kk (or -1)
-      const int p = c0 + st * SU_STEP + kk;
-      if (st >= n_steps || p >= limit) return -1;
-      if (!pool) return p;
-      const int cb = a.cand[size_t(row) * a.nb + p / a.blk];
-      if (cb < 0 || cb >= a.n_blocks) return -1;
-      const long long ee = (long long)cb * a.blk + (p % a.blk);
-      return ee < n_vis ? ee : -1;
-    };
+    StepCursor ci, cs;   // copy cursor (runs PF steps ahead), scale-factor cursor
+    ci.init(a, s_begin);
+    cs.init(a, s_begin);
     // 16-byte unit u = 4 * key + chunk of the step: consecutive threads copy consecutive
     // units, so a warp reads 512 contiguous bytes whenever the keys are contiguous.
-    auto issue = [&](int st) {
-      if (st < n_steps) {
-        const int s2 = st % SU_STAGES;
-        if (st >= SU_STAGES &&
-            !umma::mbar_wait(&a_empty[s2], ((st / SU_STAGES) - 1) & 1, &d_err_indexer)) return false;
+    auto issue = [&](int g) {
+      if (g < L) {
+        if (g > 0) ci.next(a);
+        const int s2 = g % SU_STAGES;
+        if (g >= SU_STAGES &&
+            !umma::mbar_wait(&a_empty[s2], ((g / SU_STAGES) - 1) & 1, &d_err_indexer)) return false;
+        const int row = ci.row(a);
+        const int n_vis = n_visible((long long)a.q_pos0 + ci.i, a.m, a.n_entries);
+        const int limit = pool ? a.row_len : n_vis;
+        const size_t cache_row0 = size_t(ci.b) * a.n_cap;
+        auto key_at = [&](int kk) -> long long {   // entry of step key kk (or -1)
+          const int p = ci.st * SU_STEP + kk;
+          if (p >= limit) return -1;
+          if (!pool) return p;
+          const int cb = a.cand[size_t(row) * a.nb + p / a.blk];
+          if (cb < 0 || cb >= a.n_blocks) return -1;
+          const long long ee = (long long)cb * a.blk + (p % a.blk);
+          return ee < n_vis ? ee : -1;
+        };
         uint8_t* dst = As + s2 * SU_STAGE_BYTES;
 #pragma unroll
         for (int rep = 0; rep < 8; ++rep) {
           const int u = rep * 128 + tid, kk = u >> 2, c = u & 3;
           int tile, r;
           step_slot(kk, tile, r);
-          const long long e = key_at(st, kk);
+          const long long e = key_at(kk);
           umma::cp_async16(dst + tile * SU_A_BYTES + fp4_chunk_off(r, c),
                            a.codes + (cache_row0 + size_t(e >= 0 ? e : 0)) * 64 + 16 * c,
                            e >= 0 ? 16u : 0u);
@@ -350,11 +405,9 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
 #pragma unroll
         for (int rep = 0; rep < 2; ++rep) {
           const int kk = rep * 128 + tid;
-          int tile, r;
-          step_slot(kk, tile, r);
-          const long long e = key_at(st, kk);
+          const long long e = key_at(kk);
           asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;"
-                       :: "r"(umma::smem_u32(Ss + (s2 * 2 + tile) * SU_TILE + r)),
+                       :: "r"(umma::smem_u32(Ss + s2 * SU_STEP + kk)),
                           "l"(a.scales + (cache_row0 + size_t(e >= 0 ? e : 0)) * 4),
                           "r"(e >= 0 ? 4u : 0u) : "memory");
         }
@@ -367,27 +420,33 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
     constexpr int PF = SU_STAGES - 2;
     bool ok = true;
     if (!a.use_tma)
-      for (int st = 0; st < PF && ok; ++st) ok = issue(st);
-    for (int st = 0; st < n_steps && ok; ++st) {
-      const int s2 = st % SU_STAGES;
-      if (!a.use_tma) {   // (with the tensor map the copy warp fills the ring)
-        ok = issue(st + PF);
-        umma::cp_async_wait_pending(PF);    // this thread's copies for step st landed
+      for (int g = 0; g < PF && ok; ++g) ok = issue(g);
+    for (int g = 0; g < L && ok; ++g) {
+      const bool new_row = g == 0 || cs.next(a);
+      const int s2 = g % SU_STAGES;
+      if (!a.use_tma) {   // (with the tensor map the copy thread fills the ring)
+        ok = issue(g + PF);
+        umma::cp_async_wait_pending(PF);    // this thread's copies for step g landed
         umma::fence_proxy_async();
         umma::mbar_arrive(&land[s2]);
       }
-      if (!umma::mbar_wait(&land[s2], (st / SU_STAGES) & 1, &d_err_indexer)) { ok = false; break; }
-      // scale factors of rows lane, lane + 32, lane + 64, lane + 96 of both tiles
+      if (!umma::mbar_wait(&land[s2], (g / SU_STAGES) & 1, &d_err_indexer)) { ok = false; break; }
+      if (new_row) {   // query scale factors: heads 0..31 in word 0 of each 4-column group
+        const uint32_t qs = reinterpret_cast<const uint32_t*>(Qb + (cs.k & 1) * SU_QROW_BYTES + SU_Q_BYTES)[lane];
+        const uint32_t v[8] = {sf_lo(qs), 0u, 0u, 0u, sf_hi(qs), 0u, 0u, 0u};
+        tmem_st8(tmem + lane_addr + SU_SFB_COL + 8 * (cs.k & 1), v);
+      }
+      // scale factors of rows lane, lane + 32, lane + 64, lane + 96 of both tiles; the
+      // step's scale bytes are stored in step-key order
 #pragma unroll
       for (int tile = 0; tile < 2; ++tile) {
         uint32_t v[8];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          // row 32 g + lane of `tile` holds step key 64 g + 32 tile + lane
-          const uint32_t s4 = a.use_tma ? Ss[s2 * SU_STEP + 64 * g + 32 * tile + lane]
-                                        : Ss[(s2 * 2 + tile) * SU_TILE + g * 32 + lane];
-          v[g] = sf_lo(s4);
-          v[4 + g] = sf_hi(s4);
+        for (int g4 = 0; g4 < 4; ++g4) {
+          // row 32 g4 + lane of `tile` holds step key 64 g4 + 32 tile + lane
+          const uint32_t s4 = Ss[s2 * SU_STEP + 64 * g4 + 32 * tile + lane];
+          v[g4] = sf_lo(s4);
+          v[4 + g4] = sf_hi(s4);
         }
         tmem_st8(tmem + lane_addr + SU_SFA_COL + 16 * s2 + 8 * tile, v);
       }
@@ -400,12 +459,20 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
   } else if (warp < 8) {
     // ---------------- epilogue: warp q holds step keys 64 q .. 64 q + 63 (two tiles)
     const int q = warp & 3;
+    StepCursor ce;
+    ce.init(a, s_begin);
     float wv[32];
+    for (int g = 0; g < L; ++g) {
+      const bool new_row = g == 0 || ce.next(a);
+      const int row = ce.row(a);
+      if (new_row) {
 #pragma unroll
-    for (int h = 0; h < 32; ++h) wv[h] = a.w[size_t(row) * 32 + h];
-    for (int st = 0; st < n_steps; ++st) {
-      const int d = st % SU_ND;
-      if (!umma::mbar_wait(&d_full[d], (st / SU_ND) & 1, &d_err_indexer)) break;
+        for (int h = 0; h < 32; ++h) wv[h] = a.w[size_t(row) * 32 + h];
+      }
+      const int n_vis = n_visible((long long)a.q_pos0 + ce.i, a.m, a.n_entries);
+      const int limit = pool ? a.row_len : n_vis;
+      const int d = g % SU_ND;
+      if (!umma::mbar_wait(&d_full[d], (g / SU_ND) & 1, &d_err_indexer)) break;
       umma::fence_after();
       uint32_t v0[32], v1[32];
       umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(64 * d), v0);
@@ -414,7 +481,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&d_empty[d]);      // accumulators copied out
-      const int pbase = c0 + st * SU_STEP + 64 * q + lane;
+      const int pbase = ce.st * SU_STEP + 64 * q + lane;
       float sc0 = 0.f, sc1 = 0.f;
 #pragma unroll
       for (int h = 0; h < 32; ++h) {
@@ -448,18 +515,23 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
           float mx = fmaxf(score[0], score[1]);
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          const int bi = (c0 + st * SU_STEP + 64 * q) / 64;
+          const int bi = (ce.st * SU_STEP + 64 * q) / 64;
           if (lane == 0 && bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = mx;
         }
       }
     }
   } else if (warp == 8 && lane == 0) {
     // ---------------- MMA issuer: per step two tiles x two K = 64 block-scaled MMAs
-    const uint32_t a0 = umma::smem_u32(As), q0 = umma::smem_u32(Qs);
-    for (int st = 0; st < n_steps; ++st) {
-      const int s2 = st % SU_STAGES, d = st % SU_ND;
-      if (!umma::mbar_wait(&sf_ready[s2], (st / SU_STAGES) & 1, &d_err_indexer)) break;
-      if (!umma::mbar_wait(&d_empty[d], ((st / SU_ND) & 1) ^ 1, &d_err_indexer)) break;
+    const uint32_t a0 = umma::smem_u32(As), q0 = umma::smem_u32(Qb);
+    StepCursor cm;
+    cm.init(a, s_begin);
+    for (int g = 0; g < L; ++g) {
+      // a new row: the MMAs so far are the last ones that read the other query buffer's
+      // predecessor, so that buffer may be refilled once they complete
+      if (g > 0 && cm.next(a)) umma::commit(&q_empty[(cm.k - 1) & 1]);
+      const int s2 = g % SU_STAGES, d = g % SU_ND, qb = cm.k & 1;
+      if (!umma::mbar_wait(&sf_ready[s2], (g / SU_STAGES) & 1, &d_err_indexer)) break;
+      if (!umma::mbar_wait(&d_empty[d], ((g / SU_ND) & 1) ^ 1, &d_err_indexer)) break;
       umma::fence_after();
 #pragma unroll
       for (int tile = 0; tile < 2; ++tile)
@@ -468,39 +540,67 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
           mma_fp4(tmem + 64 * d + 32 * tile,
                   a.use_tma ? desc_sw64(a0 + s2 * SU_STAGE_BYTES + tile * SU_A_BYTES + ks * 32)
                             : desc_noswz(a0 + s2 * SU_STAGE_BYTES + tile * SU_A_BYTES + ks * 256),
-                  desc_noswz(q0 + ks * 256), tmem + SU_SFA_COL + 16 * s2 + 8 * tile + 4 * ks,
-                  tmem + SU_SFB_COL + 4 * ks, ks);
+                  desc_noswz(q0 + qb * SU_QROW_BYTES + ks * 256),
+                  tmem + SU_SFA_COL + 16 * s2 + 8 * tile + 4 * ks,
+                  tmem + SU_SFB_COL + 8 * qb + 4 * ks, ks);
       umma::commit(&a_empty[s2]);
       umma::commit(&d_full[d]);
     }
-  } else if (warp == 9 && lane == 0 && a.use_tma) {
-    // ---------------- copy thread: each step as eight 2 KB tensor copies (one per 64-key
-    // block and half) plus the scale bytes, counted in bytes on land[stage]; it runs as
-    // far ahead as the ring allows, apart from the producers that read the scales.
+  } else if (warp == 9 && lane == 0) {
+    // ---------------- copy thread: the row's query image at each new row; with the tensor
+    // map also each step as eight 2 KB tensor copies (one per 64-key block and half) plus
+    // the scale bytes.  Completion is counted in bytes on land[stage]; it runs as far ahead
+    // as the ring allows.
     const long long total_keys = (long long)a.rows / a.Tq * a.n_cap;   // B * n_cap
-    auto issue_tma = [&](int st) {
-      if (st >= n_steps) return true;
-      const int s2 = st % SU_STAGES;
-      if (st >= SU_STAGES &&
-          !umma::mbar_wait(&a_empty[s2], ((st / SU_STAGES) - 1) & 1, &d_err_indexer)) return false;
-      const int p0 = c0 + st * SU_STEP;                // first slot of the step (64-aligned)
-      long long blk_key[4];
-      uint32_t bytes = 0;
+    StepCursor cc;
+    cc.init(a, s_begin);
+    for (int g = 0; g < L; ++g) {
+      const bool new_row = g == 0 || cc.next(a);
+      const int s2 = g % SU_STAGES;
+      if (g >= SU_STAGES &&
+          !umma::mbar_wait(&a_empty[s2], ((g / SU_STAGES) - 1) & 1, &d_err_indexer)) break;
+      const int qb = cc.k & 1;
+      if (new_row && cc.k >= 2 &&
+          !umma::mbar_wait(&q_empty[qb], ((cc.k >> 1) - 1) & 1, &d_err_indexer)) break;
+      const int row = cc.row(a);
+      long long blk_key[4] = {-1, -1, -1, -1};   // pool steps: the four blocks' first keys
+      long long dense_key = -1;                   // dense steps: the step's first key
+      uint32_t bytes = new_row ? SU_QROW_BYTES : 0u;
+      if (a.use_tma) {
+        const int p0 = cc.st * SU_STEP;                // first slot of the step (64-aligned)
+        const int limit = pool ? a.row_len : n_visible((long long)a.q_pos0 + cc.i, a.m, a.n_entries);
+        const long long cache_row0 = (long long)cc.b * a.n_cap;
+        if (!pool) {
+          // four consecutive blocks in two 8 KB boxes (blocks past the end of the cache
+          // arrive zero-filled; keys past the visible ones are masked by the epilogue)
+          if (p0 < limit) {
+            dense_key = cache_row0 + p0;
+            bytes += 2 * SU_A_BYTES + uint32_t(min(256ll, total_keys - dense_key)) * 4;
+          }
+        } else {
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        long long k0 = -1;
-        if (p0 + 64 * qq < limit) {
-          if (!pool) k0 = (long long)cache_row0 + p0 + 64 * qq;
-          else {
-            const int cb = a.cand[size_t(row) * a.nb + (p0 >> 6) + qq];
-            if (cb >= 0 && cb < a.n_blocks) k0 = (long long)cache_row0 + 64ll * cb;
+          for (int qq = 0; qq < 4; ++qq) {
+            long long k0 = -1;
+            if (p0 + 64 * qq < limit) {
+              const int cb = a.cand[size_t(row) * a.nb + (p0 >> 6) + qq];
+              if (cb >= 0 && cb < a.n_blocks) k0 = cache_row0 + 64ll * cb;
+            }
+            blk_key[qq] = k0;
+            if (k0 >= 0) bytes += 2 * 2048 + uint32_t(min(64ll, total_keys - k0)) * 4;
           }
         }
-        blk_key[qq] = k0;
-        if (k0 >= 0) bytes += 2 * 2048 + uint32_t(min(64ll, total_keys - k0)) * 4;
       }
       mbar_arrive_expect_tx(&land[s2], bytes);
+      if (new_row)
+        bulk_load(Qb + qb * SU_QROW_BYTES, a.qprep + size_t(row) * SU_QROW_BYTES, SU_QROW_BYTES, &land[s2]);
       uint8_t* dst = As + s2 * SU_STAGE_BYTES;
+      if (dense_key >= 0) {
+        const int blk_id = int(dense_key >> 6);
+        tma_load_4d(dst, &codes_map4, 0, 0, 0, blk_id, &land[s2]);
+        tma_load_4d(dst + SU_A_BYTES, &codes_map4, 0, 0, 1, blk_id, &land[s2]);
+        bulk_load(Ss + s2 * SU_STEP, a.scales + dense_key * 4,
+                  uint32_t(min(256ll, total_keys - dense_key)) * 4, &land[s2]);
+      }
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         if (blk_key[qq] < 0) continue;
@@ -510,10 +610,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
         bulk_load(Ss + s2 * SU_STEP + 64 * qq, a.scales + blk_key[qq] * 4,
                   uint32_t(min(64ll, total_keys - blk_key[qq])) * 4, &land[s2]);
       }
-      return true;
-    };
-    for (int st = 0; st < n_steps; ++st)
-      if (!issue_tma(st)) break;
+    }
   }
   umma::fence_before();
   __syncthreads();
@@ -667,6 +764,8 @@ size_t csa2_indexer_workspace_size(int B, int Tq, int n_entries, int nb, int blk
     const size_t n_chunks = size_t((row_len + TK_CHUNK - 1) / TK_CHUNK);
     bytes += 2 * align_up(size_t(B) * Tq * n_chunks * CSA2_MAX_TOPK * 4, 256);
   }
+  // FP4 query images and the step prefix table of the tensor-core scorer
+  bytes += align_up(size_t(B) * Tq * SU_QROW_BYTES, 256) + align_up(size_t(Tq + 1) * 4, 256);
   return bytes;
 }
 
@@ -684,8 +783,9 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
 
 namespace {
 // 4-D view of the indexer-code cache for the TMA: (64 bytes of a key) x (32 keys) x
-// (2 halves) x (64-key blocks over all sequences); a box of {64, 32, 1, 1} lands one half
-// block as 32 rows of 64 bytes with the 64-byte swizzle.
+// (2 halves) x (64-key blocks over all sequences).  A box of {64, 32, 1, nblk} lands one
+// half of nblk consecutive blocks as 32 nblk rows of 64 bytes with the 64-byte swizzle:
+// with nblk = 4 that is one whole MMA tile of a 256-key step.
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -703,12 +803,12 @@ EncodeTiledFn encode_fn() {
   }
   return fn;
 }
-bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys) {
+bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys, int nblk) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || total_keys % 64 != 0 || total_keys / 64 > (1ll << 31) - 1) return false;
   const cuuint64_t dims[4] = {64, 32, 2, cuuint64_t(total_keys / 64)};
   const cuuint64_t strides[3] = {64, 64 * 32, 64 * 64};
-  const cuuint32_t box[4] = {64, 32, 1, 1};
+  const cuuint32_t box[4] = {64, 32, 1, cuuint32_t(nblk)};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(codes), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -740,37 +840,68 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
     return fail(CSA2_ERR_INVALID_ARG, "indexer: pointers must be 16-byte aligned");
   const long long rows = (long long)B * Tq;
   const long long row_len = cand ? (long long)nb * blk : n_entries;
-  if (rows * ((row_len + SC_CHUNK - 1) / SC_CHUNK) > (1ll << 31) - 1 || row_len > (1ll << 30))
+  if (rows * ((row_len + SC_CHUNK - 1) / SC_CHUNK) > (1ll << 31) - 1 || row_len > (1ll << 30) ||
+      rows > (1ll << 26))
     return fail(CSA2_ERR_UNSUPPORTED, "indexer: problem too large for one call");
   // workspace: [scores unless scores_out is given][candidate lists for long rows]
   const size_t scores_bytes = align_up(size_t(rows) * size_t(row_len) * sizeof(float), 256);
   const bool chunked = row_len > TK_SMEM_KEYS;
   const size_t n_chunks_tk = chunked ? size_t((row_len + TK_CHUNK - 1) / TK_CHUNK) : 0;
   const size_t cand_bytes = chunked ? align_up(size_t(rows) * n_chunks_tk * CSA2_MAX_TOPK * 4, 256) : 0;
-  const size_t need = (scores_out ? 0 : scores_bytes) + 2 * cand_bytes;
-  if (need && (!workspace || ws_bytes < need || !aligned256(workspace)))
+  const size_t qprep_bytes = align_up(size_t(rows) * SU_QROW_BYTES, 256);
+  const size_t prefix_bytes = align_up(size_t(Tq + 1) * 4, 256);
+  const size_t need = (scores_out ? 0 : scores_bytes) + 2 * cand_bytes + qprep_bytes + prefix_bytes;
+  if (!workspace || ws_bytes < need || !aligned256(workspace))
     return fail(CSA2_ERR_WORKSPACE, "indexer: workspace needs %zu bytes, 256-aligned", need);
   float* scores = scores_out ? scores_out : static_cast<float*>(workspace);
   char* cand_area = static_cast<char*>(workspace) + (scores_out ? 0 : scores_bytes);
+  uint8_t* qprep = reinterpret_cast<uint8_t*>(cand_area + 2 * cand_bytes);
+  int* prefix = reinterpret_cast<int*>(qprep + qprep_bytes);
   cudaStream_t st = (cudaStream_t)stream;
   const int n_blocks = (cand || blockmax_out) ? ceil_div(n_entries, blk) : 0;
   if (row_len > 0) {
     ScoreArgs sa{(const uint16_t*)q_idx, w, int(rows), Tq, q_pos0, codes, scales, n_cap,
                  n_entries, m, cand, nb, blk, n_blocks, scores, int(row_len), blockmax_out,
-                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0};
+                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0, qprep, prefix, 0};
     const bool umma_ok = !(cand || blockmax_out) || blk <= 64;
     if (umma_ok) {
-      sa.n_chunks = int((row_len + SU_STEP * SU_STEPS - 1) / (SU_STEP * SU_STEPS));
-      cudaError_t e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            int(SU_SMEM));
-      if (e0 == cudaSuccess)
-        e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-      if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: shared memory attribute");
-      CUtensorMap map;
-      memset(&map, 0, sizeof(map));
+      long long per_seq = 0;   // steps of one sequence's Tq rows (same formula as the device)
+      for (int i = 0; i < Tq; ++i)
+        per_seq += row_steps(i, q_pos0, m, n_entries, int(row_len), cand != nullptr, blockmax_out != nullptr);
+      sa.total_steps = per_seq * B;
+      if (per_seq > (1ll << 31) - 1 || sa.total_steps > (1ll << 40))
+        return fail(CSA2_ERR_UNSUPPORTED, "indexer: problem too large for one call");
+      static int slots[64] = {0};   // resident scoring CTAs per device
+      int dev = 0;
+      cudaError_t e0 = cudaGetDevice(&dev);
+      if (e0 == cudaSuccess && (dev < 0 || dev >= 64)) return fail(CSA2_ERR_UNSUPPORTED, "indexer: device id");
+      if (e0 == cudaSuccess && slots[dev] == 0) {
+        e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(SU_SMEM));
+        if (e0 == cudaSuccess)
+          e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        // two CTAs per SM when their shared memory fits (the launch bounds cap registers for
+        // two, and their TMEM is 2 x 256 columns); the occupancy query reports one for
+        // kernels that use the tensor memory, so it is not consulted
+        int sms = 0, smem_sm = 0;
+        if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e0 == cudaSuccess)
+          e0 = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        const int per_cta = int(SU_SMEM) + 2048;   // + static shared memory and the reserved 1 KB
+        if (e0 == cudaSuccess) slots[dev] = sms * (smem_sm >= 2 * per_cta ? 2 : 1);
+      }
+      if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: scorer attributes");
+      CUtensorMap map1, map4;   // boxes of one block (pool steps) and four (dense steps)
+      memset(&map1, 0, sizeof(map1));
+      memset(&map4, 0, sizeof(map4));
       sa.use_tma = (n_cap % 64 == 0) && (!cand || blk == 64) &&
-                   make_codes_map(&map, codes, (long long)B * n_cap);
-      score_fp4_kernel<<<unsigned(rows * sa.n_chunks), SU_T, SU_SMEM, st>>>(sa, map);
+                   make_codes_map(&map1, codes, (long long)B * n_cap, 1) &&
+                   make_codes_map(&map4, codes, (long long)B * n_cap, 4);
+      if (sa.total_steps > 0) {
+        q_prep_kernel<<<unsigned(rows * 32), 128, 0, st>>>(sa, qprep, prefix);
+        const long long grid = sa.total_steps < slots[dev] ? sa.total_steps : slots[dev];
+        score_fp4_kernel<<<unsigned(grid), SU_T, SU_SMEM, st>>>(sa, map1, map4);
+      }
     } else {
       score_kernel<<<unsigned(rows * sa.n_chunks), SC_T, 0, st>>>(sa);
     }
