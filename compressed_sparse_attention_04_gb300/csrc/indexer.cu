@@ -24,6 +24,7 @@
 //   topk_kernel    one CTA per query row: radix select (select.cuh).
 //   hsi_kernel     one CTA per query row: top-nb blocks with the newest block forced.
 #include <cuda.h>
+#include <algorithm>
 #include <cstring>
 
 #include "common.cuh"
@@ -55,6 +56,8 @@ struct ScoreArgs {
   const uint8_t* qprep;    // [rows][SU_QROW_BYTES] FP4 query images (tensor-core path)
   const int* prefix;       // [Tq + 1] exclusive prefix of the steps per query index
   long long total_steps;   // B * prefix[Tq]
+  float* bm64;             // [rows][nb64] maxima of 64-key blocks for the top-k threshold, or null
+  int nb64;
 };
 
 __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
@@ -519,6 +522,13 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
           if (lane == 0 && bi < a.n_blocks) a.blockmax[size_t(row) * a.n_blocks + bi] = mx;
         }
       }
+      if (a.bm64) {   // maxima of this warp's 64 keys: a lower bound for the k-th score
+        float mx = fmaxf(score[0], score[1]);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const int bi = ce.st * (SU_STEP / 64) + q;
+        if (lane == 0 && bi < a.nb64) a.bm64[size_t(row) * a.nb64 + bi] = mx;
+      }
     }
   } else if (warp == 8 && lane == 0) {
     // ---------------- MMA issuer: per step two tiles x two K = 64 block-scaled MMAs
@@ -620,6 +630,25 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
 constexpr int TK_T = 512;
 constexpr int TK_SMEM_KEYS = 32768;   // rows up to this length are staged in shared memory
 
+// Stage n words into shared memory with eight loads in flight per thread: the loads are
+// unconditional (index clamped to n - 1) so that none waits behind a branch on another's
+// value.  src[j] is converted by conv(raw) after all eight have been issued.
+template <class T, class Conv>
+__device__ __forceinline__ void stage_keys(int n, unsigned* dst, const T* src, Conv conv) {
+  for (int base = 0; base < n; base += 8 * TK_T) {
+    T v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = src[min(base + u * TK_T + int(threadIdx.x), n - 1)];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = base + u * TK_T + int(threadIdx.x);
+      if (j < n) dst[j] = conv(v[u]);
+    }
+  }
+  __syncthreads();
+}
+__device__ __forceinline__ unsigned score_key(float f) { return (f == -INFINITY) ? 0u : f32_key(f); }
+
 struct TopkArgs {
   const float* scores;
   int row_len, Tq, q_pos0, m, n_entries;
@@ -637,18 +666,8 @@ __global__ void __launch_bounds__(TK_T) topk_kernel(TopkArgs a) {
   const int n = pool ? a.row_len : n_visible(t, a.m, a.n_entries);
   const float* srow = a.scores + size_t(row) * a.row_len;
   const bool staged = n <= TK_SMEM_KEYS;
-  if (staged) {
-    for (int j = threadIdx.x; j < n; j += TK_T) {
-      const float f = srow[j];
-      keys_sm[j] = (f == -INFINITY) ? 0u : f32_key(f);
-    }
-    __syncthreads();
-  }
-  auto key_of = [&](int j) -> unsigned {
-    if (staged) return keys_sm[j];
-    const float f = srow[j];
-    return (f == -INFINITY) ? 0u : f32_key(f);
-  };
+  if (staged) stage_keys(n, keys_sm, srow, score_key);
+  auto key_of = [&](int j) -> unsigned { return staged ? keys_sm[j] : score_key(srow[j]); };
   int32_t* orow = a.out + size_t(row) * a.k;
   const int32_t* crow = pool ? a.cand + size_t(row) * a.nb : nullptr;
   auto emit = [&](int pos, int j) {
@@ -670,7 +689,170 @@ struct TopkChunkArgs {
   int n_chunks;
   unsigned* cand_keys;   // [rows][n_chunks][k]
   int32_t* cand_pos;     // [rows][n_chunks][k]
+  const unsigned* tau;   // [rows] keys below tau cannot be among the top k (or null)
 };
+
+// Threshold from the 64-key block maxima: the k-th largest block maximum is at most the
+// k-th largest score (k blocks hold a key at least that large), so keys below it can be
+// dropped before selecting.  All competing keys pass when fewer than k blocks compete.
+constexpr int TAU_SMEM_BLOCKS = 8192;   // rows of up to 512 Ki entries stage their maxima
+__global__ void __launch_bounds__(TK_T) topk_tau_kernel(TopkArgs a, const float* bm64, int nb64,
+                                                        unsigned* tau, unsigned* count) {
+  extern __shared__ unsigned bkeys[];
+  __shared__ SelectSmem sm;
+  const int row = blockIdx.x, i = row % a.Tq;
+  const int n_vis = n_visible((long long)a.q_pos0 + i, a.m, a.n_entries);
+  const int nb = (n_vis + 63) / 64;
+  const float* brow = bm64 + size_t(row) * nb64;
+  const bool staged = nb64 <= TAU_SMEM_BLOCKS;   // (the launch's shared memory holds nb64 keys)
+  if (staged) stage_keys(nb, bkeys, brow, score_key);
+  auto key_of = [&](int j) -> unsigned { return staged ? bkeys[j] : score_key(brow[j]); };
+  int n_valid, k_rem;
+  const unsigned kth = radix_kth<TK_T>(nb, a.k, key_of, sm, n_valid, k_rem);
+  if (threadIdx.x == 0) {
+    tau[row] = n_valid > a.k ? kth : 1u;
+    if (count) count[row] = 0u;
+  }
+}
+
+// Long dense rows, pass 1: every visible key at or above the row's threshold is appended
+// to the row's candidate list (slot position and key; order of arrival).  A CTA gathers
+// its candidates in shared memory and reserves room in the row's list with one atomic.
+constexpr int FT_T = 256, FT_SEG = 8192, FT_CAP = 16384, FT_LOCAL = 2048;
+struct FilterArgs {
+  TopkArgs a;
+  const unsigned* tau;
+  unsigned* count;      // [rows] candidates found (may exceed cap)
+  unsigned* ckey;       // [rows][cap]
+  int32_t* cpos;        // [rows][cap]
+  int cap, n_seg;
+};
+__global__ void __launch_bounds__(FT_T) topk_filter_kernel(FilterArgs f) {
+  __shared__ unsigned lkey[FT_LOCAL];
+  __shared__ int32_t lpos[FT_LOCAL];
+  __shared__ unsigned n_local, base_sm;
+  const TopkArgs& a = f.a;
+  const int row = blockIdx.x / f.n_seg, seg = blockIdx.x % f.n_seg, i = row % a.Tq;
+  const int n_row = n_visible((long long)a.q_pos0 + i, a.m, a.n_entries);
+  const int p0 = seg * FT_SEG;
+  if (p0 >= n_row) return;   // uniform
+  const unsigned thr = f.tau[row];
+  const float* srow = a.scores + size_t(row) * a.row_len;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) n_local = 0u;
+  __syncthreads();
+  const int p_end = min(p0 + FT_SEG, n_row);
+  for (int base = p0; base < p_end; base += 8 * FT_T) {
+    float v[8];   // unconditional loads (clamped index): all eight in flight at once
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = srow[min(base + u * FT_T + int(threadIdx.x), p_end - 1)];
+    unsigned key[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) key[u] = base + u * FT_T + int(threadIdx.x) < p_end ? score_key(v[u]) : 0u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool sel = key[u] >= thr && key[u] != 0u;
+      const unsigned mask = __ballot_sync(0xffffffffu, sel);
+      if (mask == 0u) continue;
+      const int leader = __ffs(mask) - 1;
+      unsigned at = 0;
+      if (lane == leader) at = atomicAdd(&n_local, unsigned(__popc(mask)));
+      at = __shfl_sync(0xffffffffu, at, leader) + unsigned(__popc(mask & ((1u << lane) - 1u)));
+      const int p = base + u * FT_T + int(threadIdx.x);
+      if (sel) {
+        if (at < unsigned(FT_LOCAL)) {
+          lkey[at] = key[u];
+          lpos[at] = p;
+        } else {   // more than the local list holds: straight into the row's list
+          const unsigned g = atomicAdd(&f.count[row], 1u);
+          if (g < unsigned(f.cap)) {
+            f.ckey[size_t(row) * f.cap + g] = key[u];
+            f.cpos[size_t(row) * f.cap + g] = p;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const unsigned n_loc = min(n_local, unsigned(FT_LOCAL));
+  if (n_loc == 0u) return;   // uniform
+  if (threadIdx.x == 0) base_sm = atomicAdd(&f.count[row], n_loc);
+  __syncthreads();
+  const unsigned b0 = base_sm;
+  for (unsigned j = threadIdx.x; j < n_loc; j += FT_T) {
+    if (b0 + j < unsigned(f.cap)) {
+      f.ckey[size_t(row) * f.cap + b0 + j] = lkey[j];
+      f.cpos[size_t(row) * f.cap + b0 + j] = lpos[j];
+    }
+  }
+}
+
+// Pass 2, one CTA per row: the exact top k of the candidates (larger key first, lower
+// position first among equal keys), emitted in ascending position order.  A row whose
+// candidates overflowed the list is selected from its full score row instead.
+__global__ void __launch_bounds__(TK_T) topk_final_kernel(FilterArgs f) {
+  extern __shared__ unsigned fsm[];   // keys [cap] | positions [cap] | selected [k pow2]
+  __shared__ SelectSmem sm;
+  __shared__ unsigned n_sel_sm;
+  const TopkArgs& a = f.a;
+  const int row = blockIdx.x, i = row % a.Tq, tid = threadIdx.x;
+  const int n_row = n_visible((long long)a.q_pos0 + i, a.m, a.n_entries);
+  const unsigned thr = f.tau[row];
+  int32_t* orow = a.out + size_t(row) * a.k;
+  const unsigned c = f.count[row];
+  if (c > unsigned(f.cap)) {   // overflow: the whole row (from global memory)
+    const float* srow = a.scores + size_t(row) * a.row_len;
+    auto key_of = [&](int j) -> unsigned {
+      const unsigned key = score_key(srow[j]);
+      return key >= thr ? key : 0u;
+    };
+    auto emit = [&](int pos, int j) { orow[pos] = j; };
+    radix_topk<TK_T>(n_row, a.k, key_of, emit, sm);
+    return;
+  }
+  const int n = int(c);
+  unsigned* keys = fsm;
+  int32_t* pos = reinterpret_cast<int32_t*>(fsm + f.cap);
+  int32_t* sel = reinterpret_cast<int32_t*>(fsm + 2 * f.cap);
+  const unsigned* gk = f.ckey + size_t(row) * f.cap;
+  const int32_t* gp = f.cpos + size_t(row) * f.cap;
+  stage_keys(n, keys, gk, [](unsigned x) { return x; });
+  stage_keys(n, reinterpret_cast<unsigned*>(pos), gp, [](int32_t x) { return unsigned(x); });
+  int n_valid, k_rem;
+  const unsigned kth = radix_kth<TK_T>(n, a.k, [&](int j) { return keys[j]; }, sm, n_valid, k_rem);
+  // ties at kth: the k_rem lowest positions (key ~pos orders them)
+  unsigned pkth = 0u;
+  if (n_valid > a.k) {
+    int nv2, kr2;
+    pkth = radix_kth<TK_T>(n, k_rem, [&](int j) { return keys[j] == kth ? ~unsigned(pos[j]) : 0u; },
+                           sm, nv2, kr2);
+  }
+  if (tid == 0) n_sel_sm = 0u;
+  __syncthreads();
+  for (int j = tid; j < n; j += TK_T) {
+    const unsigned key = keys[j];
+    const bool take = n_valid <= a.k || key > kth || (key == kth && ~unsigned(pos[j]) >= pkth);
+    if (take) sel[atomicAdd(&n_sel_sm, 1u)] = pos[j];
+  }
+  __syncthreads();
+  const int n_sel = int(n_sel_sm);
+  int P = 1;
+  while (P < n_sel) P <<= 1;
+  for (int j = n_sel + tid; j < P; j += TK_T) sel[j] = 0x7FFFFFFF;
+  __syncthreads();
+  for (int len = 2; len <= P; len <<= 1) {   // bitonic sort, ascending
+    for (int d = len >> 1; d > 0; d >>= 1) {
+      for (int t = tid; t < P / 2; t += TK_T) {
+        const int lo = (t / d) * 2 * d + (t % d), hi = lo + d;
+        const bool up = (lo & len) == 0;
+        const int x = sel[lo], y = sel[hi];
+        if ((x > y) == up) { sel[lo] = y; sel[hi] = x; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int j = tid; j < a.k; j += TK_T) orow[j] = j < n_sel ? sel[j] : -1;
+}
 
 __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
   extern __shared__ unsigned keys_sm[];
@@ -682,11 +864,11 @@ __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
   const int p0 = ch * TK_CHUNK;
   const int n = max(0, min(TK_CHUNK, n_row - p0));
   const float* srow = a.scores + size_t(row) * a.row_len + p0;
-  for (int j = threadIdx.x; j < n; j += TK_T) {
-    const float f = srow[j];
-    keys_sm[j] = (f == -INFINITY) ? 0u : f32_key(f);
-  }
-  __syncthreads();
+  const unsigned thr = c.tau ? c.tau[row] : 1u;
+  stage_keys(n, keys_sm, srow, [&](float f) {
+    const unsigned key = score_key(f);
+    return key >= thr ? key : 0u;
+  });
   unsigned* ck = c.cand_keys + (size_t(row) * c.n_chunks + ch) * a.k;
   int32_t* cp = c.cand_pos + (size_t(row) * c.n_chunks + ch) * a.k;
   auto key_of = [&](int j) -> unsigned { return keys_sm[j]; };
@@ -706,10 +888,7 @@ __global__ void __launch_bounds__(TK_T) topk_merge_kernel(TopkChunkArgs c) {
   const unsigned* ck = c.cand_keys + size_t(row) * n;
   const int32_t* cp = c.cand_pos + size_t(row) * n;
   const bool staged = n <= TK_SMEM_KEYS;
-  if (staged) {
-    for (int j = threadIdx.x; j < n; j += TK_T) keys_sm[j] = ck[j];
-    __syncthreads();
-  }
+  if (staged) stage_keys(n, keys_sm, ck, [](unsigned x) { return x; });
   auto key_of = [&](int j) -> unsigned { return staged ? keys_sm[j] : ck[j]; };
   int32_t* orow = a.out + size_t(row) * a.k;
   const int32_t* crow = a.cand ? a.cand + size_t(row) * a.nb : nullptr;
@@ -731,6 +910,7 @@ struct HsiArgs {
 };
 
 __global__ void __launch_bounds__(TK_T) hsi_kernel(HsiArgs a) {
+  extern __shared__ unsigned bkeys[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
   const long long t = (long long)a.q_pos0 + i;
@@ -738,10 +918,11 @@ __global__ void __launch_bounds__(TK_T) hsi_kernel(HsiArgs a) {
   const int nb_vis = (n_vis + a.blk - 1) / a.blk;
   const int forced = n_vis > 0 ? (n_vis - 1) / a.blk : -1;
   const float* brow = a.blockmax + size_t(row) * a.n_blocks;
+  const bool staged = a.n_blocks <= TAU_SMEM_BLOCKS;   // (the launch's shared memory)
+  if (staged) stage_keys(nb_vis, bkeys, brow, score_key);
   auto key_of = [&](int j) -> unsigned {
     if (j == forced) return 0xFFFFFFFFu;
-    const float f = brow[j];
-    return (f == -INFINITY) ? 0u : f32_key(f);
+    return staged ? bkeys[j] : score_key(brow[j]);
   };
   int32_t* orow = a.out + size_t(row) * a.nb;
   auto emit = [&](int pos, int j) { orow[pos] = j; };
@@ -760,9 +941,11 @@ size_t csa2_indexer_workspace_size(int B, int Tq, int n_entries, int nb, int blk
   const long long row_len = with_cand ? (long long)nb * blk : n_entries;
   if (row_len <= 0) return 0;
   size_t bytes = align_up(size_t(B) * Tq * size_t(row_len) * sizeof(float), 256);
-  if (row_len > TK_SMEM_KEYS) {   // candidate lists of the chunked selection
-    const size_t n_chunks = size_t((row_len + TK_CHUNK - 1) / TK_CHUNK);
+  if (row_len > TK_SMEM_KEYS) {   // candidate lists of the chunked selection, block maxima,
+    const size_t n_chunks = size_t((row_len + TK_CHUNK - 1) / TK_CHUNK);   // thresholds
     bytes += 2 * align_up(size_t(B) * Tq * n_chunks * CSA2_MAX_TOPK * 4, 256);
+    bytes += align_up(size_t(B) * Tq * size_t((row_len + 63) / 64) * 4, 256) +
+             2 * align_up(size_t(B) * Tq * 4, 256);
   }
   // FP4 query images and the step prefix table of the tensor-core scorer
   bytes += align_up(size_t(B) * Tq * SU_QROW_BYTES, 256) + align_up(size_t(Tq + 1) * 4, 256);
@@ -850,20 +1033,38 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   const size_t cand_bytes = chunked ? align_up(size_t(rows) * n_chunks_tk * CSA2_MAX_TOPK * 4, 256) : 0;
   const size_t qprep_bytes = align_up(size_t(rows) * SU_QROW_BYTES, 256);
   const size_t prefix_bytes = align_up(size_t(Tq + 1) * 4, 256);
-  const size_t need = (scores_out ? 0 : scores_bytes) + 2 * cand_bytes + qprep_bytes + prefix_bytes;
+  const int nb64 = int((row_len + 63) / 64);
+  const size_t bm64_bytes = chunked ? align_up(size_t(rows) * nb64 * 4, 256) : 0;
+  const size_t tau_bytes = chunked ? 2 * align_up(size_t(rows) * 4, 256) : 0;   // + counts
+  const size_t need = (scores_out ? 0 : scores_bytes) + 2 * cand_bytes + qprep_bytes + prefix_bytes +
+                      bm64_bytes + tau_bytes;
   if (!workspace || ws_bytes < need || !aligned256(workspace))
     return fail(CSA2_ERR_WORKSPACE, "indexer: workspace needs %zu bytes, 256-aligned", need);
   float* scores = scores_out ? scores_out : static_cast<float*>(workspace);
   char* cand_area = static_cast<char*>(workspace) + (scores_out ? 0 : scores_bytes);
   uint8_t* qprep = reinterpret_cast<uint8_t*>(cand_area + 2 * cand_bytes);
   int* prefix = reinterpret_cast<int*>(qprep + qprep_bytes);
+  float* bm64_ws = reinterpret_cast<float*>(reinterpret_cast<char*>(prefix) + prefix_bytes);
+  unsigned* tau = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(bm64_ws) + bm64_bytes);
+  unsigned* cand_count = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(tau) + tau_bytes / 2);
+  // long dense rows: a threshold from the 64-key block maxima prunes the chunked selection;
+  // the maxima are the caller's block maxima when those are 64-key blocks
+  const float* bm64_src = nullptr;
   cudaStream_t st = (cudaStream_t)stream;
   const int n_blocks = (cand || blockmax_out) ? ceil_div(n_entries, blk) : 0;
   if (row_len > 0) {
     ScoreArgs sa{(const uint16_t*)q_idx, w, int(rows), Tq, q_pos0, codes, scales, n_cap,
                  n_entries, m, cand, nb, blk, n_blocks, scores, int(row_len), blockmax_out,
-                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0, qprep, prefix, 0};
+                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0, qprep, prefix, 0, nullptr, nb64};
     const bool umma_ok = !(cand || blockmax_out) || blk <= 64;
+    if (umma_ok && chunked && !cand) {
+      if (blockmax_out && blk == 64) {
+        bm64_src = blockmax_out;
+      } else {
+        sa.bm64 = bm64_ws;
+        bm64_src = bm64_ws;
+      }
+    }
     if (umma_ok) {
       long long per_seq = 0;   // steps of one sequence's Tq rows (same formula as the device)
       for (int i = 0; i < Tq; ++i)
@@ -916,8 +1117,26 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
     if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
     topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
   } else {
+    if (bm64_src) {
+      // threshold from the block maxima, one filtering pass, one exact select per row
+      const int cap = int(std::min<long long>((long long)n_chunks_tk * CSA2_MAX_TOPK, FT_CAP));
+      FilterArgs fa{ta, tau, cand_count, reinterpret_cast<unsigned*>(cand_area),
+                    reinterpret_cast<int32_t*>(cand_area + cand_bytes), cap,
+                    int((row_len + FT_SEG - 1) / FT_SEG)};
+      const size_t fsm = (2 * size_t(cap) + CSA2_MAX_TOPK) * 4;
+      cudaError_t e0 = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            int(fsm));
+      if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
+      topk_tau_kernel<<<unsigned(rows), TK_T, size_t(nb64 <= TAU_SMEM_BLOCKS ? nb64 : 0) * 4, st>>>(
+          ta, bm64_src, nb64, tau, cand_count);
+      topk_filter_kernel<<<unsigned(rows * fa.n_seg), FT_T, 0, st>>>(fa);
+      topk_final_kernel<<<unsigned(rows), TK_T, fsm, st>>>(fa);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+      return CSA2_OK;
+    }
     TopkChunkArgs tc{ta, int(n_chunks_tk), reinterpret_cast<unsigned*>(cand_area),
-                     reinterpret_cast<int32_t*>(cand_area + cand_bytes)};
+                     reinterpret_cast<int32_t*>(cand_area + cand_bytes), nullptr};
     cudaError_t e0 = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           TK_SMEM_KEYS * 4);
     if (e0 == cudaSuccess)
@@ -947,7 +1166,8 @@ int csa2_hsi_candidates(const float* blockmax, int B, int Tq, int q_pos0, int n_
   const long long rows = (long long)B * Tq;
   if (rows > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "hsi: too many rows");
   HsiArgs ha{blockmax, ceil_div(n_entries, blk), Tq, q_pos0, m, n_entries, blk, nb, cand_out};
-  hsi_kernel<<<unsigned(rows), TK_T, 0, (cudaStream_t)stream>>>(ha);
+  hsi_kernel<<<unsigned(rows), TK_T, size_t(ha.n_blocks <= TAU_SMEM_BLOCKS ? ha.n_blocks : 0) * 4,
+               (cudaStream_t)stream>>>(ha);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "hsi launch");
   return CSA2_OK;

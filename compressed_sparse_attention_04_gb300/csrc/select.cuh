@@ -53,10 +53,11 @@ struct SelectSmem {
   int found;           // bin index found by the scan (-1 = none yet)
 };
 
-// key_of(i) -> uint32 key (0 = not competing); emit(pos, i) writes output slot pos
-// (i = -1 for padding).  Returns min(k, #competing).
-template <int NT, class KeyFn, class EmitFn>
-__device__ int radix_topk(int n, int k, KeyFn key_of, EmitFn emit, SelectSmem& sm) {
+// The selection threshold: returns kth and sets n_valid (competing keys) and k_rem so that
+// the top-k are the keys > kth plus the first k_rem keys == kth.  When n_valid <= k every
+// competing key is taken (kth = 1, k_rem = 0).  kth is then the k-th largest key.
+template <int NT, class KeyFn>
+__device__ unsigned radix_kth(int n, int k, KeyFn key_of, SelectSmem& sm, int& n_valid, int& k_rem) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   // count competitors and their key range
   int cnt = 0;
@@ -75,10 +76,9 @@ __device__ int radix_topk(int n, int k, KeyFn key_of, EmitFn emit, SelectSmem& s
     kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
   }
   if (lane == 0) { sm.red_min[wid] = kmin; sm.red_max[wid] = kmax; }
-  int n_valid;
   block_excl_scan<NT>(cnt, sm.scan, n_valid);   // (its barriers also publish red_min/max)
-  unsigned kth = 1u;   // select key > kth, plus k_rem keys == kth (first by position)
-  int k_rem = 0;
+  unsigned kth = 1u;
+  k_rem = 0;
   if (n_valid > k) {
     if (tid == 0) {
       unsigned mn = 0xFFFFFFFFu, mx = 0u;
@@ -132,6 +132,16 @@ __device__ int radix_topk(int n, int k, KeyFn key_of, EmitFn emit, SelectSmem& s
     kth = sm.prefix;
     k_rem = sm.k_rem;
   }
+  return kth;
+}
+
+// key_of(i) -> uint32 key (0 = not competing); emit(pos, i) writes output slot pos
+// (i = -1 for padding).  Returns min(k, #competing).
+template <int NT, class KeyFn, class EmitFn>
+__device__ int radix_topk(int n, int k, KeyFn key_of, EmitFn emit, SelectSmem& sm) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int n_valid, k_rem;
+  const unsigned kth = radix_kth<NT>(n, k, key_of, sm, n_valid, k_rem);
   // emission in position order: warp w owns the contiguous segment [w*seg, (w+1)*seg);
   // pass A counts its '>' and '==' keys, one block scan places the warps, pass B writes.
   constexpr int NW = NT / 32;

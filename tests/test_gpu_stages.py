@@ -187,6 +187,8 @@ def _oracle_scores(qi64, w64, codes, scales, n):
     (1, 1, 29999, 30000, 1, 512),     # row longer than the shared-memory staging
     (1, 300, 0, 150, 2, 64),          # causal prefill: early rows see fewer than k entries
     (2, 5, 2040, 2048, 1, 2048),      # k = 2048 (maximum)
+    (2, 1, 69999, 70000, 1, 512),     # chunked selection pruned by the caller's block maxima
+    (1, 3, 79997, 40000, 2, 2048),    # chunked, rows of different lengths, k = 2048
 ])
 def test_indexer_full_parity(B, Tq, q_pos0, n_entries, m, k):
     ops = _ops()
@@ -232,6 +234,51 @@ def test_indexer_non_staged_no_scores_out_uses_workspace():
     for b in range(B):
         so = _oracle_scores(qi64[b, 0], w64[b, 0], codes[b], scales[b], n_entries)
         Hp.check_topk_row(topk[b, 0], so, np.ones(n_entries, bool), k)
+
+
+def test_indexer_long_rows_with_32_key_blocks():
+    # block maxima of 32-key blocks: the top-k threshold uses its own 64-key maxima
+    ops = _ops()
+    B, Tq, n_entries, m, k, blk = 2, 2, 50000, 1, 256, 32
+    q_pos0 = n_entries - 2
+    qi, qi64, w, w64, codes, scales = _indexer_inputs(11, B, Tq, n_entries)
+    nblk = -(-n_entries // blk)
+    bmax = torch.empty(B, Tq, nblk, dtype=torch.float32, device="cuda")
+    topk = ops.indexer_score_topk(qi, w, q_pos0, Hp.to_dev(codes, torch.uint8),
+                                  Hp.to_dev(scales, torch.uint8), n_entries, m, k, blk=blk,
+                                  blockmax_out=bmax)
+    torch.cuda.synchronize()
+    _ok()
+    topk, bmax = topk.cpu().numpy(), bmax.cpu().numpy()
+    for b in range(B):
+        for i in range(Tq):
+            nv = R.n_visible(q_pos0 + i, m, n_entries)
+            so = _oracle_scores(qi64[b, i], w64[b, i], codes[b], scales[b], nv)
+            Hp.check_topk_row(topk[b, i], so, np.ones(nv, bool), k, f"row {b},{i}")
+            bm_o = R.block_max(so, nv, blk)
+            np.testing.assert_allclose(bmax[b, i, :len(bm_o)], bm_o, rtol=1e-5,
+                                       atol=1e-5 * max(np.max(np.abs(so)), 1e-3))
+
+
+def test_indexer_long_rows_all_tied_take_the_lowest_positions():
+    # identical keys: every score ties, so the threshold admits the whole row (more
+    # candidates than the list holds) and the selection must return positions 0 .. k-1
+    ops = _ops()
+    B, n_entries, k = 2, 40000, 512
+    qi, qi64, w, w64, codes, scales = _indexer_inputs(17, B, 1, n_entries)
+    codes[:] = codes[:, :1]
+    scales[:] = scales[:, :1]
+    bmax = torch.empty(B, 1, -(-n_entries // 64), dtype=torch.float32, device="cuda")
+    topk = ops.indexer_score_topk(qi, w, n_entries - 1, Hp.to_dev(codes, torch.uint8),
+                                  Hp.to_dev(scales, torch.uint8), n_entries, 1, k, blk=64,
+                                  blockmax_out=bmax)
+    torch.cuda.synchronize()
+    _ok()
+    topk = topk.cpu().numpy()
+    for b in range(B):
+        so = _oracle_scores(qi64[b, 0], w64[b, 0], codes[b], scales[b], n_entries)
+        assert np.all(so == so[0])
+        np.testing.assert_array_equal(topk[b, 0], np.arange(k))
 
 
 def _cand_input(seed, B, Tq, n_blocks, nb, n_vis):
