@@ -44,6 +44,7 @@ SIGNATURES = {
     "csa2_status_str": (C.c_char_p, [i32]),
     "csa2_last_error_message": (C.c_char_p, []),
     "csa2_version": (C.c_char_p, []),
+    "csa2_kernel_launches": (C.c_ulonglong, []),
     "csa2_last_device_status": (i32, [vp]),
     "csa2_compress_workspace_size": (sz, [i32, i32, i32, i32]),
     "csa2_compress": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, vp, f32, f32, vp, i32, vp,

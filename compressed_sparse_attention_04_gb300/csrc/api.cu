@@ -1,4 +1,5 @@
 // Status strings, per-thread error messages and the device error word readers.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -7,6 +8,9 @@
 #include "common.cuh"
 
 namespace csa2 {
+
+std::atomic<unsigned long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 namespace {
 thread_local char g_msg[512] = "";
@@ -54,6 +58,8 @@ const char* csa2_status_str(int s) {
 const char* csa2_last_error_message(void) { return csa2::g_msg; }
 
 const char* csa2_version(void) { return "csa2-gb300 0.1 (sm_103a)"; }
+
+unsigned long long csa2_kernel_launches(void) { return csa2::g_launches.load(); }
 
 int csa2_last_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -499,9 +499,12 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
                                           int(AU_SMEM));
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: shared memory attribute");
     attn_umma_kernel<<<unsigned(rows * n_tiles), AU_T, AU_SMEM, st>>>(ua);
+    note_launch();
     attn_combine_kernel<<<unsigned(rows * (AU_H / AC_HG)), 128, 0, st>>>(ua);
+    note_launch();
   } else {
     attn_simt_kernel<<<unsigned(rows * n_hg), AT_T, 0, st>>>(aa);
+    note_launch();
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse_attn launch");

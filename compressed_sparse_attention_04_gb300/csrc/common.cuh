@@ -15,6 +15,8 @@ namespace csa2 {
 // ------------------------------------------------------------------ host side
 // Records a one-line reason for the calling thread and returns `status`.
 int fail(int status, const char* fmt, ...);
+// Counts one kernel launch (csa2_kernel_launches reads the total).
+void note_launch();
 int cuda_fail(cudaError_t e, const char* what);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

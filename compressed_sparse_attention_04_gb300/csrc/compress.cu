@@ -388,14 +388,17 @@ int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, cons
     proj_umma_kernel<<<grid, PU_T, PU_SMEM, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
                                                   (const uint16_t*)w_gate, M, hidden, nout,
                                                   hidden / splits, P);
+    note_launch();
   } else {
     dim3 grid(nout / GN, ceil_div(M, GM));
     proj_gemm_kernel<<<grid, GT, 0, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
                                           (const uint16_t*)w_gate, M, hidden, nout, P);
+    note_launch();
   }
   compress_epilogue_kernel<<<B * G, 128, 0, st>>>(P, splits, size_t(M) * nout, nout, B, T, m, pos0,
                                                    G, norm_w, eps, rope_base, (uint16_t*)kv_cache,
                                                    n_cap, kv_pre);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return CSA2_OK;
@@ -419,6 +422,7 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, con
   const int total = B * G;
   index_k_kernel<<<ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream>>>(
       kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_k_quant launch");
   return CSA2_OK;

@@ -1100,11 +1100,14 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                    make_codes_map(&map4, codes, (long long)B * n_cap, 4);
       if (sa.total_steps > 0) {
         q_prep_kernel<<<unsigned(rows * 32), 128, 0, st>>>(sa, qprep, prefix);
+        note_launch();
         const long long grid = sa.total_steps < slots[dev] ? sa.total_steps : slots[dev];
         score_fp4_kernel<<<unsigned(grid), SU_T, SU_SMEM, st>>>(sa, map1, map4);
+        note_launch();
       }
     } else {
       score_kernel<<<unsigned(rows * sa.n_chunks), SC_T, 0, st>>>(sa);
+      note_launch();
     }
   }
   if (ev_score_end) cudaEventRecord(ev_score_end, st);
@@ -1116,6 +1119,7 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                                           TK_SMEM_KEYS * 4);
     if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
     topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
+    note_launch();
   } else {
     if (bm64_src) {
       // threshold from the block maxima, one filtering pass, one exact select per row
@@ -1129,8 +1133,11 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
       if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
       topk_tau_kernel<<<unsigned(rows), TK_T, size_t(nb64 <= TAU_SMEM_BLOCKS ? nb64 : 0) * 4, st>>>(
           ta, bm64_src, nb64, tau, cand_count);
+      note_launch();
       topk_filter_kernel<<<unsigned(rows * fa.n_seg), FT_T, 0, st>>>(fa);
+      note_launch();
       topk_final_kernel<<<unsigned(rows), TK_T, fsm, st>>>(fa);
+      note_launch();
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
       return CSA2_OK;
@@ -1145,8 +1152,10 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
     if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
     if (rows * (long long)n_chunks_tk > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "indexer: too many rows");
     topk_chunk_kernel<<<unsigned(rows * n_chunks_tk), TK_T, size_t(TK_CHUNK) * 4, st>>>(tc);
+    note_launch();
     const long long n_merge = (long long)n_chunks_tk * k;
     topk_merge_kernel<<<unsigned(rows), TK_T, size_t(n_merge <= TK_SMEM_KEYS ? n_merge : 0) * 4, st>>>(tc);
+    note_launch();
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
@@ -1168,6 +1177,7 @@ int csa2_hsi_candidates(const float* blockmax, int B, int Tq, int q_pos0, int n_
   HsiArgs ha{blockmax, ceil_div(n_entries, blk), Tq, q_pos0, m, n_entries, blk, nb, cand_out};
   hsi_kernel<<<unsigned(rows), TK_T, size_t(ha.n_blocks <= TAU_SMEM_BLOCKS ? ha.n_blocks : 0) * 4,
                (cudaStream_t)stream>>>(ha);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "hsi launch");
   return CSA2_OK;

@@ -61,6 +61,10 @@ const char* csa2_status_str(int status);
 const char* csa2_last_error_message(void);
 /* Library version string. */
 const char* csa2_version(void);
+/* Number of GPU kernels this library has launched in this process so far (all entry
+ * points, all devices; a monotone counter for instrumentation -- the difference across
+ * a region is the launch count of that region).  No counterpart in the method. */
+unsigned long long csa2_kernel_launches(void);
 
 /* Synchronises `stream`, then reads and clears the device error word of the current
  * device.  Returns CSA2_OK, CSA2_ERR_DEVICE_CHECK, CSA2_ERR_TIMEOUT or CSA2_ERR_CUDA. */
