@@ -8,18 +8,22 @@
 // [P3] "DeepSeek-V4.1-Flash：把百万 Token 的记忆，压缩成一套分级缓存" (junki.cn), §四:
 //      p_j = softmax_j(c_j . q / sqrt d), o = sum_j p_j c_j.
 //
-// attn_umma_kernel (64 heads): one CTA per (query row, tile of 128 rows of A).  The rows
-// are gathered with 16-byte asynchronous copies into a K-major 128-byte-swizzled tile;
-// tcgen05 computes S^T = C Q^T (128 rows x 64 heads, K = 512) into TMEM; each head's
-// softmax over the tile's rows gives (max, sum) and P^T (bf16, MN-major); tcgen05 then
-// computes O^T = C^T P^T (512 dims x 64 heads, K = 128 rows) reading the SAME shared
-// tile as an MN-major operand (K = V).  attn_combine_kernel merges the per-tile
-// (max, sum, O) partials of a row into the normalised output.
+// attn_flash_kernel (64 heads): a cluster of 1-4 CTAs per query row splits the row's
+// attended list into chunks of 64 rows; each CTA streams its chunks through a two-slot
+// ring (16-byte asynchronous gathers into a K-major 128-byte-swizzled tile), tcgen05
+// computes S = Q C^T (64 heads x 64 rows, K = 512) so that one thread owns one head's
+// scores, an online softmax writes P^T (bf16), and tcgen05 accumulates O^T = C^T P^T
+// (512 dims x 64 heads) in TMEM, reading the SAME shared tile as the MN-major operand
+// (K = V).  The CTAs of a cluster combine their (max, sum, O) through distributed shared
+// memory; nothing intermediate goes to global memory.
 //
 // attn_simt_kernel (any H): one CTA per (query row, group of 8 heads), one warp per head.
 // Rows of A (top-k slots then window rows) stream through shared memory in tiles of
 // 32; lane j scores row j of the tile; an online softmax keeps (max, sum) per head
 // and every lane accumulates 16 of the 512 output dims.
+#include <algorithm>
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -172,269 +176,412 @@ __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
 }
 
 
-constexpr int AU_T = 256;            // threads
-constexpr int AU_ROWS = 128;         // rows of A per CTA (M of the first MMA)
-constexpr int AU_H = 64;             // heads (N of both MMAs)
-constexpr uint32_t AU_KV_BYTES = AU_ROWS * 512 * 2;    // 128 KB
-constexpr uint32_t AU_Q_BYTES = AU_H * 512 * 2;        // 64 KB (reused for S^T in f32)
-constexpr uint32_t AU_P_BYTES = AU_ROWS * AU_H * 2;    // 16 KB
-constexpr uint32_t AU_SMEM = AU_KV_BYTES + AU_Q_BYTES + AU_P_BYTES + 1024;
+// ---------------------------------------------------------------- pipelined tensor-core
+// attention (64 heads).  A row's attended list (top-k slots, then window rows) is cut into
+// chunks of 64 rows; the CTAs of one cluster take consecutive ranges of chunks and
+// merge their partial results through distributed shared memory.  Per chunk:
+//   S   = Q C^T     (M = 64 heads, N = 64 rows, K = 512)   -> TMEM, one head per lane,
+//                    so each head's softmax runs inside one thread;
+//   O^T += C^T P^T  (M = 4 x 128 dims, N = 64 heads, K = 64 rows) -> TMEM,
+// reading the SAME shared tile of C (K = V) as a K-major and an MN-major operand.
+// The running maximum is only moved when a chunk exceeds it by more than 2^8 (probabilities
+// then stay below 256, exact in float32 sums); moving it rescales that head's columns of
+// O^T in TMEM after the previous chunk's products have landed.
+constexpr int AF_CH = 64;                              // rows per chunk
+constexpr int AF_T = 288;                              // 4 copy + 4 softmax + 1 MMA warp
+constexpr uint32_t AF_KV_BYTES = AF_CH * 1024;         // 64 KB per ring slot
+constexpr uint32_t AF_Q_BYTES = 64 * 1024;
+constexpr uint32_t AF_P_BYTES = AF_CH * 64 * 2;        // 8 KB per P^T buffer
+constexpr uint32_t AF_SMEM = 2 * AF_KV_BYTES + AF_Q_BYTES + 2 * AF_P_BYTES + 1024;
+// S: 2 buffers x 2 K-halves x 64 columns (the two halves are independent accumulators so
+// that consecutive MMAs do not wait on each other); O^T: 4 x 64 columns
+constexpr uint32_t AF_S_COL = 0, AF_O_COL = 256;
+constexpr float AF_LAZY = 8.f;                         // log2 slack before the max moves
+constexpr int AF_MAX_SPLIT = 4;
 
-struct AttnUmmaArgs {
+struct AttnFlashArgs {
   AttnArgs a;
-  int n_tiles;
-  float* part_o;    // [rows][n_tiles][64][512]
-  float* part_ml;   // [rows][n_tiles][64][2]
+  int n_split;        // CTAs per row (cluster size)
 };
 
-__global__ void __launch_bounds__(AU_T, 1) attn_umma_kernel(AttnUmmaArgs u) {
+// Named barrier over n threads that also reduces a predicate (and / or) across them.
+__device__ __forceinline__ bool bar_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r) : "r"(uint32_t(v)), "r"(id), "r"(n) : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool bar_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+               "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+               : "=r"(r) : "r"(uint32_t(v)), "r"(id), "r"(n) : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
+  namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* KV = base;
-  uint8_t* Qs = base + AU_KV_BYTES;
-  float* Sbuf = reinterpret_cast<float*>(Qs);          // [64][128] after the first MMA
-  uint8_t* Ps = base + AU_KV_BYTES + AU_Q_BYTES;
-  __shared__ const uint16_t* row_src[AU_ROWS];
-  __shared__ int row_ok[AU_ROWS];
-  __shared__ __align__(8) uint64_t bar[2];
+  uint8_t* KV = base;                                   // 2 slots x 64 rows (K-major SW128)
+  uint8_t* Qs = base + 2 * AF_KV_BYTES;                 // 64 heads (K-major SW128)
+  uint8_t* Ps = Qs + AF_Q_BYTES;                        // 2 x P^T (64 rows x 64 heads, MN-major)
+  // after the last chunk: partial O^T tiles pushed by the cluster's CTAs to the tile's owner,
+  // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
+  float* Obuf = reinterpret_cast<float*>(KV);
+  __shared__ const uint16_t* row_src[2][AF_CH];
+  __shared__ unsigned long long row_mask[2];
+  __shared__ __align__(8) uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], o_ready;
   __shared__ uint32_t tmem_slot;
-  __shared__ int any_valid;
+  __shared__ float fac[64];                              // per-head factor (rescale / final)
+  __shared__ __align__(8) float ml_all[AF_MAX_SPLIT][64][2];   // every CTA's (max, sum), log2 units
 
   const AttnArgs& a = u.a;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = int(cluster.block_rank());
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = blockIdx.x / u.n_tiles, tile = blockIdx.x % u.n_tiles;
+  const int row = blockIdx.x / u.n_split;
   const int b = row / a.Tq, i = row % a.Tq;
   const long long t = (long long)a.q_pos0 + i;
   const long long lo = t - a.window + 1 > 0 ? t - a.window + 1 : 0;
   const int n_rows = a.k + int(t - lo + 1);
-  float* ml = u.part_ml + (size_t(row) * u.n_tiles + tile) * AU_H * 2;
+  const int n_ch_all = (n_rows + AF_CH - 1) / AF_CH;
+  const int c_begin = int((long long)n_ch_all * rank / u.n_split);
+  const int n_ch = int((long long)n_ch_all * (rank + 1) / u.n_split) - c_begin;
+  const float scale_log2 = a.scale * 1.4426950408889634f;
 
-  if (tid == 0) any_valid = 0;
-  __syncthreads();
-  if (tid < AU_ROWS) {
-    const int j = tile * AU_ROWS + tid;
-    int ok = 0;
-    const uint16_t* src = a.swa;   // any valid address for zero-filled copies
-    if (j < a.k) {
-      const int e = a.topk[size_t(row) * a.k + j];
-      if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
-      if (e >= 0 && e < a.n_entries) {
-        ok = 1;
-        src = a.kv + (size_t(b) * a.n_cap + e) * 512;
-      }
-    } else if (j < n_rows) {
-      ok = 1;
-      src = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
-    }
-    row_src[tid] = src;
-    row_ok[tid] = ok;
-    if (ok) atomicOr(&any_valid, 1);
-  }
-  __syncthreads();
-  if (!any_valid) {          // tile entirely past this row's set: empty partial
-    if (tid < AU_H) { ml[2 * tid] = -INFINITY; ml[2 * tid + 1] = 0.f; }
-    return;
-  }
   if (tid == 0) {
-    umma::mbar_init(&bar[0], 1);
-    umma::mbar_init(&bar[1], 1);
+    for (int s = 0; s < 2; ++s) {
+      umma::mbar_init(&kv_full[s], 128);
+      umma::mbar_init(&kv_empty[s], 1);
+      umma::mbar_init(&s_full[s], 1);
+      umma::mbar_init(&s_empty[s], 4);
+      umma::mbar_init(&p_full[s], 4);
+    }
+    umma::mbar_init(&o_ready, 1);
     umma::mbar_fence_init();
   }
   if (warp == 0) umma::tmem_alloc(&tmem_slot, 512);
-
-  // gather, one commit group per 64-dim atom column: 128 rows x 8 chunks of the KV tile
-  // and 64 heads x 8 chunks of the query block; the first MMA consumes atom a as soon
-  // as every thread's group a has landed.
-  const uint16_t* qrow = a.q + size_t(row) * a.H * 512;
-#pragma unroll 1
-  for (int at = 0; at < 8; ++at) {
-    for (int c = tid; c < AU_ROWS * 8; c += AU_T) {
-      const int r = c >> 3, ch = at * 8 + (c & 7);
-      umma::cp_async16(KV + umma::kmajor_sw128_offset(r, ch * 8, AU_ROWS), row_src[r] + ch * 8,
-                       row_ok[r] ? 16u : 0u);
-    }
-    for (int c = tid; c < AU_H * 8; c += AU_T) {
-      const int h = c >> 3, ch = at * 8 + (c & 7);
-      umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, AU_H), qrow + h * 512 + ch * 8, 16u);
-    }
-    umma::cp_async_commit();
-  }
-  uint32_t tmem = 0;
-  constexpr uint32_t idesc_s = umma::idesc_f16(AU_ROWS, AU_H, 1, 0, 0);
-  const uint32_t kv_base = umma::smem_u32(KV), q_base = umma::smem_u32(Qs);
-#pragma unroll
-  for (int at = 0; at < 8; ++at) {
-    umma::cp_async_wait_pending(7 - at);
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    umma::fence_after();
-    if (at == 0) tmem = tmem_slot;
-    // S^T = C Q^T over dims 64*at .. 64*at + 63 (4 steps of K = 16)
-    if (tid == 0) {
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const uint64_t da = umma::desc_sw128(kv_base + at * (AU_ROWS * 128) + k4 * 32, 16, 1024);
-        const uint64_t db = umma::desc_sw128(q_base + at * (AU_H * 128) + k4 * 32, 16, 1024);
-        umma::mma_f16(tmem, da, db, idesc_s, (at | k4) != 0);
-      }
-      if (at == 7) umma::commit(&bar[0]);
-    }
-  }
-  // logits are kept in base-2 units (scaled by log2 e) so the softmax uses exp2;
-  // (max, sum) partials are converted back to natural units for the combine.
-  const float scale_log2 = a.scale * 1.4426950408889634f;
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = tmem_slot;
   bool ok = true;
-  ok = umma::mbar_wait(&bar[0], 0, &d_err_attn);
-  umma::fence_after();
-  if (ok) {
-    const int q = warp & 3, half = warp >> 2;
-    const int r = q * 32 + lane;
-    const bool valid = row_ok[r] != 0;
-    uint32_t v[32];
-    umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(half * 32), v);
-    umma::tmem_ld_wait();
-#pragma unroll
-    for (int h = 0; h < 32; ++h)
-      Sbuf[(half * 32 + h) * AU_ROWS + r] = valid ? __uint_as_float(v[h]) * scale_log2 : -INFINITY;
-  }
-  umma::fence_before();
-  __syncthreads();
-  umma::fence_after();
+  float m_fin = -INFINITY, l_fin = 0.f;   // softmax lanes: this CTA's (max, sum) of their head
+  // announce that this CTA runs; the matching wait precedes the first remote access
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-  // softmax within the tile: warp w owns heads 8w .. 8w+7, lane owns rows lane + 32 j;
-  // P^T row r gets the 8 heads' probabilities as one 16-byte chunk.
-  {
-    const int h0 = warp * 8;
-    float p[4][8];
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh) {
-      const float* srow = Sbuf + (h0 + hh) * AU_ROWS + lane;
-      float v0 = srow[0], v1 = srow[32], v2 = srow[64], v3 = srow[96];
-      float m = fmaxf(fmaxf(v0, v1), fmaxf(v2, v3));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      const bool live = m != -INFINITY;
-      p[0][hh] = live ? exp2f(v0 - m) : 0.f;
-      p[1][hh] = live ? exp2f(v1 - m) : 0.f;
-      p[2][hh] = live ? exp2f(v2 - m) : 0.f;
-      p[3][hh] = live ? exp2f(v3 - m) : 0.f;
-      float l = (p[0][hh] + p[1][hh]) + (p[2][hh] + p[3][hh]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      if (lane == 0) { ml[2 * (h0 + hh)] = m * 0.6931471805599453f; ml[2 * (h0 + hh) + 1] = l; }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int r = lane + 32 * j;
-      uint32_t w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(p[j][2 * u], p[j][2 * u + 1]);
-        w[u] = *reinterpret_cast<uint32_t*>(&v2);
+  if (warp < 4) {
+    // ---------------- copy warps: chunk c of this CTA into slot c % 2 (and Q with chunk 0).
+    // Thread t < 64 holds the selected entry of row t of the next chunk, loaded one chunk
+    // ahead so that its latency overlaps the wait for a free slot.
+    auto topk_at = [&](int c) -> int {
+      const int j = (c_begin + c) * AF_CH + tid;
+      return (tid < AF_CH && c < n_ch && j < a.k) ? a.topk[size_t(row) * a.k + j] : -1;
+    };
+    int e_next = topk_at(0);
+    auto issue = [&](int c) {
+      if (c < n_ch) {
+        const int s = c & 1;
+        const int e = e_next;
+        e_next = topk_at(c + 1);
+        bool okw = c < 2 || umma::mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, &d_err_attn);
+        if (tid < AF_CH) {   // warps 0 and 1, whole warps (the ballot below needs every lane)
+          const int j = (c_begin + c) * AF_CH + tid;
+          int okr = 0;
+          const uint16_t* src = a.swa;   // any valid address for zero-filled copies
+          if (j < a.k) {
+            if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
+            if (e >= 0 && e < a.n_entries) { okr = 1; src = a.kv + (size_t(b) * a.n_cap + e) * 512; }
+          } else if (j < n_rows) {
+            okr = 1;
+            src = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
+          }
+          const unsigned m0 = __ballot_sync(0xffffffffu, okr);
+          if (okw) {
+            row_src[s][tid] = okr ? src : nullptr;
+            if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[warp] = m0;
+          }
+        }
+        // row sources ready; the copy warps agree on whether the slot wait succeeded
+        if (!bar_and(2, 128, okw)) return false;
+        uint8_t* dst = KV + s * AF_KV_BYTES;
+#pragma unroll 4
+        for (int rep = 0; rep < 32; ++rep) {
+          const int uidx = rep * 128 + tid, r = uidx >> 6, ch = uidx & 63;
+          const uint16_t* src = row_src[s][r];
+          umma::cp_async16(dst + umma::kmajor_sw128_offset(r, ch * 8, AF_CH),
+                           src ? src + ch * 8 : a.swa, src ? 16u : 0u);
+        }
+        if (c == 0) {
+          const uint16_t* qrow = a.q + size_t(row) * 64 * 512;
+#pragma unroll 4
+          for (int rep = 0; rep < 32; ++rep) {
+            const int uidx = rep * 128 + tid, h = uidx >> 6, ch = uidx & 63;
+            umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow + h * 512 + ch * 8, 16u);
+          }
+        }
       }
-      const uint32_t off = uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((warp ^ (r & 7)) << 4));
-      *reinterpret_cast<uint4*>(Ps + off) = make_uint4(w[0], w[1], w[2], w[3]);
+      umma::cp_async_commit();
+      return true;
+    };
+    // chunks 0 and 1 go out at once; chunk c + 1 is announced before this thread blocks on
+    // the products of chunk c, which free the slot for chunk c + 2
+    ok = issue(0) && issue(1);
+    if (ok && n_ch > 0) {
+      umma::cp_async_wait_pending(1);
+      umma::fence_proxy_async();
+      umma::mbar_arrive(&kv_full[0]);
     }
-  }
-  umma::fence_proxy_async();
-  umma::fence_before();
-  __syncthreads();
-  umma::fence_after();
-
-  // O^T = C^T P^T: four 128-dim tiles, 8 steps of K = 16 rows
-  if (tid == 0 && ok) {
-    constexpr uint32_t idesc = umma::idesc_f16(128, AU_H, 1, 1, 1);
-    const uint32_t kv0 = umma::smem_u32(KV), p0 = umma::smem_u32(Ps);
-    for (int dt = 0; dt < 4; ++dt)
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t da = umma::desc_sw128(kv0 + (2 * dt) * (AU_ROWS * 128) + kk * 2048,
-                                             AU_ROWS * 128, 1024);
-        const uint64_t db = umma::desc_sw128(p0 + kk * 2048, AU_ROWS * 128, 1024);
-        umma::mma_f16(tmem + 64 + 64 * dt, da, db, idesc, kk > 0);
+    for (int c = 0; c < n_ch && ok; ++c) {
+      if (c + 1 < n_ch) {
+        umma::cp_async_wait_pending(0);   // this thread's copies of chunk c + 1 landed
+        umma::fence_proxy_async();
+        umma::mbar_arrive(&kv_full[(c + 1) & 1]);
       }
-    umma::commit(&bar[1]);
-  }
-  if (ok) ok = umma::mbar_wait(&bar[1], 0, &d_err_attn);
-  umma::fence_after();
-  if (ok) {
-    const int q = warp & 3;
-    float* po = u.part_o + (size_t(row) * u.n_tiles + tile) * AU_H * 512;
-#pragma unroll 1
-    for (int dti = 0; dti < 2; ++dti) {
-      const int dt = (warp >> 2) * 2 + dti;
-      const int d = dt * 128 + q * 32 + lane;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(64 + 64 * dt + 32 * half), v);
+      ok = issue(c + 2);
+    }
+    umma::cp_async_wait_all();
+  } else if (warp < 8) {
+    // ---------------- softmax warps: warp q holds heads 16 q .. 16 q + 15 in lanes 0..15
+    const int q = warp & 3, h = 16 * q + (lane & 15);
+    const bool head_lane = lane < 16;
+    const uint32_t lane_addr = uint32_t(32 * q) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    for (int c = 0; c < n_ch && ok; ++c) {
+      const int s = c & 1;
+      bool okc = __all_sync(0xffffffffu, umma::mbar_wait(&s_full[s], (c >> 1) & 1, &d_err_attn));
+      if (!bar_and(1, 128, okc)) { ok = false; break; }
+      umma::fence_after();
+      float sv[64];
+      {
+        uint32_t v0[32], v1[32], w0[32], w1[32];
+        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s, v0);
+        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 32, v1);
+        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 64, w0);
+        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 96, w1);
         umma::tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) po[size_t(half * 32 + h) * 512 + d] = __uint_as_float(v[h]);
+        for (int j = 0; j < 32; ++j) {
+          sv[j] = __uint_as_float(v0[j]) + __uint_as_float(w0[j]);
+          sv[32 + j] = __uint_as_float(v1[j]) + __uint_as_float(w1[j]);
+        }
+      }
+      umma::fence_before();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&s_empty[s]);
+      const unsigned long long mask = row_mask[s];
+      float cmx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) cmx[u] = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        sv[j] = ((mask >> j) & 1ull) ? sv[j] * scale_log2 : -INFINITY;
+        cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
+      }
+      const float cm = fmaxf(fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3])),
+                             fmaxf(fmaxf(cmx[4], cmx[5]), fmaxf(cmx[6], cmx[7])));
+      // move the running max only when this chunk exceeds it by more than AF_LAZY
+      float f = 1.f;
+      if (cm > m_used + AF_LAZY || (m_used == -INFINITY && cm != -INFINITY)) {
+        f = m_used == -INFINITY ? 0.f : exp2f(m_used - cm);
+        m_used = cm;
+        l *= f;
+      }
+      float psx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) psx[u] = 0.f;
+      float p[64];
+      const float msub = m_used == -INFINITY ? INFINITY : m_used;   // all p = 0 before a valid row
+#pragma unroll
+      for (int j = 0; j < 64; ++j) {
+        p[j] = exp2f(sv[j] - msub);
+        psx[j & 7] += p[j];
+      }
+      l += ((psx[0] + psx[1]) + (psx[2] + psx[3])) + ((psx[4] + psx[5]) + (psx[6] + psx[7]));
+      // P^T buffer s is free once the products of chunk c - 2 have completed
+      bool okp = c < 2 || umma::mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, &d_err_attn);
+      if (!bar_and(1, 128, okp)) { ok = false; break; }
+      uint8_t* pb = Ps + s * AF_P_BYTES;
+      if (head_lane) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const uint32_t off = uint32_t((j >> 3) * 1024 + (j & 7) * 128 + (((h >> 3) ^ (j & 7)) << 4) + (h & 7) * 2);
+          *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(p[j]);
+        }
+      }
+      // heads whose max moved after products were accumulated: rescale their O^T columns
+      const bool need = head_lane && f != 1.f && c > 0;
+      if (head_lane) fac[h] = need ? f : 1.f;
+      if (bar_or(1, 128, need)) {
+        // the previous chunk's products must have landed in O^T first
+        const bool okr = __all_sync(0xffffffffu,
+                                    umma::mbar_wait(&kv_empty[(c - 1) & 1], ((c - 1) >> 1) & 1, &d_err_attn));
+        if (!bar_and(1, 128, okr)) { ok = false; break; }
+        umma::fence_after();
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          float fr[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) fr[x] = fac[32 * hf + x];
+#pragma unroll 1
+          for (int dt = 0; dt < 4; ++dt) {
+            uint32_t o[32];
+            const uint32_t addr = tmem + lane_addr + AF_O_COL + 64 * dt + 32 * hf;
+            umma::tmem_ld32(addr, o);
+            umma::tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * fr[x]);
+            umma::tmem_st32(addr, o);
+          }
+        }
+        umma::tmem_st_wait();
+      }
+      umma::fence_proxy_async();
+      umma::fence_before();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&p_full[s]);
+    }
+    m_fin = m_used;
+    l_fin = l;
+  } else if (warp == 8 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc_s = umma::idesc_f16(64, 64, 1, 0, 0);
+    constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 1);
+    const uint32_t kv0 = umma::smem_u32(KV), q0 = umma::smem_u32(Qs), p0 = umma::smem_u32(Ps);
+    auto issue_s = [&](int c) {
+      const int s = c & 1;
+      if (!umma::mbar_wait(&kv_full[s], (c >> 1) & 1, &d_err_attn)) return false;
+      if (c >= 2 && !umma::mbar_wait(&s_empty[s], ((c >> 1) - 1) & 1, &d_err_attn)) return false;
+      umma::fence_after();
+      // K steps alternate between the two half accumulators (dims 0-255, 256-511)
+      const uint64_t da0 = umma::desc_sw128(q0, 16, 1024);
+      const uint64_t db0 = umma::desc_sw128(kv0 + s * AF_KV_BYTES, 16, 1024);
+#pragma unroll
+      for (int st = 0; st < 16; ++st)
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+          const int ks = hk * 16 + st;
+          const uint32_t off = uint32_t(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
+          umma::mma_f16(tmem + AF_S_COL + 128 * s + 64 * hk, da0 + off, db0 + off, idesc_s, st > 0);
+        }
+      umma::commit(&s_full[s]);
+      return true;
+    };
+    // issue whichever is ready: the next chunk's S (its rows landed, its TMEM buffer read
+    // out) or the oldest pending P V (its probabilities written)
+    int next_s = 0, next_pv = 0;
+    uint32_t idle = 0;
+    while (next_pv < n_ch) {
+      if (next_s < n_ch && next_s <= next_pv + 1) {
+        const int c = next_s, s = c & 1;
+        if (umma::mbar_test(&kv_full[s], (c >> 1) & 1) &&
+            (c < 2 || umma::mbar_test(&s_empty[s], ((c >> 1) - 1) & 1))) {
+          issue_s(c);
+          ++next_s;
+          idle = 0;
+          continue;
+        }
+      }
+      const int c = next_pv, s = c & 1;
+      if (next_pv >= next_s || !umma::mbar_test(&p_full[s], (c >> 1) & 1)) {
+        if (++idle > (1u << 26)) { atomicOr(&d_err_attn, ERR_TIMEOUT); break; }
+        continue;
+      }
+      idle = 0;
+      ++next_pv;
+      umma::fence_after();
+      // the four dims tiles are independent accumulators: interleave them
+      const uint64_t pa0 = umma::desc_sw128(kv0 + s * AF_KV_BYTES, 8192, 1024);
+      const uint64_t pb0 = umma::desc_sw128(p0 + s * AF_P_BYTES, 8192, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt)
+          umma::mma_f16(tmem + AF_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * 8192 + kk * 2048) >> 4),
+                        pb0 + uint32_t((kk * 2048) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
+      umma::commit(&kv_empty[s]);
+    }
+    umma::commit(&o_ready);
+  }
+
+  // ---------------- merge.  Every CTA pushes its (max, sum) per head to all CTAs of the
+  // row and its scaled O^T tiles to each tile's owner (CTA dt % n_split); remote stores
+  // only, so no CTA waits on a remote load.  The owner then sums the slots it received.
+  __syncthreads();
+  if (n_ch > 0 && warp >= 4 && warp < 8) {
+    ok = ok && umma::mbar_wait(&o_ready, 0, &d_err_attn);
+    umma::fence_after();
+  }
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer has started
+  if (warp >= 4 && warp < 8 && lane < 16) {
+    const int h = 16 * (warp & 3) + lane;
+    const float2 mine = make_float2(m_fin, l_fin);
+    for (int r = 0; r < u.n_split; ++r)
+      *reinterpret_cast<float2*>(cluster.map_shared_rank(&ml_all[rank][h][0], r)) = mine;
+  }
+  cluster.sync();
+  if (tid < 64) {
+    const int h = tid;
+    const float sk = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
+    float M = sk;
+    for (int r = 0; r < u.n_split; ++r) M = fmaxf(M, ml_all[r][h][0]);
+    float L = a.sink ? exp2f(sk - M) : 0.f;
+    for (int r = 0; r < u.n_split; ++r)
+      if (ml_all[r][h][1] > 0.f) L += ml_all[r][h][1] * exp2f(ml_all[r][h][0] - M);
+    fac[h] = ml_all[rank][h][1] > 0.f ? exp2f(ml_all[rank][h][0] - M) / L : 0.f;
+    if (rank == 0 && a.lse) a.lse[size_t(row) * 64 + h] = (M + log2f(L)) * 0.6931471805599453f;
+  }
+  __syncthreads();
+  const int n_lt = (4 + u.n_split - 1) / u.n_split;   // tile slots per source rank
+  if (warp >= 4 && warp < 8) {
+    const int q = warp & 3;
+    const uint32_t lane_addr = uint32_t(32 * q) << 16;
+    // the factors go to registers first: the compiler cannot tell the stores from fac[],
+    // and would otherwise reload fac behind every store
+    float fr[64];
+#pragma unroll
+    for (int x = 0; x < 64; ++x) fr[x] = n_ch > 0 ? fac[x] : 0.f;
+    for (int dt = 0; dt < 4; ++dt) {
+      float* dst = cluster.map_shared_rank(Obuf, dt % u.n_split) +
+                   size_t((rank * n_lt + dt / u.n_split) * 64) * 128 + 32 * q + lane;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t o[32];
+        if (n_ch > 0) {
+          umma::tmem_ld32(tmem + lane_addr + AF_O_COL + 64 * dt + 32 * hf, o);
+          umma::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0u;
+        }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) dst[(32 * hf + x) * 128] = __uint_as_float(o[x]) * fr[32 * hf + x];
       }
     }
   }
   umma::fence_before();
-  __syncthreads();
-  if (warp == 0) umma::tmem_free(tmem, 512);
-}
-
-// One CTA per (query row, group of 8 heads), 128 threads: thread t owns dims 4t..4t+3.
-// All tile partials of a head are loaded before they are combined so that the loads
-// are in flight together.
-constexpr int AC_HG = 8;
-__global__ void __launch_bounds__(128) attn_combine_kernel(AttnUmmaArgs u) {
-  const AttnArgs& a = u.a;
-  __shared__ float wgt[AC_HG][8];    // per head, per tile: e^(m_t - M) / L (0 if empty)
-  const int row = blockIdx.x / (AU_H / AC_HG), hg = blockIdx.x % (AU_H / AC_HG);
-  const int tid = threadIdx.x;
-  const float* __restrict__ ml = u.part_ml + size_t(row) * u.n_tiles * AU_H * 2;
-  if (tid < AC_HG) {
-    const int h = hg * AC_HG + tid;
-    float M = -INFINITY;
-    for (int tt = 0; tt < u.n_tiles; ++tt)
-      if (ml[(tt * AU_H + h) * 2 + 1] > 0.f) M = fmaxf(M, ml[(tt * AU_H + h) * 2]);
-    if (a.sink) M = fmaxf(M, a.sink[h]);
-    float L = 0.f;
-    for (int tt = 0; tt < u.n_tiles; ++tt) {
-      const float l = ml[(tt * AU_H + h) * 2 + 1];
-      if (l > 0.f) L += l * expf(ml[(tt * AU_H + h) * 2] - M);
-    }
-    if (a.sink) L += expf(a.sink[h] - M);
-    for (int tt = 0; tt < 8; ++tt) {
-      float wv = 0.f;
-      if (tt < u.n_tiles) {
-        const float l = ml[(tt * AU_H + h) * 2 + 1];
-        if (l > 0.f) wv = expf(ml[(tt * AU_H + h) * 2] - M) / L;
+  cluster.sync();
+  // owned tiles: sum the slots (local shared memory), write bf16
+  for (int lt = 0; rank + lt * u.n_split < 4; ++lt) {
+    const int dt = rank + lt * u.n_split;
+    for (int idx = tid; idx < 64 * 32; idx += AF_T) {   // (head, 4-dim group)
+      const int hh = idx >> 5, d4 = (idx & 31) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < u.n_split; ++r) {
+        const float4 v = *reinterpret_cast<const float4*>(Obuf + size_t(((r * n_lt + lt) * 64 + hh)) * 128 + d4);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
-      wgt[tid][tt] = wv;
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y), hi2 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 st;
+      st.x = *reinterpret_cast<uint32_t*>(&lo2);
+      st.y = *reinterpret_cast<uint32_t*>(&hi2);
+      *reinterpret_cast<uint2*>(a.out + (size_t(row) * 64 + hh) * 512 + dt * 128 + d4) = st;
     }
-    if (a.lse) a.lse[size_t(row) * AU_H + h] = M + logf(L);
   }
-  __syncthreads();
-  const float4* __restrict__ po =
-      reinterpret_cast<const float4*>(u.part_o + size_t(row) * u.n_tiles * AU_H * 512);
-  __nv_bfloat16* __restrict__ out = reinterpret_cast<__nv_bfloat16*>(a.out);
-#pragma unroll 1
-  for (int hh = 0; hh < AC_HG; ++hh) {
-    const int h = hg * AC_HG + hh;
-    float4 v[8];
-#pragma unroll
-    for (int tt = 0; tt < 8; ++tt)
-      v[tt] = (wgt[hh][tt] != 0.f) ? po[(size_t(tt) * AU_H + h) * 128 + tid] : make_float4(0, 0, 0, 0);
-    float4 acc = make_float4(0, 0, 0, 0);
-#pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
-      const float wv = wgt[hh][tt];
-      acc.x = fmaf(wv, v[tt].x, acc.x); acc.y = fmaf(wv, v[tt].y, acc.y);
-      acc.z = fmaf(wv, v[tt].z, acc.z); acc.w = fmaf(wv, v[tt].w, acc.w);
-    }
-    __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y), hi2 = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 st;
-    st.x = *reinterpret_cast<uint32_t*>(&lo2);
-    st.y = *reinterpret_cast<uint32_t*>(&hi2);
-    *reinterpret_cast<uint2*>(out + (size_t(row) * AU_H + h) * 512 + 4 * tid) = st;
-  }
+  umma::fence_after();
+  if (warp == 0) umma::tmem_free(tmem, 512);
 }
 
 }  // namespace
@@ -445,11 +592,8 @@ using namespace csa2;
 extern "C" {
 
 size_t csa2_sparse_attn_workspace_size(int B, int Tq, int H, int k, int window) {
-  if (H != AU_H || B <= 0 || Tq <= 0 || k < 0 || window < 1) return 0;
-  const size_t n_tiles = size_t(ceil_div(k + window, AU_ROWS));
-  const size_t rows = size_t(B) * Tq;
-  return align_up(rows * n_tiles * AU_H * 512 * sizeof(float), 256) +
-         align_up(rows * n_tiles * AU_H * 2 * sizeof(float), 256);
+  (void)B; (void)Tq; (void)H; (void)k; (void)window;
+  return 0;   // partial results are merged on chip
 }
 
 int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
@@ -484,23 +628,39 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
               n_cap, n_entries, topk, k, (const uint16_t*)swa_kv, S, swa_pos0, window, sink,
               scale, (uint16_t*)out, lse_out};
   cudaStream_t st = (cudaStream_t)stream;
-  if (H == AU_H) {
-    // tensor-core path: per-tile partials in the workspace, then the combine
-    const size_t need = csa2_sparse_attn_workspace_size(B, Tq, H, k, window);
-    if (!workspace || ws_bytes < need || !aligned256(workspace))
-      return fail(CSA2_ERR_WORKSPACE, "sparse_attn: workspace needs %zu bytes, 256-aligned", need);
-    const int n_tiles = ceil_div(k + window, AU_ROWS);
-    if (n_tiles > 8) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: k + window > 1024 with 64 heads");
-    if (rows * n_tiles > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
-    AttnUmmaArgs ua{aa, n_tiles, static_cast<float*>(workspace), nullptr};
-    ua.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          align_up(size_t(rows) * n_tiles * AU_H * 512 * 4, 256));
-    cudaError_t e0 = cudaFuncSetAttribute(attn_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          int(AU_SMEM));
-    if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: shared memory attribute");
-    attn_umma_kernel<<<unsigned(rows * n_tiles), AU_T, AU_SMEM, st>>>(ua);
-    note_launch();
-    attn_combine_kernel<<<unsigned(rows * (AU_H / AC_HG)), 128, 0, st>>>(ua);
+  if (H == 64) {
+    // tensor-core path: a cluster of n_split CTAs per row (enough CTAs to cover the SMs),
+    // partial results merged through distributed shared memory
+    (void)workspace; (void)ws_bytes;
+    static int sms_cache[64] = {0};
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: device id");
+    if (sms_cache[dev] == 0) {
+      e0 = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
+      if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
+    }
+    const int n_ch_max = ceil_div(k + window, AF_CH);
+    int n_split = int(sms_cache[dev] / rows);
+    n_split = std::max(1, std::min(std::min(n_split, AF_MAX_SPLIT), n_ch_max));
+    if (rows * n_split > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
+    AttnFlashArgs fa{aa, n_split};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(rows * n_split), 1, 1);
+    cfg.blockDim = dim3(AF_T, 1, 1);
+    cfg.dynamicSmemBytes = AF_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(n_split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e0 = cudaLaunchKernelEx(&cfg, attn_flash_kernel, fa);
+    if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: launch");
     note_launch();
   } else {
     attn_simt_kernel<<<unsigned(rows * n_hg), AT_T, 0, st>>>(aa);

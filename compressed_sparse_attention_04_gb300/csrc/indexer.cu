@@ -201,12 +201,6 @@ __device__ __forceinline__ void mma_fp4(uint32_t tmem_d, uint64_t da, uint64_t d
       "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
       :: "r"(tmem_d), "l"(da), "l"(db), "r"(SU_IDESC), "r"(sfa), "r"(sfb), "r"(accumulate));
 }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-               :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
-                  "r"(v[6]), "r"(v[7]) : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // per-16 scale words for the two K = 64 halves from four per-32 E4M3 bytes: (s0 s0 s1 s1),
 // (s2 s2 s3 s3)
 __device__ __forceinline__ uint32_t sf_lo(uint32_t s4) { return __byte_perm(s4, 0u, 0x1100); }
@@ -437,7 +431,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
       if (new_row) {   // query scale factors: heads 0..31 in word 0 of each 4-column group
         const uint32_t qs = reinterpret_cast<const uint32_t*>(Qb + (cs.k & 1) * SU_QROW_BYTES + SU_Q_BYTES)[lane];
         const uint32_t v[8] = {sf_lo(qs), 0u, 0u, 0u, sf_hi(qs), 0u, 0u, 0u};
-        tmem_st8(tmem + lane_addr + SU_SFB_COL + 8 * (cs.k & 1), v);
+        umma::tmem_st8(tmem + lane_addr + SU_SFB_COL + 8 * (cs.k & 1), v);
       }
       // scale factors of rows lane, lane + 32, lane + 64, lane + 96 of both tiles; the
       // step's scale bytes are stored in step-key order
@@ -451,9 +445,9 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
           v[g4] = sf_lo(s4);
           v[4 + g4] = sf_hi(s4);
         }
-        tmem_st8(tmem + lane_addr + SU_SFA_COL + 16 * s2 + 8 * tile, v);
+        umma::tmem_st8(tmem + lane_addr + SU_SFA_COL + 16 * s2 + 8 * tile, v);
       }
-      tmem_st_wait();
+      umma::tmem_st_wait();
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&sf_ready[s2]);

@@ -369,6 +369,9 @@ def _topk_input(seed, B, Tq, k, n_entries, holes=True):
     (1, 40, 64, 0, 20, 128, 40, 0, True),
     (2, 3, 64, 500, 700, 300, 200, 370, False),
     (2, 1, 64, 300, 0, 0, 128, 173, True),
+    # enough rows for one CTA per row, and the decode batch (two CTAs per row)
+    (80, 1, 64, 4095, 2000, 256, 128, 4095 - 127, False),
+    (64, 1, 64, 131071, 3000, 512, 128, 131071 - 127, True),
 ])
 def test_sparse_attn_parity(B, Tq, H, q_pos0, n_entries, k, S, swa_pos0, sink):
     ops = _ops()
@@ -399,6 +402,43 @@ def test_sparse_attn_parity(B, Tq, H, q_pos0, n_entries, k, S, swa_pos0, sink):
                 mx = np.maximum(mx, sk64)
             l_o = np.log(np.exp(lg - mx[:, None]).sum(1) + (np.exp(sk64 - mx) if sink else 0)) + mx
             np.testing.assert_allclose(lse[b, i].cpu().numpy(), l_o, rtol=1e-4, atol=1e-4)
+
+
+def _bf16_dev(x64):
+    bits = R.f64_to_bf16_bits(x64)
+    return torch.from_numpy(bits.view(np.int16).copy()).cuda().view(torch.bfloat16), R.bf16_to_f64(bits)
+
+
+@pytest.mark.parametrize("B", [1, 64])
+def test_sparse_attn_rising_logits_move_the_running_max(B):
+    # logits rise by about 50 (log2 units) from one 64-row chunk to the next, so every
+    # chunk moves each head's running maximum and rescales what was accumulated so far
+    ops = _ops()
+    H, k, n_entries, S, t = 64, 512, 1024, 128, 2047
+    g = np.random.default_rng(7)   # seeded structure on top of the synthetic streams
+    u = np.zeros(512); u[0] = 1.0
+    e = np.arange(n_entries)
+    kv64 = np.empty((B, n_entries, 512))
+    kv64[:] = 0.1 * g.standard_normal((B, n_entries, 512))
+    kv64[:, :, 0] = e / n_entries
+    swa64 = 0.1 * g.standard_normal((B, S, 512))
+    swa64[:, :, 0] = -0.5
+    gamma = np.linspace(400.0, 800.0, H) * np.sqrt(512)
+    q64 = np.zeros((B, 1, H, 512))
+    q64[:, 0] = gamma[:, None] * u[None, :] + 0.05 * g.standard_normal((B, H, 512))
+    q, q64 = _bf16_dev(q64)
+    kv, kv64 = _bf16_dev(kv64)
+    swa, swa64 = _bf16_dev(swa64)
+    topk_np = np.broadcast_to(np.arange(k, dtype=np.int32), (B, 1, k)).copy()
+    out = ops.sparse_attn(q, t, kv, n_entries, Hp.to_dev(topk_np, torch.int32), swa, t - 127,
+                          window=128)
+    torch.cuda.synchronize()
+    _ok()
+    gout = Hp.bf16_of(out)
+    for b in range(B):
+        rows = R.attention_rows(kv64[b], topk_np[b, 0], swa64[b], t - 127, t, 128)
+        Hp.check_attention(gout[b, 0], R.sparse_attention(q64[b, 0], rows, R.ATTN_SCALE, None),
+                           f"row {b}")
 
 
 def test_sparse_attn_out_of_range_index_is_reported_and_skipped():
