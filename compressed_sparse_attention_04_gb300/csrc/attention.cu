@@ -12,7 +12,7 @@
 // attended list into chunks of 64 rows; each CTA streams its chunks through a two-slot
 // ring (16-byte asynchronous gathers into a K-major 128-byte-swizzled tile), tcgen05
 // computes S = Q C^T (64 heads x 64 rows, K = 512) so that one thread owns one head's
-// scores, an online softmax writes P^T (bf16), and tcgen05 accumulates O^T = C^T P^T
+// scores, an online softmax writes P (bf16, a head per row), and tcgen05 accumulates O^T = C^T P^T
 // (512 dims x 64 heads) in TMEM, reading the SAME shared tile as the MN-major operand
 // (K = V).  The CTAs of a cluster combine their (max, sum, O) through distributed shared
 // memory; nothing intermediate goes to global memory.
@@ -191,7 +191,7 @@ constexpr int AF_CH = 64;                              // rows per chunk
 constexpr int AF_T = 288;                              // 4 copy + 4 softmax + 1 MMA warp
 constexpr uint32_t AF_KV_BYTES = AF_CH * 1024;         // 64 KB per ring slot
 constexpr uint32_t AF_Q_BYTES = 64 * 1024;
-constexpr uint32_t AF_P_BYTES = AF_CH * 64 * 2;        // 8 KB per P^T buffer
+constexpr uint32_t AF_P_BYTES = AF_CH * 64 * 2;        // 8 KB per P buffer
 constexpr uint32_t AF_SMEM = 2 * AF_KV_BYTES + AF_Q_BYTES + 2 * AF_P_BYTES + 1024;
 // S: 2 buffers x 2 K-halves x 64 columns (the two halves are independent accumulators so
 // that consecutive MMAs do not wait on each other); O^T: 4 x 64 columns
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* KV = base;                                   // 2 slots x 64 rows (K-major SW128)
   uint8_t* Qs = base + 2 * AF_KV_BYTES;                 // 64 heads (K-major SW128)
-  uint8_t* Ps = Qs + AF_Q_BYTES;                        // 2 x P^T (64 rows x 64 heads, MN-major)
+  uint8_t* Ps = Qs + AF_Q_BYTES;                        // 2 x P (64 heads x 64 rows, K-major)
   // after the last chunk: partial O^T tiles pushed by the cluster's CTAs to the tile's owner,
   // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
   float* Obuf = reinterpret_cast<float*>(KV);
@@ -403,12 +403,19 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       // P^T buffer s is free once the products of chunk c - 2 have completed
       bool okp = c < 2 || umma::mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, &d_err_attn);
       if (!bar_and(1, 128, okp)) { ok = false; break; }
-      uint8_t* pb = Ps + s * AF_P_BYTES;
+      // P as the K-major B operand of O^T += C^T P^T: head h's 64 probabilities are one
+      // 128-byte row (8-head swizzle atoms), written as eight 16-byte chunks
+      uint8_t* pb = Ps + s * AF_P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
       if (head_lane) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const uint32_t off = uint32_t((j >> 3) * 1024 + (j & 7) * 128 + (((h >> 3) ^ (j & 7)) << 4) + (h & 7) * 2);
-          *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(p[j]);
+        for (int c16 = 0; c16 < 8; ++c16) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u2 = 0; u2 < 4; ++u2) {
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(p[8 * c16 + 2 * u2], p[8 * c16 + 2 * u2 + 1]);
+            w[u2] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          *reinterpret_cast<uint4*>(pb + ((c16 ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       // heads whose max moved after products were accumulated: rescale their O^T columns
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   } else if (warp == 8 && lane == 0) {
     // ---------------- MMA issuer
     constexpr uint32_t idesc_s = umma::idesc_f16(64, 64, 1, 0, 0);
-    constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 1);
+    constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 0);   // A = C^T (MN-major), B = P (K-major)
     const uint32_t kv0 = umma::smem_u32(KV), q0 = umma::smem_u32(Qs), p0 = umma::smem_u32(Ps);
     auto issue_s = [&](int c) {
       const int s = c & 1;
@@ -494,13 +501,13 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       umma::fence_after();
       // the four dims tiles are independent accumulators: interleave them
       const uint64_t pa0 = umma::desc_sw128(kv0 + s * AF_KV_BYTES, 8192, 1024);
-      const uint64_t pb0 = umma::desc_sw128(p0 + s * AF_P_BYTES, 8192, 1024);
+      const uint64_t pb0 = umma::desc_sw128(p0 + s * AF_P_BYTES, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
         for (int dt = 0; dt < 4; ++dt)
           umma::mma_f16(tmem + AF_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * 8192 + kk * 2048) >> 4),
-                        pb0 + uint32_t((kk * 2048) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
+                        pb0 + uint32_t((kk * 32) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
       umma::commit(&kv_empty[s]);
     }
     umma::commit(&o_ready);
@@ -535,15 +542,18 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   }
   __syncthreads();
   const int n_lt = (4 + u.n_split - 1) / u.n_split;   // tile slots per source rank
-  if (warp >= 4 && warp < 8) {
-    const int q = warp & 3;
-    const uint32_t lane_addr = uint32_t(32 * q) << 16;
-    // the factors go to registers first: the compiler cannot tell the stores from fac[],
-    // and would otherwise reload fac behind every store
-    float fr[64];
+  // softmax warps: lane = dim 32 q + lane of each 128-dim tile; the factors go to registers
+  // first (the compiler cannot tell the stores below from fac[] and would reload it)
+  const bool o_warp = warp >= 4 && warp < 8;
+  const int q = warp & 3;
+  const uint32_t lane_addr = uint32_t(32 * q) << 16;
+  float fr[64];
+  if (o_warp) {
 #pragma unroll
     for (int x = 0; x < 64; ++x) fr[x] = n_ch > 0 ? fac[x] : 0.f;
+    // tiles owned by another CTA: scaled O^T to the owner's slot for this rank
     for (int dt = 0; dt < 4; ++dt) {
+      if (dt % u.n_split == rank) continue;
       float* dst = cluster.map_shared_rank(Obuf, dt % u.n_split) +
                    size_t((rank * n_lt + dt / u.n_split) * 64) * 128 + 32 * q + lane;
 #pragma unroll
@@ -563,21 +573,37 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   }
   umma::fence_before();
   cluster.sync();
-  // owned tiles: sum the slots (local shared memory), write bf16
-  for (int lt = 0; rank + lt * u.n_split < 4; ++lt) {
-    const int dt = rank + lt * u.n_split;
-    for (int idx = tid; idx < 64 * 32; idx += AF_T) {   // (head, 4-dim group)
-      const int hh = idx >> 5, d4 = (idx & 31) * 4;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int r = 0; r < u.n_split; ++r) {
-        const float4 v = *reinterpret_cast<const float4*>(Obuf + size_t(((r * n_lt + lt) * 64 + hh)) * 128 + d4);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  // owned tiles: own O^T (TMEM) plus the other CTAs' slots (local shared memory), bf16 out
+  if (o_warp) {
+    for (int lt = 0; rank + lt * u.n_split < 4; ++lt) {
+      const int dt = rank + lt * u.n_split;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + size_t(row) * 64 * 512 +
+                            dt * 128 + 32 * q + lane;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t o[32];
+        if (n_ch > 0) {
+          umma::tmem_ld32(tmem + lane_addr + AF_O_COL + 64 * dt + 32 * hf, o);
+          umma::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] = 0u;
+        }
+        float acc[32];
+#pragma unroll
+        for (int x = 0; x < 32; ++x) acc[x] = __uint_as_float(o[x]) * fr[32 * hf + x];
+        for (int r = 0; r < u.n_split; ++r) {
+          if (r == rank) continue;
+          const float* src = Obuf + size_t((r * n_lt + lt) * 64 + 32 * hf) * 128 + 32 * q + lane;
+          float v[32];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] = src[x * 128];
+#pragma unroll
+          for (int x = 0; x < 32; ++x) acc[x] += v[x];
+        }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) orow[(32 * hf + x) * 512] = __float2bfloat16_rn(acc[x]);
       }
-      __nv_bfloat162 lo2 = __floats2bfloat162_rn(acc.x, acc.y), hi2 = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 st;
-      st.x = *reinterpret_cast<uint32_t*>(&lo2);
-      st.y = *reinterpret_cast<uint32_t*>(&hi2);
-      *reinterpret_cast<uint2*>(a.out + (size_t(row) * 64 + hh) * 512 + dt * 128 + d4) = st;
     }
   }
   umma::fence_after();
