@@ -210,27 +210,47 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
     int n_cap, float* __restrict__ kv_pre) {
   const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x;
   const size_t row0 = size_t(b) * T + size_t(g) * m;
+  // channels 4t..4t+3 of up to m = 2 rows, projection (kv) and gate (z) halves: the split-K
+  // partials are summed in split order; four splits' loads are in flight at a time
+  const int nv = m == 1 ? 1 : 4;   // float4 vectors per split: kv0 | z0 kv1 z1
+  size_t off[4];
+  off[0] = row0 * Nout + 4 * t;
+  off[1] = row0 * Nout + 512 + 4 * t;
+  off[2] = (row0 + 1) * Nout + 4 * t;
+  off[3] = (row0 + 1) * Nout + 512 + 4 * t;
+  float4 acc[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp0 = 0; sp0 < n_split; sp0 += 4) {
+    float4 ld[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        ld[q][v] = (sp0 + q < n_split && v < nv)
+                       ? *reinterpret_cast<const float4*>(P + off[v] + size_t(sp0 + q) * split_stride)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        if (sp0 + q >= n_split || v >= nv) continue;
+        if (sp0 + q == 0) { acc[v] = ld[q][v]; continue; }
+        acc[v].x += ld[q][v].x; acc[v].y += ld[q][v].y; acc[v].z += ld[q][v].z; acc[v].w += ld[q][v].w;
+      }
+  }
   float pooled[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    const int c = 4 * t + u;
-    auto proj = [&](size_t idx) {
-      float acc = P[idx];
-      for (int sp = 1; sp < n_split; ++sp) acc += P[idx + sp * split_stride];
-      return acc;
-    };
+    auto comp = [&](const float4& x) { return u == 0 ? x.x : u == 1 ? x.y : u == 2 ? x.z : x.w; };
     if (m == 1) {
-      pooled[u] = proj(row0 * Nout + c);
+      pooled[u] = comp(acc[0]);
     } else {
-      float kvv[2], zz[2];
-      float mx = -INFINITY;
-      for (int i = 0; i < m; ++i) {
-        zz[i] = proj((row0 + i) * Nout + 512 + c);
-        kvv[i] = proj((row0 + i) * Nout + c);
-        mx = fmaxf(mx, zz[i]);
-      }
+      const float kvv[2] = {comp(acc[0]), comp(acc[2])}, zz[2] = {comp(acc[1]), comp(acc[3])};
+      const float mx = fmaxf(zz[0], zz[1]);
       float num = 0.f, den = 0.f;
-      for (int i = 0; i < m; ++i) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
         const float w = expf(zz[i] - mx);
         den += w;
         num = fmaf(w, kvv[i], num);
@@ -276,41 +296,59 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
   *reinterpret_cast<uint2*>(kv_cache + crow * 512 + 4 * t) = st;
 }
 
-constexpr int IK_E = 8;  // entries per block
+constexpr int IK_E = 8;  // entries per block (few entries, as in decode: 2)
 
-// 128 threads: thread j computes key dim j for IK_E entries; warp w then quantises
-// block w (dims 32w..32w+31) of each entry.
+// 128 threads: thread j computes key dim j for E entries; warp w then quantises
+// block w (dims 32w..32w+31) of each entry.  The weight row is read 128 bytes at a time
+// (eight 16-byte loads in flight); the sum over the 512 inputs runs in index order.
+template <int E>
 __global__ void __launch_bounds__(128) index_k_kernel(const float* __restrict__ kv_pre, int B,
                                                       int G, int entry0, int m,
                                                       const uint16_t* __restrict__ w_ik,
                                                       float rope_base, uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales, int n_cap,
                                                       float* __restrict__ k_out) {
-  __shared__ float kv[IK_E][512];
+  __shared__ float kv[E][512];
   const int j = threadIdx.x, lane = j & 31, w = j >> 5;
   const int total = B * G;
-  const int e0 = blockIdx.x * IK_E;
-  for (int idx = j; idx < IK_E * 512; idx += 128) {
-    const int e = e0 + idx / 512;
-    kv[idx / 512][idx % 512] = (e < total) ? kv_pre[size_t(e) * 512 + idx % 512] : 0.f;
+  const int e0 = blockIdx.x * E;
+  {
+    float4 v4[E];   // all of this thread's loads in flight together
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+      const int idx = (r * 128 + j) * 4, e = e0 + idx / 512;
+      v4[r] = (e < total) ? *reinterpret_cast<const float4*>(kv_pre + size_t(e) * 512 + idx % 512)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < E; ++r) {
+      const int idx = (r * 128 + j) * 4;
+      *reinterpret_cast<float4*>(&kv[idx / 512][idx % 512]) = v4[r];
+    }
   }
   __syncthreads();
-  float acc[IK_E];
+  float acc[E];
 #pragma unroll
-  for (int e = 0; e < IK_E; ++e) acc[e] = 0.f;
-  const uint16_t* wr = w_ik + size_t(j) * 512;
-  for (int h = 0; h < 512; h += 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(wr + h);
-    const uint16_t* pv = reinterpret_cast<const uint16_t*>(&v);
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  const uint4* wr = reinterpret_cast<const uint4*>(w_ik + size_t(j) * 512);
+#pragma unroll 1
+  for (int h0 = 0; h0 < 512; h0 += 128) {
+    uint4 vv[16];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float wv = bf16_to_f32(pv[u]);
+    for (int u8 = 0; u8 < 16; ++u8) vv[u8] = wr[(h0 >> 3) + u8];
 #pragma unroll
-      for (int e = 0; e < IK_E; ++e) acc[e] = fmaf(wv, kv[e][h + u], acc[e]);
+    for (int u8 = 0; u8 < 16; ++u8) {
+      const uint16_t* pv = reinterpret_cast<const uint16_t*>(&vv[u8]);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wv = bf16_to_f32(pv[u]);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] = fmaf(wv, kv[e][h0 + 8 * u8 + u], acc[e]);
+      }
     }
   }
 #pragma unroll
-  for (int e = 0; e < IK_E; ++e) {
+  for (int e = 0; e < E; ++e) {
     const int ei = e0 + e;
     if (ei >= total) break;  // uniform across the block
     const int b = ei / G, g = ei % G;
@@ -420,8 +458,13 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, con
     return fail(CSA2_ERR_UNSUPPORTED, "index_k_quant: too many entries for one call");
   if (G == 0) return CSA2_OK;
   const int total = B * G;
-  index_k_kernel<<<ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream>>>(
-      kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+  if (total <= 1024) {   // few entries (decode): more CTAs, each reading the weights once
+    index_k_kernel<2><<<ceil_div(total, 2), 128, 0, (cudaStream_t)stream>>>(
+        kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+  } else {
+    index_k_kernel<IK_E><<<ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream>>>(
+        kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+  }
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_k_quant launch");
