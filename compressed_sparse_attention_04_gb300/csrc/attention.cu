@@ -204,6 +204,13 @@ struct AttnFlashArgs {
   int n_split;        // CTAs per row (cluster size)
 };
 
+// 2^x by the MUFU approximation (relative error about 2^-22; the probabilities are rounded
+// to bf16 for the products, and the sums use the same values).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 // Named barrier over n threads that also reduces a predicate (and / or) across them.
 __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
   uint32_t r;
@@ -344,9 +351,12 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     }
     umma::cp_async_wait_all();
   } else if (warp < 8) {
-    // ---------------- softmax warps: warp q holds heads 16 q .. 16 q + 15 in lanes 0..15
+    // ---------------- softmax warps: warp q holds heads 16 q .. 16 q + 15 in TMEM lanes
+    // 0..15; lane l < 16 then takes rows 0..31 of head 16 q + l and lane l + 16 rows 32..63
+    // (handed over by shuffles), so the whole warp shares the work.
     const int q = warp & 3, h = 16 * q + (lane & 15);
     const bool head_lane = lane < 16;
+    const int half = lane >> 4;
     const uint32_t lane_addr = uint32_t(32 * q) << 16;
     float m_used = -INFINITY, l = 0.f;
     for (int c = 0; c < n_ch && ok; ++c) {
@@ -354,7 +364,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       bool okc = __all_sync(0xffffffffu, umma::mbar_wait(&s_full[s], (c >> 1) & 1, &d_err_attn));
       if (!bar_and(1, 128, okc)) { ok = false; break; }
       umma::fence_after();
-      float sv[64];
+      float sv[32];   // this lane's 32 rows of its head (scaled to log2 units, masked)
       {
         uint32_t v0[32], v1[32], w0[32], w1[32];
         umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s, v0);
@@ -364,24 +374,35 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
         umma::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          sv[j] = __uint_as_float(v0[j]) + __uint_as_float(w0[j]);
-          sv[32 + j] = __uint_as_float(v1[j]) + __uint_as_float(w1[j]);
+          const float lo_rows = __uint_as_float(v0[j]) + __uint_as_float(w0[j]);
+          const float hi_rows = __uint_as_float(v1[j]) + __uint_as_float(w1[j]);
+          const float moved = __shfl_sync(0xffffffffu, hi_rows, lane & 15);
+          sv[j] = half ? moved : lo_rows;
         }
       }
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_empty[s]);
-      const unsigned long long mask = row_mask[s];
+      const unsigned mask = half ? unsigned(row_mask[s] >> 32) : unsigned(row_mask[s]);
       float cmx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) cmx[u] = -INFINITY;
+      if (mask == 0xffffffffu) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        sv[j] = ((mask >> j) & 1ull) ? sv[j] * scale_log2 : -INFINITY;
-        cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
+        for (int j = 0; j < 32; ++j) {
+          sv[j] *= scale_log2;
+          cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          sv[j] = ((mask >> j) & 1u) ? sv[j] * scale_log2 : -INFINITY;
+          cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
+        }
       }
-      const float cm = fmaxf(fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3])),
-                             fmaxf(fmaxf(cmx[4], cmx[5]), fmaxf(cmx[6], cmx[7])));
+      float cm = fmaxf(fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3])),
+                       fmaxf(fmaxf(cmx[4], cmx[5]), fmaxf(cmx[6], cmx[7])));
+      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));   // the head's maximum
       // move the running max only when this chunk exceeds it by more than AF_LAZY
       float f = 1.f;
       if (cm > m_used + AF_LAZY || (m_used == -INFINITY && cm != -INFINITY)) {
@@ -392,11 +413,11 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       float psx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) psx[u] = 0.f;
-      float p[64];
+      float p[32];
       const float msub = m_used == -INFINITY ? INFINITY : m_used;   // all p = 0 before a valid row
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        p[j] = exp2f(sv[j] - msub);
+      for (int j = 0; j < 32; ++j) {
+        p[j] = fast_exp2(sv[j] - msub);
         psx[j & 7] += p[j];
       }
       l += ((psx[0] + psx[1]) + (psx[2] + psx[3])) + ((psx[4] + psx[5]) + (psx[6] + psx[7]));
@@ -406,17 +427,16 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       // P as the K-major B operand of O^T += C^T P^T: head h's 64 probabilities are one
       // 128-byte row (8-head swizzle atoms), written as eight 16-byte chunks
       uint8_t* pb = Ps + s * AF_P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
-      if (head_lane) {
 #pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
-          uint32_t w[4];
+      for (int c4 = 0; c4 < 4; ++c4) {   // this lane's half of the row: chunks 4 half .. +3
+        uint32_t w[4];
 #pragma unroll
-          for (int u2 = 0; u2 < 4; ++u2) {
-            __nv_bfloat162 v2 = __floats2bfloat162_rn(p[8 * c16 + 2 * u2], p[8 * c16 + 2 * u2 + 1]);
-            w[u2] = *reinterpret_cast<uint32_t*>(&v2);
-          }
-          *reinterpret_cast<uint4*>(pb + ((c16 ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int u2 = 0; u2 < 4; ++u2) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(p[8 * c4 + 2 * u2], p[8 * c4 + 2 * u2 + 1]);
+          w[u2] = *reinterpret_cast<uint32_t*>(&v2);
         }
+        const int c16 = 4 * half + c4;
+        *reinterpret_cast<uint4*>(pb + ((c16 ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       // heads whose max moved after products were accumulated: rescale their O^T columns
       const bool need = head_lane && f != 1.f && c > 0;
@@ -451,7 +471,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       if (lane == 0) umma::mbar_arrive(&p_full[s]);
     }
     m_fin = m_used;
-    l_fin = l;
+    l_fin = l + __shfl_xor_sync(0xffffffffu, l, 16);   // both halves of the head's rows
   } else if (warp == 8 && lane == 0) {
     // ---------------- MMA issuer
     constexpr uint32_t idesc_s = umma::idesc_f16(64, 64, 1, 0, 0);
