@@ -34,6 +34,10 @@ WORKLOADS = {
     "decode40": dict(B=64, C=131072, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
     # a small stand-in for quick checks (not a bench line)
     "small": dict(B=4, C=8192, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
+    # the headline batch at an 8K context: every attention launch has the headline shape
+    # (64 rows x (512 + 128) rows x 64 heads) with a few GB of caches, small enough for a
+    # full profiler capture (not a bench line)
+    "b64_ctx8k": dict(B=64, C=8192, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
 }
 
 
@@ -44,6 +48,29 @@ def peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def attention_traffic(modes):
+    """DRAM bytes per attention launch, averaged over one step's layers, from the ncu record in
+    profiles/attn_flash_b64_ctx8k.md (layers with a global branch read the headline shape,
+    window-only layers 128 rows).  None when the kernel source no longer matches the record
+    or the record is missing."""
+    import hashlib
+    try:
+        rec = {}
+        with open(os.path.join(ROOT, "profiles", "attn_flash_b64_ctx8k.md")) as f:
+            for line in f:
+                parts = line.strip().split(":")
+                if len(parts) == 2 and parts[0].startswith(("traffic_", "attention_source")):
+                    rec[parts[0].strip()] = parts[1].strip()
+        with open(os.path.join(ROOT, "compressed_sparse_attention_04_gb300", "csrc", "attention.cu"), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if rec.get("attention_source_sha256_16") != h:
+            return None
+        full, win = int(rec["traffic_full_launch_bytes"]), int(rec["traffic_window_launch_bytes"])
+        return sum(win if m == 0 else full for m in modes) / len(modes)
+    except Exception:
+        return None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -391,7 +418,9 @@ def run_ours(args, wl, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": STAGE_NAMES[dom], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "launches_timed": stage_launches[dom]},
+                     "traffic": attention_traffic(st.modes) if STAGE_NAMES[dom] == "sparse_attn" and
+                                wl["C"] == 131072 and wl["B"] == 64 else None,
+                     "launches_timed": stage_launches[dom]},
         "hot_path_roofline": {"stages": [STAGE_NAMES[s] for s in hot], "achieved": hot_gbs,
                               "frac": hot_gbs / peak, "unit": "GB/s"},
         "stage_ms_per_step": {STAGE_NAMES[s]: stage_ms[s] / args.steps for s in range(6)},
