@@ -187,12 +187,18 @@ __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
 // The running maximum is only moved when a chunk exceeds it by more than 2^8 (probabilities
 // then stay below 256, exact in float32 sums); moving it rescales that head's columns of
 // O^T in TMEM after the previous chunk's products have landed.
-constexpr int AF_CH = 64;                              // rows per chunk
+constexpr int AF_CH = 48;                              // rows per chunk
+constexpr int AF_SLOTS = 3;                            // KV ring depth (chunks)
 constexpr int AF_T = 288;                              // 4 copy + 4 softmax + 1 MMA warp
-constexpr uint32_t AF_KV_BYTES = AF_CH * 1024;         // 64 KB per ring slot
+constexpr uint32_t AF_KV_BYTES = AF_CH * 1024;         // 48 KB per ring slot
+constexpr uint32_t AF_ATOM = AF_CH * 128;              // one 64-dim atom column of a slot
 constexpr uint32_t AF_Q_BYTES = 64 * 1024;
-constexpr uint32_t AF_P_BYTES = AF_CH * 64 * 2;        // 8 KB per P buffer
-constexpr uint32_t AF_SMEM = 2 * AF_KV_BYTES + AF_Q_BYTES + 2 * AF_P_BYTES + 1024;
+// P: 64 heads x 48 rows, K-major without swizzle: 8-head x 8-row core matrices of 128 B,
+// K (rows) direction 128 B apart, 8-head groups AF_P_SBO apart
+constexpr uint32_t AF_P_SBO = (AF_CH / 8) * 128;
+constexpr uint32_t AF_P_BYTES = 8 * AF_P_SBO;          // 6 KB per P buffer
+constexpr uint32_t AF_SMEM = AF_SLOTS * AF_KV_BYTES + AF_Q_BYTES + 2 * AF_P_BYTES + 1024;
+constexpr int AF_HALF = AF_CH / 2;                     // rows per lane (two lanes per head)
 // S: 2 buffers x 2 K-halves x 64 columns (the two halves are independent accumulators so
 // that consecutive MMAs do not wait on each other); O^T: 4 x 64 columns
 constexpr uint32_t AF_S_COL = 0, AF_O_COL = 256;
@@ -204,6 +210,16 @@ struct AttnFlashArgs {
   int n_split;        // CTAs per row (cluster size)
 };
 
+// Shared-memory descriptor without swizzle: 8-row x 16-byte core matrices, LBO = stride
+// between core matrices along K, SBO = stride between 8-row groups.
+__device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  return d;
+}
 // 2^x by the MUFU approximation (relative error about 2^-22; the probabilities are rounded
 // to bf16 for the products, and the sums use the same values).
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -231,15 +247,16 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* KV = base;                                   // 2 slots x 64 rows (K-major SW128)
-  uint8_t* Qs = base + 2 * AF_KV_BYTES;                 // 64 heads (K-major SW128)
+  uint8_t* KV = base;                                   // AF_SLOTS x 48 rows (K-major SW128)
+  uint8_t* Qs = base + AF_SLOTS * AF_KV_BYTES;          // 64 heads (K-major SW128)
   uint8_t* Ps = Qs + AF_Q_BYTES;                        // 2 x P (64 heads x 64 rows, K-major)
   // after the last chunk: partial O^T tiles pushed by the cluster's CTAs to the tile's owner,
   // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
   float* Obuf = reinterpret_cast<float*>(KV);
-  __shared__ const uint16_t* row_src[2][AF_CH];
-  __shared__ unsigned long long row_mask[2];
-  __shared__ __align__(8) uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2], o_ready;
+  __shared__ const uint16_t* row_src[AF_SLOTS][AF_CH];
+  __shared__ unsigned long long row_mask[AF_SLOTS];
+  __shared__ __align__(8) uint64_t kv_full[AF_SLOTS], kv_empty[AF_SLOTS];
+  __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready;
   __shared__ uint32_t tmem_slot;
   __shared__ float fac[64];                              // per-head factor (rescale / final)
   __shared__ __align__(8) float ml_all[AF_MAX_SPLIT][64][2];   // every CTA's (max, sum), log2 units
@@ -259,9 +276,11 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   const float scale_log2 = a.scale * 1.4426950408889634f;
 
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
-      umma::mbar_init(&kv_full[s], 128);
+    for (int s = 0; s < AF_SLOTS; ++s) {
+      umma::mbar_init(&kv_full[s], 64);   // the 64 threads of the group that fills it
       umma::mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       umma::mbar_init(&s_full[s], 1);
       umma::mbar_init(&s_empty[s], 4);
       umma::mbar_init(&p_full[s], 4);
@@ -280,79 +299,67 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   if (warp < 4) {
-    // ---------------- copy warps: chunk c of this CTA into slot c % 2 (and Q with chunk 0).
-    // Thread t < 64 holds the selected entry of row t of the next chunk, loaded one chunk
-    // ahead so that its latency overlaps the wait for a free slot.
+    // ---------------- copy warps, two groups of two warps: group g fills chunks g, g + 2,
+    // g + 4, ... (slot c % 3; group 0 also the queries with chunk 0), waits for its own copies
+    // and announces the chunk, so one group waiting for a free slot never holds back the
+    // other's announcement.  Thread t < 48 of a group holds the selected entry of row t of
+    // the group's next chunk, loaded one chunk ahead.
+    const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
     auto topk_at = [&](int c) -> int {
-      const int j = (c_begin + c) * AF_CH + tid;
-      return (tid < AF_CH && c < n_ch && j < a.k) ? a.topk[size_t(row) * a.k + j] : -1;
+      const int j = (c_begin + c) * AF_CH + gt;
+      return (gt < AF_CH && c < n_ch && j < a.k) ? a.topk[size_t(row) * a.k + j] : -1;
     };
-    int e_next = topk_at(0);
-    auto issue = [&](int c) {
-      if (c < n_ch) {
-        const int s = c & 1;
-        const int e = e_next;
-        e_next = topk_at(c + 1);
-        bool okw = c < 2 || umma::mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, &d_err_attn);
-        if (tid < AF_CH) {   // warps 0 and 1, whole warps (the ballot below needs every lane)
-          const int j = (c_begin + c) * AF_CH + tid;
-          int okr = 0;
-          const uint16_t* src = a.swa;   // any valid address for zero-filled copies
-          if (j < a.k) {
-            if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
-            if (e >= 0 && e < a.n_entries) { okr = 1; src = a.kv + (size_t(b) * a.n_cap + e) * 512; }
-          } else if (j < n_rows) {
-            okr = 1;
-            src = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
-          }
-          const unsigned m0 = __ballot_sync(0xffffffffu, okr);
-          if (okw) {
-            row_src[s][tid] = okr ? src : nullptr;
-            if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[warp] = m0;
-          }
+    int e_next = topk_at(grp);
+    for (int c = grp; c < n_ch && ok; c += 2) {
+      const int s = c % AF_SLOTS;
+      const int e = e_next;
+      e_next = topk_at(c + 2);
+      bool okw = c < AF_SLOTS || umma::mbar_wait(&kv_empty[s], ((c / AF_SLOTS) - 1) & 1, &d_err_attn);
+      {   // row sources (both warps of the group, whole warps for the ballot)
+        const int j = (c_begin + c) * AF_CH + gt;
+        int okr = 0;
+        const uint16_t* src = a.swa;   // any valid address for zero-filled copies
+        if (gt >= AF_CH) {
+          // (lanes past the chunk only complete the ballot)
+        } else if (j < a.k) {
+          if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
+          if (e >= 0 && e < a.n_entries) { okr = 1; src = a.kv + (size_t(b) * a.n_cap + e) * 512; }
+        } else if (j < n_rows) {
+          okr = 1;
+          src = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
         }
-        // row sources ready; the copy warps agree on whether the slot wait succeeded
-        if (!bar_and(2, 128, okw)) return false;
-        uint8_t* dst = KV + s * AF_KV_BYTES;
-#pragma unroll 4
-        for (int rep = 0; rep < 32; ++rep) {
-          const int uidx = rep * 128 + tid, r = uidx >> 6, ch = uidx & 63;
-          const uint16_t* src = row_src[s][r];
-          umma::cp_async16(dst + umma::kmajor_sw128_offset(r, ch * 8, AF_CH),
-                           src ? src + ch * 8 : a.swa, src ? 16u : 0u);
+        const unsigned m0 = __ballot_sync(0xffffffffu, okr);
+        if (okw) {
+          if (gt < AF_CH) row_src[s][gt] = okr ? src : nullptr;
+          if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[gw] = m0;
         }
-        if (c == 0) {
-          const uint16_t* qrow = a.q + size_t(row) * 64 * 512;
+      }
+      // row sources ready; the group agrees on whether the slot wait succeeded
+      if (!bar_and(2 + grp, 64, okw)) { ok = false; break; }
+      uint8_t* dst = KV + s * AF_KV_BYTES;
 #pragma unroll 4
-          for (int rep = 0; rep < 32; ++rep) {
-            const int uidx = rep * 128 + tid, h = uidx >> 6, ch = uidx & 63;
-            umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow + h * 512 + ch * 8, 16u);
-          }
+      for (int rep = 0; rep < AF_CH; ++rep) {   // 48 rows x 64 pieces of 16 bytes
+        const int uidx = rep * 64 + gt, r = uidx >> 6, ch = uidx & 63;
+        const uint16_t* src = row_src[s][r];
+        umma::cp_async16(dst + umma::kmajor_sw128_offset(r, ch * 8, AF_CH),
+                         src ? src + ch * 8 : a.swa, src ? 16u : 0u);
+      }
+      if (c == 0) {
+        const uint16_t* qrow = a.q + size_t(row) * 64 * 512;
+#pragma unroll 4
+        for (int rep = 0; rep < 64; ++rep) {
+          const int uidx = rep * 64 + gt, h = uidx >> 6, ch = uidx & 63;
+          umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow + h * 512 + ch * 8, 16u);
         }
       }
       umma::cp_async_commit();
-      return true;
-    };
-    // chunks 0 and 1 go out at once; chunk c + 1 is announced before this thread blocks on
-    // the products of chunk c, which free the slot for chunk c + 2
-    ok = issue(0) && issue(1);
-    if (ok && n_ch > 0) {
-      umma::cp_async_wait_pending(1);
+      umma::cp_async_wait_all();        // this thread's copies of chunk c landed
       umma::fence_proxy_async();
-      umma::mbar_arrive(&kv_full[0]);
+      umma::mbar_arrive(&kv_full[s]);
     }
-    for (int c = 0; c < n_ch && ok; ++c) {
-      if (c + 1 < n_ch) {
-        umma::cp_async_wait_pending(0);   // this thread's copies of chunk c + 1 landed
-        umma::fence_proxy_async();
-        umma::mbar_arrive(&kv_full[(c + 1) & 1]);
-      }
-      ok = issue(c + 2);
-    }
-    umma::cp_async_wait_all();
   } else if (warp < 8) {
     // ---------------- softmax warps: warp q holds heads 16 q .. 16 q + 15 in TMEM lanes
-    // 0..15; lane l < 16 then takes rows 0..31 of head 16 q + l and lane l + 16 rows 32..63
+    // 0..15; lane l < 16 then takes rows 0..23 of head 16 q + l and lane l + 16 rows 24..47
     // (handed over by shuffles), so the whole warp shares the work.
     const int q = warp & 3, h = 16 * q + (lane & 15);
     const bool head_lane = lane < 16;
@@ -364,18 +371,21 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       bool okc = __all_sync(0xffffffffu, umma::mbar_wait(&s_full[s], (c >> 1) & 1, &d_err_attn));
       if (!bar_and(1, 128, okc)) { ok = false; break; }
       umma::fence_after();
-      float sv[32];   // this lane's 32 rows of its head (scaled to log2 units, masked)
+      float sv[AF_HALF];   // this lane's 24 rows of its head (log2 units, masked)
       {
-        uint32_t v0[32], v1[32], w0[32], w1[32];
+        uint32_t v0[32], v1[32], w0[32], w1[32];   // K halves, columns 0..31 | 32..63
         umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s, v0);
         umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 32, v1);
         umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 64, w0);
         umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 96, w1);
         umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < AF_HALF; ++j) {
           const float lo_rows = __uint_as_float(v0[j]) + __uint_as_float(w0[j]);
-          const float hi_rows = __uint_as_float(v1[j]) + __uint_as_float(w1[j]);
+          const int jh = AF_HALF + j;   // row of the upper half (24..47)
+          const float hi_rows = jh < 32 ? __uint_as_float(v0[jh < 32 ? jh : 0]) + __uint_as_float(w0[jh < 32 ? jh : 0])
+                                        : __uint_as_float(v1[jh >= 32 ? jh - 32 : 0]) +
+                                              __uint_as_float(w1[jh >= 32 ? jh - 32 : 0]);
           const float moved = __shfl_sync(0xffffffffu, hi_rows, lane & 15);
           sv[j] = half ? moved : lo_rows;
         }
@@ -383,19 +393,20 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_empty[s]);
-      const unsigned mask = half ? unsigned(row_mask[s] >> 32) : unsigned(row_mask[s]);
+      constexpr unsigned half_bits = (1u << AF_HALF) - 1u;
+      const unsigned mask = unsigned(row_mask[c % AF_SLOTS] >> (half * AF_HALF)) & half_bits;
       float cmx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) cmx[u] = -INFINITY;
-      if (mask == 0xffffffffu) {
+      if (mask == half_bits) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < AF_HALF; ++j) {
           sv[j] *= scale_log2;
           cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < AF_HALF; ++j) {
           sv[j] = ((mask >> j) & 1u) ? sv[j] * scale_log2 : -INFINITY;
           cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
         }
@@ -413,30 +424,31 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       float psx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) psx[u] = 0.f;
-      float p[32];
+      float p[AF_HALF];
       const float msub = m_used == -INFINITY ? INFINITY : m_used;   // all p = 0 before a valid row
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < AF_HALF; ++j) {
         p[j] = fast_exp2(sv[j] - msub);
         psx[j & 7] += p[j];
       }
       l += ((psx[0] + psx[1]) + (psx[2] + psx[3])) + ((psx[4] + psx[5]) + (psx[6] + psx[7]));
-      // P^T buffer s is free once the products of chunk c - 2 have completed
-      bool okp = c < 2 || umma::mbar_wait(&kv_empty[s], ((c >> 1) - 1) & 1, &d_err_attn);
+      // P buffer s is free once the products of chunk c - 2 have completed
+      bool okp = c < 2 ||
+                 umma::mbar_wait(&kv_empty[(c - 2) % AF_SLOTS], ((c - 2) / AF_SLOTS) & 1, &d_err_attn);
       if (!bar_and(1, 128, okp)) { ok = false; break; }
-      // P as the K-major B operand of O^T += C^T P^T: head h's 64 probabilities are one
-      // 128-byte row (8-head swizzle atoms), written as eight 16-byte chunks
-      uint8_t* pb = Ps + s * AF_P_BYTES + (h >> 3) * 1024 + (h & 7) * 128;
+      // P as the K-major B operand of O^T += C^T P^T (no swizzle): head h's 8-row runs are
+      // 16-byte core-matrix rows; this lane writes its 24 rows as three of them
+      uint8_t* pb = Ps + s * AF_P_BYTES + (h >> 3) * AF_P_SBO + (h & 7) * 16;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {   // this lane's half of the row: chunks 4 half .. +3
+      for (int c3 = 0; c3 < AF_HALF / 8; ++c3) {
         uint32_t w[4];
 #pragma unroll
         for (int u2 = 0; u2 < 4; ++u2) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(p[8 * c4 + 2 * u2], p[8 * c4 + 2 * u2 + 1]);
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(p[8 * c3 + 2 * u2], p[8 * c3 + 2 * u2 + 1]);
           w[u2] = *reinterpret_cast<uint32_t*>(&v2);
         }
-        const int c16 = 4 * half + c4;
-        *reinterpret_cast<uint4*>(pb + ((c16 ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        const int kc = half * (AF_HALF / 8) + c3;   // 8-row group of the chunk
+        *reinterpret_cast<uint4*>(pb + kc * 128) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       // heads whose max moved after products were accumulated: rescale their O^T columns
       const bool need = head_lane && f != 1.f && c > 0;
@@ -444,7 +456,8 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       if (bar_or(1, 128, need)) {
         // the previous chunk's products must have landed in O^T first
         const bool okr = __all_sync(0xffffffffu,
-                                    umma::mbar_wait(&kv_empty[(c - 1) & 1], ((c - 1) >> 1) & 1, &d_err_attn));
+                                    umma::mbar_wait(&kv_empty[(c - 1) % AF_SLOTS], ((c - 1) / AF_SLOTS) & 1,
+                                                    &d_err_attn));
         if (!bar_and(1, 128, okr)) { ok = false; break; }
         umma::fence_after();
 #pragma unroll 1
@@ -474,24 +487,25 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     l_fin = l + __shfl_xor_sync(0xffffffffu, l, 16);   // both halves of the head's rows
   } else if (warp == 8 && lane == 0) {
     // ---------------- MMA issuer
-    constexpr uint32_t idesc_s = umma::idesc_f16(64, 64, 1, 0, 0);
+    constexpr uint32_t idesc_s = umma::idesc_f16(64, AF_CH, 1, 0, 0);
     constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 0);   // A = C^T (MN-major), B = P (K-major)
     const uint32_t kv0 = umma::smem_u32(KV), q0 = umma::smem_u32(Qs), p0 = umma::smem_u32(Ps);
     auto issue_s = [&](int c) {
-      const int s = c & 1;
-      if (!umma::mbar_wait(&kv_full[s], (c >> 1) & 1, &d_err_attn)) return false;
+      const int s = c & 1, ks_ = c % AF_SLOTS;
+      if (!umma::mbar_wait(&kv_full[ks_], (c / AF_SLOTS) & 1, &d_err_attn)) return false;
       if (c >= 2 && !umma::mbar_wait(&s_empty[s], ((c >> 1) - 1) & 1, &d_err_attn)) return false;
       umma::fence_after();
       // K steps alternate between the two half accumulators (dims 0-255, 256-511)
       const uint64_t da0 = umma::desc_sw128(q0, 16, 1024);
-      const uint64_t db0 = umma::desc_sw128(kv0 + s * AF_KV_BYTES, 16, 1024);
+      const uint64_t db0 = umma::desc_sw128(kv0 + ks_ * AF_KV_BYTES, 16, 1024);
 #pragma unroll
       for (int st = 0; st < 16; ++st)
 #pragma unroll
         for (int hk = 0; hk < 2; ++hk) {
           const int ks = hk * 16 + st;
-          const uint32_t off = uint32_t(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
-          umma::mma_f16(tmem + AF_S_COL + 128 * s + 64 * hk, da0 + off, db0 + off, idesc_s, st > 0);
+          const uint32_t offa = uint32_t(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
+          const uint32_t offb = uint32_t(((ks >> 2) * AF_ATOM + (ks & 3) * 32) >> 4);
+          umma::mma_f16(tmem + AF_S_COL + 128 * s + 64 * hk, da0 + offa, db0 + offb, idesc_s, st > 0);
         }
       umma::commit(&s_full[s]);
       return true;
@@ -503,7 +517,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     while (next_pv < n_ch) {
       if (next_s < n_ch && next_s <= next_pv + 1) {
         const int c = next_s, s = c & 1;
-        if (umma::mbar_test(&kv_full[s], (c >> 1) & 1) &&
+        if (umma::mbar_test(&kv_full[c % AF_SLOTS], (c / AF_SLOTS) & 1) &&
             (c < 2 || umma::mbar_test(&s_empty[s], ((c >> 1) - 1) & 1))) {
           issue_s(c);
           ++next_s;
@@ -520,15 +534,16 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       ++next_pv;
       umma::fence_after();
       // the four dims tiles are independent accumulators: interleave them
-      const uint64_t pa0 = umma::desc_sw128(kv0 + s * AF_KV_BYTES, 8192, 1024);
-      const uint64_t pb0 = umma::desc_sw128(p0 + s * AF_P_BYTES, 16, 1024);
+      const int ks_ = c % AF_SLOTS;
+      const uint64_t pa0 = umma::desc_sw128(kv0 + ks_ * AF_KV_BYTES, AF_ATOM, 1024);
+      const uint64_t pb0 = desc_noswz(p0 + s * AF_P_BYTES, 128, AF_P_SBO);
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
+      for (int kk = 0; kk < AF_CH / 16; ++kk)
 #pragma unroll
         for (int dt = 0; dt < 4; ++dt)
-          umma::mma_f16(tmem + AF_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * 8192 + kk * 2048) >> 4),
-                        pb0 + uint32_t((kk * 32) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
-      umma::commit(&kv_empty[s]);
+          umma::mma_f16(tmem + AF_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * AF_ATOM + kk * 2048) >> 4),
+                        pb0 + uint32_t((kk * 256) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
+      umma::commit(&kv_empty[ks_]);
     }
     umma::commit(&o_ready);
   }
