@@ -344,11 +344,14 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
         umma::cp_async16(dst + umma::kmajor_sw128_offset(r, ch * 8, AF_CH),
                          src ? src + ch * 8 : a.swa, src ? 16u : 0u);
       }
-      if (c == 0) {
+      if (c <= 1) {
+        // the queries come with the first chunk of each group: heads 0..31 with chunk 0,
+        // heads 32..63 with chunk 1 (all 64 with chunk 0 when there is no chunk 1)
         const uint16_t* qrow = a.q + size_t(row) * 64 * 512;
+        const int h0 = c == 0 ? 0 : 32, nh = (c == 0 && n_ch > 1) ? 32 : 64 - h0;
 #pragma unroll 4
-        for (int rep = 0; rep < 64; ++rep) {
-          const int uidx = rep * 64 + gt, h = uidx >> 6, ch = uidx & 63;
+        for (int rep = 0; rep < nh; ++rep) {
+          const int uidx = rep * 64 + gt, h = h0 + (uidx >> 6), ch = uidx & 63;
           umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow + h * 512 + ch * 8, 16u);
         }
       }
@@ -493,6 +496,8 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     auto issue_s = [&](int c) {
       const int s = c & 1, ks_ = c % AF_SLOTS;
       if (!umma::mbar_wait(&kv_full[ks_], (c / AF_SLOTS) & 1, &d_err_attn)) return false;
+      // the first S also needs the queries' second half, which comes with chunk 1
+      if (c == 0 && n_ch > 1 && !umma::mbar_wait(&kv_full[1], 0, &d_err_attn)) return false;
       if (c >= 2 && !umma::mbar_wait(&s_empty[s], ((c >> 1) - 1) & 1, &d_err_attn)) return false;
       umma::fence_after();
       // K steps alternate between the two half accumulators (dims 0-255, 256-511)
@@ -518,6 +523,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       if (next_s < n_ch && next_s <= next_pv + 1) {
         const int c = next_s, s = c & 1;
         if (umma::mbar_test(&kv_full[c % AF_SLOTS], (c / AF_SLOTS) & 1) &&
+            (c != 0 || n_ch == 1 || umma::mbar_test(&kv_full[1], 0)) &&
             (c < 2 || umma::mbar_test(&s_empty[s], ((c >> 1) - 1) & 1))) {
           issue_s(c);
           ++next_s;
