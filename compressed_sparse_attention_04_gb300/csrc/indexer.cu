@@ -709,143 +709,160 @@ __global__ void __launch_bounds__(TK_T) topk_tau_kernel(TopkArgs a, const float*
   }
 }
 
-// Long dense rows, pass 1: every visible key at or above the row's threshold is appended
-// to the row's candidate list (slot position and key; order of arrival).  A CTA gathers
-// its candidates in shared memory and reserves room in the row's list with one atomic.
-constexpr int FT_T = 256, FT_SEG = 8192, FT_CAP = 16384, FT_LOCAL = 2048;
+// Long dense rows, pass 1: the visible keys at or above the row's threshold, in position
+// order.  CTA (row, segment of FT_SEG slots): warp w compacts its contiguous 1024 slots in
+// order (ballots), then the warps' lists are concatenated into the segment's list of at most
+// FT_SEGCAP entries; the segment's count is stored (a count above FT_SEGCAP marks overflow).
+constexpr int FT_T = 256, FT_SEG = 8192, FT_SEGCAP = 1024, FT_WCAP = 256;
 struct FilterArgs {
   TopkArgs a;
   const unsigned* tau;
-  unsigned* count;      // [rows] candidates found (may exceed cap)
-  unsigned* ckey;       // [rows][cap]
-  int32_t* cpos;        // [rows][cap]
-  int cap, n_seg;
+  unsigned* count;      // [rows][n_seg] candidates per segment (> FT_SEGCAP: overflow)
+  unsigned* ckey;       // [rows][n_seg][FT_SEGCAP]
+  int32_t* cpos;        // [rows][n_seg][FT_SEGCAP]
+  int n_seg;
+  int stage_cap;        // candidates the final kernel's shared memory holds
 };
 __global__ void __launch_bounds__(FT_T) topk_filter_kernel(FilterArgs f) {
-  __shared__ unsigned lkey[FT_LOCAL];
-  __shared__ int32_t lpos[FT_LOCAL];
-  __shared__ unsigned n_local, base_sm;
+  constexpr int NW = FT_T / 32, WSPAN = FT_SEG / NW;   // 1024 slots per warp
+  __shared__ unsigned lkey[NW][FT_WCAP];
+  __shared__ int32_t lpos[NW][FT_WCAP];
+  __shared__ unsigned wcount[NW];
   const TopkArgs& a = f.a;
   const int row = blockIdx.x / f.n_seg, seg = blockIdx.x % f.n_seg, i = row % a.Tq;
   const int n_row = n_visible((long long)a.q_pos0 + i, a.m, a.n_entries);
   const int p0 = seg * FT_SEG;
-  if (p0 >= n_row) return;   // uniform
+  unsigned* cnt_out = f.count + size_t(row) * f.n_seg + seg;
+  if (p0 >= n_row) {   // uniform: nothing visible in this segment
+    if (threadIdx.x == 0) *cnt_out = 0u;
+    return;
+  }
   const unsigned thr = f.tau[row];
   const float* srow = a.scores + size_t(row) * a.row_len;
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) n_local = 0u;
-  __syncthreads();
-  const int p_end = min(p0 + FT_SEG, n_row);
-  for (int base = p0; base < p_end; base += 8 * FT_T) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int q0 = p0 + w * WSPAN, q_end = min(q0 + WSPAN, n_row);
+  unsigned n_w = 0;   // this warp's candidates so far (may exceed FT_WCAP: overflow)
+  for (int base = q0; base < q_end; base += 8 * 32) {
     float v[8];   // unconditional loads (clamped index): all eight in flight at once
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = srow[min(base + u * FT_T + int(threadIdx.x), p_end - 1)];
-    unsigned key[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) key[u] = base + u * FT_T + int(threadIdx.x) < p_end ? score_key(v[u]) : 0u;
+    for (int u = 0; u < 8; ++u) v[u] = srow[max(0, min(base + u * 32 + lane, q_end - 1))];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const bool sel = key[u] >= thr && key[u] != 0u;
+      const int p = base + u * 32 + lane;
+      const unsigned key = p < q_end ? score_key(v[u]) : 0u;
+      const bool sel = key >= thr && key != 0u;
       const unsigned mask = __ballot_sync(0xffffffffu, sel);
-      if (mask == 0u) continue;
-      const int leader = __ffs(mask) - 1;
-      unsigned at = 0;
-      if (lane == leader) at = atomicAdd(&n_local, unsigned(__popc(mask)));
-      at = __shfl_sync(0xffffffffu, at, leader) + unsigned(__popc(mask & ((1u << lane) - 1u)));
-      const int p = base + u * FT_T + int(threadIdx.x);
-      if (sel) {
-        if (at < unsigned(FT_LOCAL)) {
-          lkey[at] = key[u];
-          lpos[at] = p;
-        } else {   // more than the local list holds: straight into the row's list
-          const unsigned g = atomicAdd(&f.count[row], 1u);
-          if (g < unsigned(f.cap)) {
-            f.ckey[size_t(row) * f.cap + g] = key[u];
-            f.cpos[size_t(row) * f.cap + g] = p;
-          }
-        }
+      const unsigned at = n_w + unsigned(__popc(mask & ((1u << lane) - 1u)));
+      if (sel && at < unsigned(FT_WCAP)) {
+        lkey[w][at] = key;
+        lpos[w][at] = p;
       }
+      n_w += unsigned(__popc(mask));
     }
   }
+  if (lane == 0) wcount[w] = n_w;
   __syncthreads();
-  const unsigned n_loc = min(n_local, unsigned(FT_LOCAL));
-  if (n_loc == 0u) return;   // uniform
-  if (threadIdx.x == 0) base_sm = atomicAdd(&f.count[row], n_loc);
-  __syncthreads();
-  const unsigned b0 = base_sm;
-  for (unsigned j = threadIdx.x; j < n_loc; j += FT_T) {
-    if (b0 + j < unsigned(f.cap)) {
-      f.ckey[size_t(row) * f.cap + b0 + j] = lkey[j];
-      f.cpos[size_t(row) * f.cap + b0 + j] = lpos[j];
-    }
+  unsigned before = 0, total = 0;
+  bool over = false;
+#pragma unroll
+  for (int x = 0; x < NW; ++x) {
+    const unsigned c = wcount[x];
+    if (x < w) before += c;
+    total += c;
+    over |= c > unsigned(FT_WCAP);
+  }
+  if (threadIdx.x == 0) *cnt_out = over ? unsigned(FT_SEGCAP) + 1u : total;
+  if (over || total > unsigned(FT_SEGCAP)) return;
+  unsigned* gk = f.ckey + (size_t(row) * f.n_seg + seg) * FT_SEGCAP;
+  int32_t* gp = f.cpos + (size_t(row) * f.n_seg + seg) * FT_SEGCAP;
+  for (unsigned j = lane; j < n_w; j += 32) {
+    gk[before + j] = lkey[w][j];
+    gp[before + j] = lpos[w][j];
   }
 }
 
-// Pass 2, one CTA per row: the exact top k of the candidates (larger key first, lower
-// position first among equal keys), emitted in ascending position order.  A row whose
-// candidates overflowed the list is selected from its full score row instead.
-__global__ void __launch_bounds__(TK_T) topk_final_kernel(FilterArgs f) {
-  extern __shared__ unsigned fsm[];   // keys [cap] | positions [cap] | selected [k pow2]
+// Pass 2, one CTA per row: the segments' lists concatenated are in position order, so the
+// radix selection's stable order (lower index first among equal keys, output ascending)
+// is the method's order.  A row with an overflowing segment is selected from its full
+// score row instead.
+constexpr int FN_T = 256;
+__global__ void __launch_bounds__(FN_T) topk_final_kernel(FilterArgs f) {
+  extern __shared__ unsigned fsm[];   // keys [n] | positions [n]
   __shared__ SelectSmem sm;
-  __shared__ unsigned n_sel_sm;
+  __shared__ unsigned seg_base[129];
+  __shared__ int overflow;
+  __shared__ unsigned max_count;
   const TopkArgs& a = f.a;
   const int row = blockIdx.x, i = row % a.Tq, tid = threadIdx.x;
   const int n_row = n_visible((long long)a.q_pos0 + i, a.m, a.n_entries);
   const unsigned thr = f.tau[row];
   int32_t* orow = a.out + size_t(row) * a.k;
-  const unsigned c = f.count[row];
-  if (c > unsigned(f.cap)) {   // overflow: the whole row (from global memory)
+  const unsigned* cnt = f.count + size_t(row) * f.n_seg;
+  if (tid < 32) {   // warp 0: the segments' offsets (lane owns segments 4 lane .. 4 lane + 3)
+    unsigned c4[4], sum = 0, mx = 0;
+    int ov = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = 4 * tid + u;
+      c4[u] = g < f.n_seg ? cnt[g] : 0u;
+      ov |= c4[u] > unsigned(FT_SEGCAP);
+      if (c4[u] > unsigned(FT_SEGCAP)) c4[u] = 0u;
+      sum += c4[u];
+      mx = max(mx, c4[u]);
+    }
+    unsigned incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (tid >= o) incl += y;
+    }
+    unsigned acc = incl - sum;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int g = 4 * tid + u;
+      if (g < f.n_seg) seg_base[g] = acc;
+      acc += c4[u];
+    }
+    const unsigned total = __shfl_sync(0xffffffffu, incl, 31);
+    ov = __any_sync(0xffffffffu, ov);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (tid == 0) {
+      seg_base[f.n_seg] = total;
+      overflow = ov;
+      max_count = mx;
+    }
+  }
+  __syncthreads();
+  if (overflow || seg_base[f.n_seg] > unsigned(f.stage_cap)) {   // the whole row, pruned by the threshold
     const float* srow = a.scores + size_t(row) * a.row_len;
     auto key_of = [&](int j) -> unsigned {
       const unsigned key = score_key(srow[j]);
       return key >= thr ? key : 0u;
     };
     auto emit = [&](int pos, int j) { orow[pos] = j; };
-    radix_topk<TK_T>(n_row, a.k, key_of, emit, sm);
+    radix_topk<FN_T>(n_row, a.k, key_of, emit, sm);
     return;
   }
-  const int n = int(c);
+  const int n = int(seg_base[f.n_seg]);
   unsigned* keys = fsm;
-  int32_t* pos = reinterpret_cast<int32_t*>(fsm + f.cap);
-  int32_t* sel = reinterpret_cast<int32_t*>(fsm + 2 * f.cap);
-  const unsigned* gk = f.ckey + size_t(row) * f.cap;
-  const int32_t* gp = f.cpos + size_t(row) * f.cap;
-  stage_keys(n, keys, gk, [](unsigned x) { return x; });
-  stage_keys(n, reinterpret_cast<unsigned*>(pos), gp, [](int32_t x) { return unsigned(x); });
-  int n_valid, k_rem;
-  const unsigned kth = radix_kth<TK_T>(n, a.k, [&](int j) { return keys[j]; }, sm, n_valid, k_rem);
-  // ties at kth: the k_rem lowest positions (key ~pos orders them)
-  unsigned pkth = 0u;
-  if (n_valid > a.k) {
-    int nv2, kr2;
-    pkth = radix_kth<TK_T>(n, k_rem, [&](int j) { return keys[j] == kth ? ~unsigned(pos[j]) : 0u; },
-                           sm, nv2, kr2);
-  }
-  if (tid == 0) n_sel_sm = 0u;
-  __syncthreads();
-  for (int j = tid; j < n; j += TK_T) {
-    const unsigned key = keys[j];
-    const bool take = n_valid <= a.k || key > kth || (key == kth && ~unsigned(pos[j]) >= pkth);
-    if (take) sel[atomicAdd(&n_sel_sm, 1u)] = pos[j];
-  }
-  __syncthreads();
-  const int n_sel = int(n_sel_sm);
-  int P = 1;
-  while (P < n_sel) P <<= 1;
-  for (int j = n_sel + tid; j < P; j += TK_T) sel[j] = 0x7FFFFFFF;
-  __syncthreads();
-  for (int len = 2; len <= P; len <<= 1) {   // bitonic sort, ascending
-    for (int d = len >> 1; d > 0; d >>= 1) {
-      for (int t = tid; t < P / 2; t += TK_T) {
-        const int lo = (t / d) * 2 * d + (t % d), hi = lo + d;
-        const bool up = (lo & len) == 0;
-        const int x = sel[lo], y = sel[hi];
-        if ((x > y) == up) { sel[lo] = y; sel[hi] = x; }
-      }
-      __syncthreads();
+  int32_t* pos = reinterpret_cast<int32_t*>(fsm + f.stage_cap);
+  // gather the segments in order: item x is entry x / n_seg of segment x % n_seg, so all
+  // segments' loads are in flight together
+  const unsigned n_items = unsigned(f.n_seg) * max_count;
+  for (unsigned x = tid; x < n_items; x += FN_T) {
+    const int g = int(x % unsigned(f.n_seg));
+    const unsigned j = x / unsigned(f.n_seg), b0 = seg_base[g];
+    if (j < seg_base[g + 1] - b0) {
+      const size_t off = (size_t(row) * f.n_seg + g) * FT_SEGCAP + j;
+      keys[b0 + j] = f.ckey[off];
+      pos[b0 + j] = f.cpos[off];
     }
   }
-  for (int j = tid; j < a.k; j += TK_T) orow[j] = j < n_sel ? sel[j] : -1;
+  __syncthreads();
+  auto key_of = [&](int j) -> unsigned { return keys[j]; };
+  auto emit = [&](int slot, int j) { orow[slot] = j >= 0 ? pos[j] : -1; };
+  radix_topk<FN_T>(n, a.k, key_of, emit, sm);
 }
 
 __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
@@ -939,7 +956,8 @@ size_t csa2_indexer_workspace_size(int B, int Tq, int n_entries, int nb, int blk
     const size_t n_chunks = size_t((row_len + TK_CHUNK - 1) / TK_CHUNK);   // thresholds
     bytes += 2 * align_up(size_t(B) * Tq * n_chunks * CSA2_MAX_TOPK * 4, 256);
     bytes += align_up(size_t(B) * Tq * size_t((row_len + 63) / 64) * 4, 256) +
-             2 * align_up(size_t(B) * Tq * 4, 256);
+             align_up(size_t(B) * Tq * 4, 256) +                                    // thresholds
+             align_up(size_t(B) * Tq * size_t((row_len + FT_SEG - 1) / FT_SEG) * 4, 256);   // counts
   }
   // FP4 query images and the step prefix table of the tensor-core scorer
   bytes += align_up(size_t(B) * Tq * SU_QROW_BYTES, 256) + align_up(size_t(Tq + 1) * 4, 256);
@@ -1029,7 +1047,9 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   const size_t prefix_bytes = align_up(size_t(Tq + 1) * 4, 256);
   const int nb64 = int((row_len + 63) / 64);
   const size_t bm64_bytes = chunked ? align_up(size_t(rows) * nb64 * 4, 256) : 0;
-  const size_t tau_bytes = chunked ? 2 * align_up(size_t(rows) * 4, 256) : 0;   // + counts
+  const size_t thr_bytes = chunked ? align_up(size_t(rows) * 4, 256) : 0;
+  const size_t tau_bytes = chunked ? thr_bytes + align_up(size_t(rows) * size_t((row_len + FT_SEG - 1) / FT_SEG) * 4, 256)
+                                   : 0;   // thresholds + per-segment counts
   const size_t need = (scores_out ? 0 : scores_bytes) + 2 * cand_bytes + qprep_bytes + prefix_bytes +
                       bm64_bytes + tau_bytes;
   if (!workspace || ws_bytes < need || !aligned256(workspace))
@@ -1040,7 +1060,7 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   int* prefix = reinterpret_cast<int*>(qprep + qprep_bytes);
   float* bm64_ws = reinterpret_cast<float*>(reinterpret_cast<char*>(prefix) + prefix_bytes);
   unsigned* tau = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(bm64_ws) + bm64_bytes);
-  unsigned* cand_count = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(tau) + tau_bytes / 2);
+  unsigned* cand_count = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(tau) + thr_bytes);
   // long dense rows: a threshold from the 64-key block maxima prunes the chunked selection;
   // the maxima are the caller's block maxima when those are 64-key blocks
   const float* bm64_src = nullptr;
@@ -1115,22 +1135,23 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
     topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
     note_launch();
   } else {
-    if (bm64_src) {
-      // threshold from the block maxima, one filtering pass, one exact select per row
-      const int cap = int(std::min<long long>((long long)n_chunks_tk * CSA2_MAX_TOPK, FT_CAP));
+    const int n_seg = int((row_len + FT_SEG - 1) / FT_SEG);
+    if (bm64_src && n_seg <= 128) {
+      // threshold from the block maxima, one filtering pass in position order, one exact
+      // select per row (the per-segment lists fit in the chunked selection's candidate area)
+      const int stage_cap = std::min(n_seg * FT_SEGCAP, 16384);
       FilterArgs fa{ta, tau, cand_count, reinterpret_cast<unsigned*>(cand_area),
-                    reinterpret_cast<int32_t*>(cand_area + cand_bytes), cap,
-                    int((row_len + FT_SEG - 1) / FT_SEG)};
-      const size_t fsm = (2 * size_t(cap) + CSA2_MAX_TOPK) * 4;
+                    reinterpret_cast<int32_t*>(cand_area + cand_bytes), n_seg, stage_cap};
+      const size_t fsm = 2 * size_t(stage_cap) * 4;
       cudaError_t e0 = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             int(fsm));
       if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
       topk_tau_kernel<<<unsigned(rows), TK_T, size_t(nb64 <= TAU_SMEM_BLOCKS ? nb64 : 0) * 4, st>>>(
-          ta, bm64_src, nb64, tau, cand_count);
+          ta, bm64_src, nb64, tau, nullptr);
       note_launch();
-      topk_filter_kernel<<<unsigned(rows * fa.n_seg), FT_T, 0, st>>>(fa);
+      topk_filter_kernel<<<unsigned(rows * n_seg), FT_T, 0, st>>>(fa);
       note_launch();
-      topk_final_kernel<<<unsigned(rows), TK_T, fsm, st>>>(fa);
+      topk_final_kernel<<<unsigned(rows), FN_T, fsm, st>>>(fa);
       note_launch();
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "indexer launch");

@@ -186,3 +186,4 @@ __device__ int radix_topk(int n, int k, KeyFn key_of, EmitFn emit, SelectSmem& s
 }
 
 }  // namespace csa2
+
