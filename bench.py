@@ -345,6 +345,25 @@ def run_ours(args, wl, rank, world, local_rank):
         handles.append((C.c_void_p * n_ev)(*[e.cuda_event for e in evs]))
     torch.cuda.synchronize()
 
+    # each timed step is one CUDA graph of the runner's launches (with its own per-stage
+    # event records), captured and uploaded before the timed region
+    graphs, launches_per_step = [], 0
+    if args.graph:
+        cap = torch.cuda.Stream(dev)
+        n0 = lib.csa2_kernel_launches()
+        for i in range(args.steps):
+            ops.L.check(lib.csa2_runner_set_timing(st.runner._h, handles[i], n_ev), "set_timing")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                st.step(cap.cuda_stream)
+            graphs.append(g)
+        launches_per_step = (lib.csa2_kernel_launches() - n0) // args.steps
+        lib.csa2_runner_set_timing(st.runner._h, None, 0)
+        for g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+        assert ops.last_device_status() == 0, "device-side check fired in the graph upload"
+
     clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
@@ -352,13 +371,20 @@ def run_ours(args, wl, rank, world, local_rank):
     clocks.start()
     time.sleep(0.5)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_launch0 = lib.csa2_kernel_launches()
-    e0.record(stream)
-    for i in range(args.steps):
-        ops.L.check(lib.csa2_runner_set_timing(st.runner._h, handles[i], n_ev), "set_timing")
-        st.step()
-    e1.record(stream)
-    n_launches = lib.csa2_kernel_launches() - n_launch0
+    if graphs:
+        e0.record(stream)
+        for g in graphs:
+            g.replay()
+        e1.record(stream)
+        n_launches = launches_per_step * args.steps
+    else:
+        n_launch0 = lib.csa2_kernel_launches()
+        e0.record(stream)
+        for i in range(args.steps):
+            ops.L.check(lib.csa2_runner_set_timing(st.runner._h, handles[i], n_ev), "set_timing")
+            st.step()
+        e1.record(stream)
+        n_launches = lib.csa2_kernel_launches() - n_launch0
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -415,6 +441,7 @@ def run_ours(args, wl, rank, world, local_rank):
                    "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
                    "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
                    "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",
+                   "launch": "cuda_graph" if args.graph else "direct",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": STAGE_NAMES[dom], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
@@ -487,6 +514,9 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode40")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each timed step as a captured CUDA graph (measured slower than direct "
+                         "launches for this step, so off by default)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("[bench] warm-up raised to 3 steps (minimum)", file=sys.stderr)

@@ -17,6 +17,14 @@ namespace csa2 {
 int fail(int status, const char* fmt, ...);
 // Counts one kernel launch (csa2_kernel_launches reads the total).
 void note_launch();
+// Records a timing event on `stream`; inside a stream capture it becomes an event-record
+// node of the graph (a plain record there would only mark a dependency).
+inline void record_stage_event(cudaEvent_t e, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(stream, &cs);
+  if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(e, stream, cudaEventRecordExternal);
+  else cudaEventRecord(e, stream);
+}
 int cuda_fail(cudaError_t e, const char* what);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -1124,8 +1124,8 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
       note_launch();
     }
   }
-  if (ev_score_end) cudaEventRecord(ev_score_end, st);
-  if (ev_topk_begin) cudaEventRecord(ev_topk_begin, st);
+  if (ev_score_end) record_stage_event(ev_score_end, st);
+  if (ev_topk_begin) record_stage_event(ev_topk_begin, st);
   TopkArgs ta{scores, int(row_len), Tq, q_pos0, m, n_entries, cand, nb, blk, k, topk_out};
   if (!chunked) {
     const int staged = int(row_len < TK_SMEM_KEYS ? row_len : TK_SMEM_KEYS);

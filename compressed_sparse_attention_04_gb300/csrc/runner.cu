@@ -64,7 +64,7 @@ cudaEvent_t stage_event(const csa2_runner* r, int layer, int stage, int end) {
 
 void mark(const csa2_runner* r, int layer, int stage, int end, void* stream) {
   cudaEvent_t e = stage_event(r, layer, stage, end);
-  if (e) cudaEventRecord(e, static_cast<cudaStream_t>(stream));
+  if (e) record_stage_event(e, static_cast<cudaStream_t>(stream));
 }
 
 int check_params(const csa2_step_params* p) {
