@@ -227,6 +227,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Bring `bytes` (a multiple of 16) at p into L2 without waiting for them.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 // Named barrier over n threads that also reduces a predicate (and / or) across them.
 __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
   uint32_t r;
@@ -337,12 +342,29 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       // row sources ready; the group agrees on whether the slot wait succeeded
       if (!bar_and(2 + grp, 64, okw)) { ok = false; break; }
       uint8_t* dst = KV + s * AF_KV_BYTES;
-#pragma unroll 4
-      for (int rep = 0; rep < AF_CH; ++rep) {   // 48 rows x 64 pieces of 16 bytes
-        const int uidx = rep * 64 + gt, r = uidx >> 6, ch = uidx & 63;
-        const uint16_t* src = row_src[s][r];
-        umma::cp_async16(dst + umma::kmajor_sw128_offset(r, ch * 8, AF_CH),
-                         src ? src + ch * 8 : a.swa, src ? 16u : 0u);
+      // 48 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are read eight
+      // at a time before their copies (an asynchronous copy orders the loads after it)
+#pragma unroll 1
+      for (int r0 = 0; r0 < AF_CH; r0 += 8) {
+        const uint16_t* sp[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) sp[u] = row_src[s][r0 + u];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u, gt * 8, AF_CH),
+                           sp[u] ? sp[u] + gt * 8 : a.swa, sp[u] ? 16u : 0u);
+      }
+      {   // while this chunk is in flight: the rows of the group's next chunk into L2
+        const int j = (c_begin + c + 2) * AF_CH + gt;
+        if (gt < AF_CH && c + 2 < n_ch && j < n_rows) {
+          const uint16_t* pf = nullptr;
+          if (j < a.k) {
+            if (e_next >= 0 && e_next < a.n_entries) pf = a.kv + (size_t(b) * a.n_cap + e_next) * 512;
+          } else {
+            pf = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
+          }
+          if (pf) prefetch_l2(pf, 1024);
+        }
       }
       if (c <= 1) {
         // the queries come with the first chunk of each group: heads 0..31 with chunk 0,
