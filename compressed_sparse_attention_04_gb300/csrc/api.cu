@@ -2,6 +2,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -11,6 +12,13 @@ namespace csa2 {
 
 std::atomic<unsigned long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("CSA2_NO_PDL");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
 
 namespace {
 thread_local char g_msg[512] = "";

@@ -53,6 +53,8 @@ struct AttnArgs {
 };
 
 __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) uint16_t qs[AT_HG][512];
   __shared__ __align__(16) uint16_t tile[AT_TILE][AT_LD];
   __shared__ int valid[AT_TILE];
@@ -249,6 +251,7 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool v) {
 }
 
 __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
+  pdl_wait();
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -298,6 +301,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_trigger();   // after this CTA holds its TMEM columns
   bool ok = true;
   float m_fin = -INFINITY, l_fin = 0.f;   // softmax lanes: this CTA's (max, sum) of their head
   // announce that this CTA runs; the matching wait precedes the first remote access
@@ -736,23 +740,12 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
     n_split = std::max(1, std::min(std::min(n_split, AF_MAX_SPLIT), n_ch_max));
     if (rows * n_split > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
     AttnFlashArgs fa{aa, n_split};
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(rows * n_split), 1, 1);
-    cfg.blockDim = dim3(AF_T, 1, 1);
-    cfg.dynamicSmemBytes = AF_SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(n_split);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e0 = cudaLaunchKernelEx(&cfg, attn_flash_kernel, fa);
+    e0 = launch_k(attn_flash_kernel, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1), AF_SMEM, st,
+                  unsigned(n_split), fa);
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: launch");
     note_launch();
   } else {
-    attn_simt_kernel<<<unsigned(rows * n_hg), AT_T, 0, st>>>(aa);
+    CSA2_LAUNCH("attn_simt launch", attn_simt_kernel, unsigned(rows * n_hg), AT_T, 0, st, aa);
     note_launch();
   }
   cudaError_t e = cudaGetLastError();

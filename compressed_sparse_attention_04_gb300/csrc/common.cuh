@@ -27,6 +27,56 @@ inline void record_stage_event(cudaEvent_t e, cudaStream_t stream) {
 }
 int cuda_fail(cudaError_t e, const char* what);
 
+// Programmatic dependent launch.  A kernel started by launch_k() may begin while the kernel
+// before it on the stream is still running (its launch and the placement of its CTAs then
+// overlap that kernel's tail).  Before pdl_wait() it may touch nothing but its own shared
+// memory: pdl_wait() returns once the previous kernel has completed and its writes are
+// visible.  pdl_trigger() lets the next kernel be launched; it must follow any TMEM
+// allocation, so that a waiting successor never holds columns this kernel needs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Whether launches carry the programmatic-serialization attribute (default on; the
+// environment variable CSA2_NO_PDL=1 turns it off).
+bool pdl_enabled();
+
+// Launch `kernel` on `st` with programmatic serialization and, when cluster_x > 1, a
+// cluster of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// launch_k() with a 1-CTA cluster shape, returning cuda_fail(error, where) on failure.
+#define CSA2_LAUNCH(where, kernel, grid, block, smem, stream, ...)                              \
+  do {                                                                                        \
+    const cudaError_t le_ = ::csa2::launch_k(kernel, dim3(grid), dim3(block), size_t(smem),   \
+                                             (cudaStream_t)(stream), 1u, __VA_ARGS__);        \
+    if (le_ != cudaSuccess) return ::csa2::cuda_fail(le_, where);                             \
+  } while (0)
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(GT) proj_gemm_kernel(const uint16_t* __restric
                                                        const uint16_t* __restrict__ W0,
                                                        const uint16_t* __restrict__ W1, int M,
                                                        int K, int Nout, float* __restrict__ P) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[GK][GM + 4];
   __shared__ float Bs[GK][GN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __re
                                                             const uint16_t* __restrict__ W1, int M,
                                                             int K, int Nout, int k_per_split,
                                                             float* __restrict__ P) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t empty_bar[PU_STAGES], done_bar;
@@ -118,6 +121,7 @@ __global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __re
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_trigger();   // after this CTA holds its TMEM columns
   const uint16_t* wsrc[PU_TILE / 32];             // this thread's 4 channel rows
   (void)wsrc;
 
@@ -208,6 +212,8 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
     int pos0, int G,
     const float* __restrict__ norm_w, float eps, float rope_base, uint16_t* __restrict__ kv_cache,
     int n_cap, float* __restrict__ kv_pre) {
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x;
   const size_t row0 = size_t(b) * T + size_t(g) * m;
   // channels 4t..4t+3 of up to m = 2 rows, projection (kv) and gate (z) halves: the split-K
@@ -308,6 +314,8 @@ __global__ void __launch_bounds__(128) index_k_kernel(const float* __restrict__ 
                                                       float rope_base, uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales, int n_cap,
                                                       float* __restrict__ k_out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float kv[E][512];
   const int j = threadIdx.x, lane = j & 31, w = j >> 5;
   const int total = B * G;
@@ -423,19 +431,14 @@ int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, cons
                                           int(PU_SMEM));
     if (e0 != cudaSuccess) return cuda_fail(e0, "compress: shared memory attribute");
     dim3 grid(nout / PU_TILE, ceil_div(M, PU_TILE), splits);
-    proj_umma_kernel<<<grid, PU_T, PU_SMEM, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
-                                                  (const uint16_t*)w_gate, M, hidden, nout,
-                                                  hidden / splits, P);
+    CSA2_LAUNCH("proj_umma launch", proj_umma_kernel, grid, PU_T, PU_SMEM, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, hidden / splits, P);
     note_launch();
   } else {
     dim3 grid(nout / GN, ceil_div(M, GM));
-    proj_gemm_kernel<<<grid, GT, 0, st>>>((const uint16_t*)x, (const uint16_t*)w_kv,
-                                          (const uint16_t*)w_gate, M, hidden, nout, P);
+    CSA2_LAUNCH("proj_gemm launch", proj_gemm_kernel, grid, GT, 0, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, P);
     note_launch();
   }
-  compress_epilogue_kernel<<<B * G, 128, 0, st>>>(P, splits, size_t(M) * nout, nout, B, T, m, pos0,
-                                                   G, norm_w, eps, rope_base, (uint16_t*)kv_cache,
-                                                   n_cap, kv_pre);
+  CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel, B * G, 128, 0, st, P, splits, size_t(M) * nout, nout, B, T, m, pos0, G, norm_w, eps, rope_base, (uint16_t*)kv_cache, n_cap, kv_pre);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
@@ -459,11 +462,9 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, con
   if (G == 0) return CSA2_OK;
   const int total = B * G;
   if (total <= 1024) {   // few entries (decode): more CTAs, each reading the weights once
-    index_k_kernel<2><<<ceil_div(total, 2), 128, 0, (cudaStream_t)stream>>>(
-        kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+    CSA2_LAUNCH("index_k launch", index_k_kernel<2>, ceil_div(total, 2), 128, 0, (cudaStream_t)stream, kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
   } else {
-    index_k_kernel<IK_E><<<ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream>>>(
-        kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+    CSA2_LAUNCH("index_k launch", index_k_kernel<IK_E>, ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream, kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
   }
   note_launch();
   cudaError_t e = cudaGetLastError();

@@ -61,6 +61,8 @@ struct ScoreArgs {
 };
 
 __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) float qh[32][128];
   __shared__ float wsh[32];
   __shared__ float sbuf[SC_T];
@@ -288,6 +290,8 @@ struct StepCursor {
 // MMA's B operand image (32 heads x 64 bytes, K-major, no swizzle) followed by its E4M3
 // block scales (4 bytes per head).  CTA 0 also writes the step prefix table.
 __global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep, int* prefix) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int scan[32];
   const int tid = threadIdx.x, blk4 = tid >> 5, lane = tid & 31;
   const long long row = blockIdx.x >> 5;
@@ -324,6 +328,7 @@ __global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep
 
 __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const __grid_constant__ CUtensorMap codes_map,
                                                           const __grid_constant__ CUtensorMap codes_map4) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* As = base;                                              // SU_STAGES x 2 tiles x 8 KB
@@ -359,6 +364,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_trigger();   // after this CTA holds its TMEM columns
 
   if (warp < 4) {
     // ---------------- producers: (without the tensor map) the codes and scale bytes by
@@ -652,6 +658,8 @@ struct TopkArgs {
 };
 
 __global__ void __launch_bounds__(TK_T) topk_kernel(TopkArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned keys_sm[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
@@ -692,6 +700,8 @@ struct TopkChunkArgs {
 constexpr int TAU_SMEM_BLOCKS = 8192;   // rows of up to 512 Ki entries stage their maxima
 __global__ void __launch_bounds__(TK_T) topk_tau_kernel(TopkArgs a, const float* bm64, int nb64,
                                                         unsigned* tau, unsigned* count) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned bkeys[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
@@ -724,6 +734,8 @@ struct FilterArgs {
   int stage_cap;        // candidates the final kernel's shared memory holds
 };
 __global__ void __launch_bounds__(FT_T) topk_filter_kernel(FilterArgs f) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NW = FT_T / 32, WSPAN = FT_SEG / NW;   // 1024 slots per warp
   __shared__ unsigned lkey[NW][FT_WCAP];
   __shared__ int32_t lpos[NW][FT_WCAP];
@@ -787,6 +799,8 @@ __global__ void __launch_bounds__(FT_T) topk_filter_kernel(FilterArgs f) {
 // score row instead.
 constexpr int FN_T = 256;
 __global__ void __launch_bounds__(FN_T) topk_final_kernel(FilterArgs f) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned fsm[];   // keys [n] | positions [n]
   __shared__ SelectSmem sm;
   __shared__ unsigned seg_base[129];
@@ -866,6 +880,8 @@ __global__ void __launch_bounds__(FN_T) topk_final_kernel(FilterArgs f) {
 }
 
 __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned keys_sm[];
   __shared__ SelectSmem sm;
   const TopkArgs& a = c.a;
@@ -891,6 +907,8 @@ __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
 }
 
 __global__ void __launch_bounds__(TK_T) topk_merge_kernel(TopkChunkArgs c) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned keys_sm[];
   __shared__ SelectSmem sm;
   const TopkArgs& a = c.a;
@@ -921,6 +939,8 @@ struct HsiArgs {
 };
 
 __global__ void __launch_bounds__(TK_T) hsi_kernel(HsiArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned bkeys[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
@@ -1113,14 +1133,14 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                    make_codes_map(&map1, codes, (long long)B * n_cap, 1) &&
                    make_codes_map(&map4, codes, (long long)B * n_cap, 4);
       if (sa.total_steps > 0) {
-        q_prep_kernel<<<unsigned(rows * 32), 128, 0, st>>>(sa, qprep, prefix);
+        CSA2_LAUNCH("q_prep launch", q_prep_kernel, unsigned(rows * 32), 128, 0, st, sa, qprep, prefix);
         note_launch();
         const long long grid = sa.total_steps < slots[dev] ? sa.total_steps : slots[dev];
-        score_fp4_kernel<<<unsigned(grid), SU_T, SU_SMEM, st>>>(sa, map1, map4);
+        CSA2_LAUNCH("score_fp4 launch", score_fp4_kernel, unsigned(grid), SU_T, SU_SMEM, st, sa, map1, map4);
         note_launch();
       }
     } else {
-      score_kernel<<<unsigned(rows * sa.n_chunks), SC_T, 0, st>>>(sa);
+      CSA2_LAUNCH("score launch", score_kernel, unsigned(rows * sa.n_chunks), SC_T, 0, st, sa);
       note_launch();
     }
   }
@@ -1132,7 +1152,7 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
     cudaError_t e0 = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           TK_SMEM_KEYS * 4);
     if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
-    topk_kernel<<<unsigned(rows), TK_T, size_t(staged) * 4, st>>>(ta);
+    CSA2_LAUNCH("topk launch", topk_kernel, unsigned(rows), TK_T, size_t(staged) * 4, st, ta);
     note_launch();
   } else {
     const int n_seg = int((row_len + FT_SEG - 1) / FT_SEG);
@@ -1146,12 +1166,11 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
       cudaError_t e0 = cudaFuncSetAttribute(topk_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             int(fsm));
       if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
-      topk_tau_kernel<<<unsigned(rows), TK_T, size_t(nb64 <= TAU_SMEM_BLOCKS ? nb64 : 0) * 4, st>>>(
-          ta, bm64_src, nb64, tau, nullptr);
+      CSA2_LAUNCH("topk_tau launch", topk_tau_kernel, unsigned(rows), TK_T, size_t(nb64 <= TAU_SMEM_BLOCKS ? nb64 : 0) * 4, st, ta, bm64_src, nb64, tau, nullptr);
       note_launch();
-      topk_filter_kernel<<<unsigned(rows * n_seg), FT_T, 0, st>>>(fa);
+      CSA2_LAUNCH("topk_filter launch", topk_filter_kernel, unsigned(rows * n_seg), FT_T, 0, st, fa);
       note_launch();
-      topk_final_kernel<<<unsigned(rows), FN_T, fsm, st>>>(fa);
+      CSA2_LAUNCH("topk_final launch", topk_final_kernel, unsigned(rows), FN_T, fsm, st, fa);
       note_launch();
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
@@ -1166,10 +1185,10 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                                 TK_SMEM_KEYS * 4);
     if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: top-k shared memory attribute");
     if (rows * (long long)n_chunks_tk > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "indexer: too many rows");
-    topk_chunk_kernel<<<unsigned(rows * n_chunks_tk), TK_T, size_t(TK_CHUNK) * 4, st>>>(tc);
+    CSA2_LAUNCH("topk_chunk launch", topk_chunk_kernel, unsigned(rows * n_chunks_tk), TK_T, size_t(TK_CHUNK) * 4, st, tc);
     note_launch();
     const long long n_merge = (long long)n_chunks_tk * k;
-    topk_merge_kernel<<<unsigned(rows), TK_T, size_t(n_merge <= TK_SMEM_KEYS ? n_merge : 0) * 4, st>>>(tc);
+    CSA2_LAUNCH("topk_merge launch", topk_merge_kernel, unsigned(rows), TK_T, size_t(n_merge <= TK_SMEM_KEYS ? n_merge : 0) * 4, st, tc);
     note_launch();
   }
   cudaError_t e = cudaGetLastError();
@@ -1190,8 +1209,7 @@ int csa2_hsi_candidates(const float* blockmax, int B, int Tq, int q_pos0, int n_
   const long long rows = (long long)B * Tq;
   if (rows > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "hsi: too many rows");
   HsiArgs ha{blockmax, ceil_div(n_entries, blk), Tq, q_pos0, m, n_entries, blk, nb, cand_out};
-  hsi_kernel<<<unsigned(rows), TK_T, size_t(ha.n_blocks <= TAU_SMEM_BLOCKS ? ha.n_blocks : 0) * 4,
-               (cudaStream_t)stream>>>(ha);
+  CSA2_LAUNCH("hsi launch", hsi_kernel, unsigned(rows), TK_T, size_t(ha.n_blocks <= TAU_SMEM_BLOCKS ? ha.n_blocks : 0) * 4, (cudaStream_t)stream, ha);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "hsi launch");
