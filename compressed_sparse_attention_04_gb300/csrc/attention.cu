@@ -8,10 +8,11 @@
 // [P3] "DeepSeek-V4.1-Flash：把百万 Token 的记忆，压缩成一套分级缓存" (junki.cn), §四:
 //      p_j = softmax_j(c_j . q / sqrt d), o = sum_j p_j c_j.
 //
-// attn_flash_kernel (64 heads): a cluster of 1-4 CTAs per query row splits the row's
-// attended list into chunks of 64 rows; each CTA streams its chunks through a two-slot
-// ring (16-byte asynchronous gathers into a K-major 128-byte-swizzled tile), tcgen05
-// computes S = Q C^T (64 heads x 64 rows, K = 512) so that one thread owns one head's
+// attn_flash_kernel (64 heads): a cluster of 1-4 CTAs per query row shares the row's
+// attended list (each CTA an equal part of the window rows and of the top-k slots); each CTA
+// streams its rows in chunks of 48 through a three-slot ring (16-byte asynchronous gathers
+// into a K-major 128-byte-swizzled tile), tcgen05
+// computes S = Q C^T (64 heads x 48 rows, K = 512) so that one thread owns one head's
 // scores, an online softmax writes P (bf16, a head per row), and tcgen05 accumulates O^T = C^T P^T
 // (512 dims x 64 heads) in TMEM, reading the SAME shared tile as the MN-major operand
 // (K = V).  The CTAs of a cluster combine their (max, sum, O) through distributed shared
@@ -179,12 +180,13 @@ __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
 
 
 // ---------------------------------------------------------------- pipelined tensor-core
-// attention (64 heads).  A row's attended list (top-k slots, then window rows) is cut into
-// chunks of 64 rows; the CTAs of one cluster take consecutive ranges of chunks and
+// attention (64 heads).  The CTAs of one cluster share a row's attended list: CTA r takes
+// its part of the window rows followed by its part of the top-k slots (window rows first:
+// the first chunk's copies need no top-k index), cut into chunks of 48 rows, and the CTAs
 // merge their partial results through distributed shared memory.  Per chunk:
-//   S   = Q C^T     (M = 64 heads, N = 64 rows, K = 512)   -> TMEM, one head per lane,
+//   S   = Q C^T     (M = 64 heads, N = 48 rows, K = 512)   -> TMEM, one head per lane,
 //                    so each head's softmax runs inside one thread;
-//   O^T += C^T P^T  (M = 4 x 128 dims, N = 64 heads, K = 64 rows) -> TMEM,
+//   O^T += C^T P^T  (M = 4 x 128 dims, N = 64 heads, K = 48 rows) -> TMEM,
 // reading the SAME shared tile of C (K = V) as a K-major and an MN-major operand.
 // The running maximum is only moved when a chunk exceeds it by more than 2^8 (probabilities
 // then stay below 256, exact in float32 sums); moving it rescales that head's columns of
@@ -277,10 +279,13 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   const int b = row / a.Tq, i = row % a.Tq;
   const long long t = (long long)a.q_pos0 + i;
   const long long lo = t - a.window + 1 > 0 ? t - a.window + 1 : 0;
-  const int n_rows = a.k + int(t - lo + 1);
-  const int n_ch_all = (n_rows + AF_CH - 1) / AF_CH;
-  const int c_begin = int((long long)n_ch_all * rank / u.n_split);
-  const int n_ch = int((long long)n_ch_all * (rank + 1) / u.n_split) - c_begin;
+  // this CTA's rows: window rows w0 .. w1 - 1, then top-k slots k0 .. k1 - 1 (the window
+  // first, so that the first chunk's copies need no top-k index)
+  const int n_win = int(t - lo + 1);
+  const int w0 = int((long long)n_win * rank / u.n_split), nw = int((long long)n_win * (rank + 1) / u.n_split) - w0;
+  const int k0 = int((long long)a.k * rank / u.n_split), nk_mine = int((long long)a.k * (rank + 1) / u.n_split) - k0;
+  const int n_mine = nw + nk_mine;
+  const int n_ch = (n_mine + AF_CH - 1) / AF_CH;
   const float scale_log2 = a.scale * 1.4426950408889634f;
 
   if (tid == 0) {
@@ -315,8 +320,8 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     // the group's next chunk, loaded one chunk ahead.
     const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
     auto topk_at = [&](int c) -> int {
-      const int j = (c_begin + c) * AF_CH + gt;
-      return (gt < AF_CH && c < n_ch && j < a.k) ? a.topk[size_t(row) * a.k + j] : -1;
+      const int j = c * AF_CH + gt;
+      return (gt < AF_CH && c < n_ch && j >= nw && j < n_mine) ? a.topk[size_t(row) * a.k + k0 + (j - nw)] : -1;
     };
     int e_next = topk_at(grp);
     for (int c = grp; c < n_ch && ok; c += 2) {
@@ -325,17 +330,17 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       e_next = topk_at(c + 2);
       bool okw = c < AF_SLOTS || umma::mbar_wait(&kv_empty[s], ((c / AF_SLOTS) - 1) & 1, &d_err_attn);
       {   // row sources (both warps of the group, whole warps for the ballot)
-        const int j = (c_begin + c) * AF_CH + gt;
+        const int j = c * AF_CH + gt;
         int okr = 0;
         const uint16_t* src = a.swa;   // any valid address for zero-filled copies
         if (gt >= AF_CH) {
           // (lanes past the chunk only complete the ballot)
-        } else if (j < a.k) {
+        } else if (j < nw) {
+          okr = 1;
+          src = a.swa + (size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0)) * 512;
+        } else if (j < n_mine) {
           if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
           if (e >= 0 && e < a.n_entries) { okr = 1; src = a.kv + (size_t(b) * a.n_cap + e) * 512; }
-        } else if (j < n_rows) {
-          okr = 1;
-          src = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
         }
         const unsigned m0 = __ballot_sync(0xffffffffu, okr);
         if (okw) {
@@ -359,13 +364,13 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
                            sp[u] ? sp[u] + gt * 8 : a.swa, sp[u] ? 16u : 0u);
       }
       {   // while this chunk is in flight: the rows of the group's next chunk into L2
-        const int j = (c_begin + c + 2) * AF_CH + gt;
-        if (gt < AF_CH && c + 2 < n_ch && j < n_rows) {
+        const int j = (c + 2) * AF_CH + gt;
+        if (gt < AF_CH && c + 2 < n_ch && j < n_mine) {
           const uint16_t* pf = nullptr;
-          if (j < a.k) {
-            if (e_next >= 0 && e_next < a.n_entries) pf = a.kv + (size_t(b) * a.n_cap + e_next) * 512;
-          } else {
-            pf = a.swa + (size_t(b) * a.S + size_t(lo + (j - a.k) - a.swa_pos0)) * 512;
+          if (j < nw) {
+            pf = a.swa + (size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0)) * 512;
+          } else if (e_next >= 0 && e_next < a.n_entries) {
+            pf = a.kv + (size_t(b) * a.n_cap + e_next) * 512;
           }
           if (pf) prefetch_l2(pf, 1024);
         }
