@@ -740,9 +740,15 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
       if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
       if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
     }
+    // CTAs per row: all CTAs in one wave, and the estimated time of a row's chunks (about
+    // 1.5 us each, per CTA) plus the cluster merge (about 4 us) the smallest
     const int n_ch_max = ceil_div(k + window, AF_CH);
-    int n_split = int(sms_cache[dev] / rows);
-    n_split = std::max(1, std::min(std::min(n_split, AF_MAX_SPLIT), n_ch_max));
+    const int n_fit = std::max(1, std::min(int(sms_cache[dev] / rows), AF_MAX_SPLIT));
+    int n_split = 1;
+    for (int n = 2; n <= n_fit; ++n) {
+      const int t_n = 3 * ceil_div(n_ch_max, n) + 8, t_best = 3 * ceil_div(n_ch_max, n_split) + (n_split > 1 ? 8 : 0);
+      if (t_n < t_best) n_split = n;
+    }
     if (rows * n_split > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
     AttnFlashArgs fa{aa, n_split};
     e0 = launch_k(attn_flash_kernel, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1), AF_SMEM, st,
