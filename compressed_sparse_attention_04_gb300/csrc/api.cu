@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -12,6 +13,15 @@ namespace csa2 {
 
 std::atomic<unsigned long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+RopeTurns rope_turns(float rope_base) {
+  RopeTurns t;
+  const long double two_pi = 6.283185307179586476925286766559005768L;
+  for (int i = 0; i < 32; ++i) {
+    const long double f = powl((long double)rope_base, -(long double)i / 32.0L) / two_pi;
+    t.f[i] = (unsigned long long)llroundl(ldexpl(f, 64));   // f < 1/(2 pi): below 2^62
+  }
+  return t;
+}
 bool pdl_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("CSA2_NO_PDL");

@@ -179,14 +179,20 @@ __device__ __forceinline__ uint32_t fp4_quant_lane(float v, uint32_t& scale_byte
   return sign | e2m1_rne_mag(fabsf(u));
 }
 
-// RoPE angle cos/sin for position pos and pair i (of 32), computed in double.
-__device__ __forceinline__ void rope_cs(long long pos, int i, float rope_base, float& c,
-                                        float& s) {
-  const double th = pow(double(rope_base), -double(i) / 32.0);
-  double sd, cd;
-  sincos(double(pos) * th, &sd, &cd);
-  c = float(cd);
-  s = float(sd);
+// RoPE angles.  Pair i (of 32) of the last 64 dims turns by pos * theta_i, theta_i =
+// base^(-i/32).  t.f[i] holds theta_i / (2 pi) as a 64-bit binary fraction (computed on the
+// host in extended precision), so the wrapping 64-bit product pos * t.f[i] is the angle's
+// fractional turn; read as a signed fraction in [-1/2, 1/2) turn it goes to float for sincospif.
+// Angle error about 2e-7 rad for any position below 2^40; no double-precision arithmetic.
+struct RopeTurns {
+  unsigned long long f[32];
+};
+RopeTurns rope_turns(float rope_base);
+
+__device__ __forceinline__ void rope_cs(long long pos, int i, const RopeTurns& t, float& c, float& s) {
+  const unsigned long long x = (unsigned long long)pos * t.f[i];
+  const float turns = __ll2float_rn((long long)x) * 5.42101086242752217e-20f;   // 2^-64
+  sincospif(2.0f * turns, &s, &c);
 }
 
 }  // namespace csa2

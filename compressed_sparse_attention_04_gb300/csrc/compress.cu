@@ -205,46 +205,61 @@ int proj_splits(int M, int K, int Nout) {
   return s;
 }
 
-// One block of 128 threads per entry (b, g); thread owns channels 4t..4t+3.  P holds
-// n_split partial products (split-K) summed here in order.
-__global__ void __launch_bounds__(128) compress_epilogue_kernel(
+// One block of 512 threads per entry (b, g): thread t < 128 of split group sg = tid / 128
+// sums channels 4t..4t+3 of splits [sg * n / 4, (sg + 1) * n / 4) of the n_split partial
+// products (split-K), all its loads in flight together; group 0 then adds the four group sums
+// in group order and finishes the entry (the summation order is fixed: deterministic).
+__global__ void __launch_bounds__(512) compress_epilogue_kernel(
     const float* __restrict__ P, int n_split, size_t split_stride, int Nout, int B, int T, int m,
     int pos0, int G,
-    const float* __restrict__ norm_w, float eps, float rope_base, uint16_t* __restrict__ kv_cache,
+    const float* __restrict__ norm_w, float eps, const RopeTurns rt, uint16_t* __restrict__ kv_cache,
     int n_cap, float* __restrict__ kv_pre) {
   pdl_wait();
   pdl_trigger();
-  const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x;
+  __shared__ float4 part[3][128][4];   // groups 1..3: their sums per thread
+  const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x & 127, sg = threadIdx.x >> 7;
   const size_t row0 = size_t(b) * T + size_t(g) * m;
-  // channels 4t..4t+3 of up to m = 2 rows, projection (kv) and gate (z) halves: the split-K
-  // partials are summed in split order; four splits' loads are in flight at a time
+  // channels 4t..4t+3 of up to m = 2 rows, projection (kv) and gate (z) halves
   const int nv = m == 1 ? 1 : 4;   // float4 vectors per split: kv0 | z0 kv1 z1
   size_t off[4];
   off[0] = row0 * Nout + 4 * t;
   off[1] = row0 * Nout + 512 + 4 * t;
   off[2] = (row0 + 1) * Nout + 4 * t;
   off[3] = (row0 + 1) * Nout + 512 + 4 * t;
+  const int sp0 = sg * n_split / 4, sp1 = (sg + 1) * n_split / 4;
   float4 acc[4];
 #pragma unroll
   for (int v = 0; v < 4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int sp0 = 0; sp0 < n_split; sp0 += 4) {
+  for (int base = sp0; base < sp1; base += 4) {
     float4 ld[4][4];
 #pragma unroll
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int v = 0; v < 4; ++v)
-        ld[q][v] = (sp0 + q < n_split && v < nv)
-                       ? *reinterpret_cast<const float4*>(P + off[v] + size_t(sp0 + q) * split_stride)
+        ld[q][v] = (base + q < sp1 && v < nv)
+                       ? *reinterpret_cast<const float4*>(P + off[v] + size_t(base + q) * split_stride)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        if (sp0 + q >= n_split || v >= nv) continue;
-        if (sp0 + q == 0) { acc[v] = ld[q][v]; continue; }
+        if (base + q >= sp1 || v >= nv) continue;
         acc[v].x += ld[q][v].x; acc[v].y += ld[q][v].y; acc[v].z += ld[q][v].z; acc[v].w += ld[q][v].w;
       }
   }
+  if (sg > 0) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) part[sg - 1][t][v] = acc[v];
+  }
+  __syncthreads();
+  if (sg > 0) return;   // the rest runs in group 0 (4 warps)
+#pragma unroll
+  for (int q = 0; q < 3; ++q)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const float4 o = part[q][t][v];
+      acc[v].x += o.x; acc[v].y += o.y; acc[v].z += o.z; acc[v].w += o.w;
+    }
   float pooled[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -271,7 +286,7 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   __shared__ float red[4];
   if ((t & 31) == 0) red[t >> 5] = ss;
-  __syncthreads();
+  asm volatile("bar.sync 1, 128;" ::: "memory");
   const float tot = (red[0] + red[1]) + (red[2] + red[3]);
   const float inv = 1.0f / sqrtf(tot / 512.0f + eps);
   float y[4];
@@ -287,7 +302,7 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
     for (int pr = 0; pr < 2; ++pr) {
       const int i = (4 * t - 448) / 2 + pr;
       float c, s;
-      rope_cs(pos, i, rope_base, c, s);
+      rope_cs(pos, i, rt, c, s);
       const float a = y[2 * pr], bb = y[2 * pr + 1];
       y[2 * pr] = a * c - bb * s;
       y[2 * pr + 1] = a * s + bb * c;
@@ -304,57 +319,56 @@ __global__ void __launch_bounds__(128) compress_epilogue_kernel(
 
 constexpr int IK_E = 8;  // entries per block (few entries, as in decode: 2)
 
-// 128 threads: thread j computes key dim j for E entries; warp w then quantises
-// block w (dims 32w..32w+31) of each entry.  The weight row is read 128 bytes at a time
-// (eight 16-byte loads in flight); the sum over the 512 inputs runs in index order.
+// 512 threads: thread j + 128 qk computes key dim j for E entries over inputs 128 qk ..
+// 128 qk + 127 (its 16 weight loads in flight together); the four quarter sums are added in
+// quarter order (deterministic), then warp w of the first 128 threads quantises block w
+// (dims 32w..32w+31) of each entry.
 template <int E>
-__global__ void __launch_bounds__(128) index_k_kernel(const float* __restrict__ kv_pre, int B,
+__global__ void __launch_bounds__(512) index_k_kernel(const float* __restrict__ kv_pre, int B,
                                                       int G, int entry0, int m,
                                                       const uint16_t* __restrict__ w_ik,
-                                                      float rope_base, uint8_t* __restrict__ codes,
+                                                      const RopeTurns rt, uint8_t* __restrict__ codes,
                                                       uint8_t* __restrict__ scales, int n_cap,
                                                       float* __restrict__ k_out) {
   pdl_wait();
   pdl_trigger();
   __shared__ float kv[E][512];
-  const int j = threadIdx.x, lane = j & 31, w = j >> 5;
+  __shared__ float part[3][E][128];
+  const int tid = threadIdx.x, j = tid & 127, qk = tid >> 7, lane = tid & 31, w = (tid >> 5) & 3;
   const int total = B * G;
   const int e0 = blockIdx.x * E;
-  {
-    float4 v4[E];   // all of this thread's loads in flight together
-#pragma unroll
-    for (int r = 0; r < E; ++r) {
-      const int idx = (r * 128 + j) * 4, e = e0 + idx / 512;
-      v4[r] = (e < total) ? *reinterpret_cast<const float4*>(kv_pre + size_t(e) * 512 + idx % 512)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int r = 0; r < E; ++r) {
-      const int idx = (r * 128 + j) * 4;
-      *reinterpret_cast<float4*>(&kv[idx / 512][idx % 512]) = v4[r];
-    }
+  for (int idx = tid * 4; idx < E * 512; idx += 512 * 4) {
+    const int e = e0 + idx / 512;
+    *reinterpret_cast<float4*>(&kv[idx / 512][idx % 512]) =
+        (e < total) ? *reinterpret_cast<const float4*>(kv_pre + size_t(e) * 512 + idx % 512)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  uint4 vv[16];
+  const uint4* wr = reinterpret_cast<const uint4*>(w_ik + size_t(j) * 512 + 128 * qk);
+#pragma unroll
+  for (int u8 = 0; u8 < 16; ++u8) vv[u8] = wr[u8];
   __syncthreads();
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const uint4* wr = reinterpret_cast<const uint4*>(w_ik + size_t(j) * 512);
-#pragma unroll 1
-  for (int h0 = 0; h0 < 512; h0 += 128) {
-    uint4 vv[16];
 #pragma unroll
-    for (int u8 = 0; u8 < 16; ++u8) vv[u8] = wr[(h0 >> 3) + u8];
+  for (int u8 = 0; u8 < 16; ++u8) {
+    const uint16_t* pv = reinterpret_cast<const uint16_t*>(&vv[u8]);
 #pragma unroll
-    for (int u8 = 0; u8 < 16; ++u8) {
-      const uint16_t* pv = reinterpret_cast<const uint16_t*>(&vv[u8]);
+    for (int u = 0; u < 8; ++u) {
+      const float wv = bf16_to_f32(pv[u]);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float wv = bf16_to_f32(pv[u]);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = fmaf(wv, kv[e][h0 + 8 * u8 + u], acc[e]);
-      }
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wv, kv[e][128 * qk + 8 * u8 + u], acc[e]);
     }
   }
+  if (qk > 0) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) part[qk - 1][e][j] = acc[e];
+  }
+  __syncthreads();
+  if (qk > 0) return;   // the rest runs in the first 128 threads
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = ((acc[e] + part[0][e][j]) + part[1][e][j]) + part[2][e][j];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int ei = e0 + e;
@@ -365,7 +379,7 @@ __global__ void __launch_bounds__(128) index_k_kernel(const float* __restrict__ 
     const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
     if (j >= 64) {
       float c, s;
-      rope_cs(ent * m, (j - 64) >> 1, rope_base, c, s);
+      rope_cs(ent * m, (j - 64) >> 1, rt, c, s);
       v = (j & 1) ? (partner * s + v * c) : (v * c - partner * s);
     }
     if (k_out) k_out[size_t(ei) * 128 + j] = v;
@@ -438,7 +452,7 @@ int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, cons
     CSA2_LAUNCH("proj_gemm launch", proj_gemm_kernel, grid, GT, 0, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, P);
     note_launch();
   }
-  CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel, B * G, 128, 0, st, P, splits, size_t(M) * nout, nout, B, T, m, pos0, G, norm_w, eps, rope_base, (uint16_t*)kv_cache, n_cap, kv_pre);
+  CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel, B * G, 512, 0, st, P, splits, size_t(M) * nout, nout, B, T, m, pos0, G, norm_w, eps, rope_turns(rope_base), (uint16_t*)kv_cache, n_cap, kv_pre);
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
@@ -462,9 +476,9 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, con
   if (G == 0) return CSA2_OK;
   const int total = B * G;
   if (total <= 1024) {   // few entries (decode): more CTAs, each reading the weights once
-    CSA2_LAUNCH("index_k launch", index_k_kernel<2>, ceil_div(total, 2), 128, 0, (cudaStream_t)stream, kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+    CSA2_LAUNCH("index_k launch", index_k_kernel<2>, ceil_div(total, 2), 512, 0, (cudaStream_t)stream, kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_turns(rope_base), codes, scales, n_cap, k_out);
   } else {
-    CSA2_LAUNCH("index_k launch", index_k_kernel<IK_E>, ceil_div(total, IK_E), 128, 0, (cudaStream_t)stream, kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_base, codes, scales, n_cap, k_out);
+    CSA2_LAUNCH("index_k launch", index_k_kernel<IK_E>, ceil_div(total, IK_E), 512, 0, (cudaStream_t)stream, kv_pre, B, G, entry0, m, (const uint16_t*)w_ik, rope_turns(rope_base), codes, scales, n_cap, k_out);
   }
   note_launch();
   cudaError_t e = cudaGetLastError();
