@@ -526,30 +526,39 @@ def run_e2e(st, args, stream):
             out.append(g["swa_kv"][:, -1])
         return out
     dst_in = [dev_inputs(0), dev_inputs(1)]
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+    # NC streams per direction, so that the copies can use more than one copy engine
+    # (measured: 1 stream 2.44 ms per step, 2 2.17, 4 2.03, 8 2.52)
+    NC = 4
+    ups = [torch.cuda.Stream(dev) for _ in range(NC)]
+    downs = [torch.cuda.Stream(dev) for _ in range(NC)]
+    in_ready = [[torch.cuda.Event() for _ in range(NC)] for _ in range(2)]
     computed = [torch.cuda.Event(), torch.cuda.Event()]
-    out_read = [torch.cuda.Event(), torch.cuda.Event()]
+    out_read = [[torch.cuda.Event() for _ in range(NC)] for _ in range(2)]
     used = [False, False]
 
     def one(s):
         si = s & 1
-        with torch.cuda.stream(up):
+        for u, up in enumerate(ups):
+            with torch.cuda.stream(up):
+                if used[si]:
+                    up.wait_event(computed[si])      # step s - 2 has read these inputs
+                for j, (d, (_, h)) in enumerate(zip(dst_in[si], host_in)):
+                    if j % NC == u:
+                        d.copy_(h, non_blocking=True)
+                in_ready[si][u].record(up)
+        for u in range(NC):
+            stream.wait_event(in_ready[si][u])
             if used[si]:
-                up.wait_event(computed[si])          # step s - 2 has read these inputs
-            for d, (_, h) in zip(dst_in[si], host_in):
-                d.copy_(h, non_blocking=True)
-            in_ready[si].record(up)
-        stream.wait_event(in_ready[si])
-        if used[si]:
-            stream.wait_event(out_read[si])          # step s - 2's outputs are down
+                stream.wait_event(out_read[si][u])   # step s - 2's outputs are down
         st.runner.step(st.params, ios[si], st.ws, stream.cuda_stream)
         computed[si].record(stream)
-        with torch.cuda.stream(down):
-            down.wait_event(computed[si])
-            for h, g in zip(host_out, sets[si]):
-                h.copy_(g["out"], non_blocking=True)
-            out_read[si].record(down)
+        for u, down in enumerate(downs):
+            with torch.cuda.stream(down):
+                down.wait_event(computed[si])
+                for j, (h, g) in enumerate(zip(host_out, sets[si])):
+                    if j % NC == u:
+                        h.copy_(g["out"], non_blocking=True)
+                out_read[si][u].record(down)
         used[si] = True
 
     for s in range(args.warmup):
@@ -558,10 +567,12 @@ def run_e2e(st, args, stream):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
     e0.record(stream)
-    up.wait_event(e0)
+    for up in ups:
+        up.wait_event(e0)
     for s in range(args.steps):
         one(args.warmup + s)
-    stream.wait_stream(down)
+    for down in downs:
+        stream.wait_stream(down)
     e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
