@@ -286,6 +286,29 @@ def time_oracle(wl, budget_s=12.0, max_reps=4, sample=None):
     return reps, total
 
 
+# ----------------------------------------------------------------------------- ranks
+# Multi-GPU runs are independent replicas (decode sequences share nothing): each rank builds
+# its own caches from its own seeds and times the same step; the job's time is the slowest
+# rank's and its throughput counts every rank's batch.  No collective touches the data path.
+def replica_seed_base(rank):
+    return 5000 + 100 * rank
+
+
+def max_over_ranks(ms, world, device=None):
+    """The slowest rank's time; every rank returns it (an all-reduce of one number)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], device=device if device is not None else "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(batch, world, ms):
+    """Tokens per second of the whole job: every rank decodes `batch` sequences per step."""
+    return batch * world / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- main arms
 def run_reference(args, wl, rank, world):
     if rank != 0:
@@ -323,7 +346,7 @@ def run_ours(args, wl, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     log = (lambda *a: print(*a, file=sys.stderr, flush=True)) if rank == 0 else (lambda *a: None)
-    st = Stack(wl, dev, seed_base=5000 + 100 * rank, log=log)
+    st = Stack(wl, dev, seed_base=replica_seed_base(rank), log=log)
     stream = torch.cuda.current_stream(dev)
     B = wl["B"]
     for _ in range(args.warmup):
@@ -395,11 +418,7 @@ def run_ours(args, wl, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
         lib.csa2_runner_set_timing(st.runner._h, None, 0)
-        ms_ = t0.elapsed_time(t1) / args.steps
-        if world > 1:
-            tt = torch.tensor([ms_], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms_ = float(tt.item())
+        ms_ = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
         assert ops.last_device_status() == 0, "device-side check fired during the timed steps"
         return ms_, launches
 
@@ -450,7 +469,7 @@ def run_ours(args, wl, rank, world, local_rank):
     if rank != 0:
         return 0
     line = {
-        "metric": METRIC, "value": B * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": job_throughput(B, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"csa2_decode_40layer_b{B}_ctx{wl['C']}", "batch": B,
