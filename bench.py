@@ -371,7 +371,7 @@ def run_ours(args, wl, rank, world, local_rank):
     # Two timed passes of K steps each.  Pass A gives the headline: the runner records no
     # per-stage events.  Pass B repeats the K steps with one event pair per (layer, stage) on
     # the launching stream, for the per-stage times and the roofline of the dominant kernel.
-    # By default every step of a pass is one CUDA graph of the runner's launches, captured
+    # With --graph every step of a pass is one CUDA graph of the runner's launches, captured
     # and uploaded before the timed region.
     def make_graphs(with_events):
         cap = torch.cuda.Stream(dev)
@@ -610,9 +610,9 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode40")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-graph", dest="graph", action="store_false",
-                    help="launch each timed step's kernels directly instead of replaying the step as a "
-                         "captured CUDA graph")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay each timed step as a captured CUDA graph (measured 1.607 ms per step "
+                         "against 1.587 ms for direct launches with programmatic dependent launch)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("[bench] warm-up raised to 3 steps (minimum)", file=sys.stderr)

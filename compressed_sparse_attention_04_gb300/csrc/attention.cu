@@ -55,7 +55,6 @@ struct AttnArgs {
 
 __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
   pdl_wait();
-  pdl_trigger();
   __shared__ __align__(16) uint16_t qs[AT_HG][512];
   __shared__ __align__(16) uint16_t tile[AT_TILE][AT_LD];
   __shared__ int valid[AT_TILE];
@@ -306,7 +305,6 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
-  pdl_trigger();   // after this CTA holds its TMEM columns
   bool ok = true;
   float m_fin = -INFINITY, l_fin = 0.f;   // softmax lanes: this CTA's (max, sum) of their head
   // announce that this CTA runs; the matching wait precedes the first remote access

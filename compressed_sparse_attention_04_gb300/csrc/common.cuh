@@ -28,13 +28,13 @@ inline void record_stage_event(cudaEvent_t e, cudaStream_t stream) {
 int cuda_fail(cudaError_t e, const char* what);
 
 // Programmatic dependent launch.  A kernel started by launch_k() may begin while the kernel
-// before it on the stream is still running (its launch and the placement of its CTAs then
-// overlap that kernel's tail).  Before pdl_wait() it may touch nothing but its own shared
-// memory: pdl_wait() returns once the previous kernel has completed and its writes are
-// visible.  pdl_trigger() lets the next kernel be launched; it must follow any TMEM
-// allocation, so that a waiting successor never holds columns this kernel needs.
+// before it on the stream is finishing: its launch then overlaps that kernel's last CTAs.
+// Before pdl_wait() it may touch nothing but its own shared memory: pdl_wait() returns once
+// the previous kernel has completed and its writes are visible.  Kernels do not trigger their
+// successor early (griddepcontrol.launch_dependents): successor CTAs placed beside a running
+// kernel and waiting for it slowed it down (measured: a 64-row top-k 11 -> 20 us), so each
+// kernel's successor is released as its CTAs exit.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Whether launches carry the programmatic-serialization attribute (default on; the
 // environment variable CSA2_NO_PDL=1 turns it off).

@@ -34,7 +34,6 @@ __global__ void __launch_bounds__(GT) proj_gemm_kernel(const uint16_t* __restric
                                                        const uint16_t* __restrict__ W1, int M,
                                                        int K, int Nout, float* __restrict__ P) {
   pdl_wait();
-  pdl_trigger();
   __shared__ float As[GK][GM + 4];
   __shared__ float Bs[GK][GN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -121,7 +120,6 @@ __global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __re
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
-  pdl_trigger();   // after this CTA holds its TMEM columns
   const uint16_t* wsrc[PU_TILE / 32];             // this thread's 4 channel rows
   (void)wsrc;
 
@@ -215,7 +213,6 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
     const float* __restrict__ norm_w, float eps, const RopeTurns rt, uint16_t* __restrict__ kv_cache,
     int n_cap, float* __restrict__ kv_pre) {
   pdl_wait();
-  pdl_trigger();
   __shared__ float4 part[3][128][4];   // groups 1..3: their sums per thread
   const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x & 127, sg = threadIdx.x >> 7;
   const size_t row0 = size_t(b) * T + size_t(g) * m;
@@ -331,7 +328,6 @@ __global__ void __launch_bounds__(512) index_k_kernel(const float* __restrict__ 
                                                       uint8_t* __restrict__ scales, int n_cap,
                                                       float* __restrict__ k_out) {
   pdl_wait();
-  pdl_trigger();
   __shared__ float kv[E][512];
   __shared__ float part[3][E][128];
   const int tid = threadIdx.x, j = tid & 127, qk = tid >> 7, lane = tid & 31, w = (tid >> 5) & 3;

@@ -62,7 +62,6 @@ struct ScoreArgs {
 
 __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
   pdl_wait();
-  pdl_trigger();
   __shared__ __align__(16) float qh[32][128];
   __shared__ float wsh[32];
   __shared__ float sbuf[SC_T];
@@ -291,7 +290,6 @@ struct StepCursor {
 // block scales (4 bytes per head).  CTA 0 also writes the step prefix table.
 __global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep, int* prefix) {
   pdl_wait();
-  pdl_trigger();
   __shared__ int scan[32];
   const int tid = threadIdx.x, blk4 = tid >> 5, lane = tid & 31;
   const long long row = blockIdx.x >> 5;
@@ -364,7 +362,6 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
-  pdl_trigger();   // after this CTA holds its TMEM columns
 
   if (warp < 4) {
     // ---------------- producers: (without the tensor map) the codes and scale bytes by
@@ -629,6 +626,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
 
 constexpr int TK_T = 512;
 constexpr int TK_SMEM_KEYS = 32768;   // rows up to this length are staged in shared memory
+constexpr int TK_POOL_SMEM = 1024;    // candidate blocks staged in shared memory (pool mode)
 
 // Stage n words into shared memory with eight loads in flight per thread: the loads are
 // unconditional (index clamped to n - 1) so that none waits behind a branch on another's
@@ -659,7 +657,6 @@ struct TopkArgs {
 
 __global__ void __launch_bounds__(TK_T) topk_kernel(TopkArgs a) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ unsigned keys_sm[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
@@ -672,9 +669,22 @@ __global__ void __launch_bounds__(TK_T) topk_kernel(TopkArgs a) {
   auto key_of = [&](int j) -> unsigned { return staged ? keys_sm[j] : score_key(srow[j]); };
   int32_t* orow = a.out + size_t(row) * a.k;
   const int32_t* crow = pool ? a.cand + size_t(row) * a.nb : nullptr;
+  // pool mode: the candidate blocks' first entries, in shared memory so that emitting a
+  // selected slot needs no dependent global load
+  __shared__ int cbase[TK_POOL_SMEM];
+  const bool cstaged = pool && a.nb <= TK_POOL_SMEM;
+  if (cstaged)
+    for (int c = threadIdx.x; c < a.nb; c += TK_T) cbase[c] = crow[c] * a.blk;
+  __syncthreads();
   auto emit = [&](int pos, int j) {
     int32_t v = -1;
-    if (j >= 0) v = pool ? crow[j / a.blk] * a.blk + (j % a.blk) : j;
+    if (j >= 0) {
+      if (!pool) v = j;
+      else {
+        const int c = j / a.blk;
+        v = (cstaged ? cbase[c] : crow[c] * a.blk) + (j - c * a.blk);
+      }
+    }
     orow[pos] = v;
   };
   radix_topk<TK_T>(n, a.k, key_of, emit, sm);
@@ -701,7 +711,6 @@ constexpr int TAU_SMEM_BLOCKS = 8192;   // rows of up to 512 Ki entries stage th
 __global__ void __launch_bounds__(TK_T) topk_tau_kernel(TopkArgs a, const float* bm64, int nb64,
                                                         unsigned* tau, unsigned* count) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ unsigned bkeys[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
@@ -735,7 +744,6 @@ struct FilterArgs {
 };
 __global__ void __launch_bounds__(FT_T) topk_filter_kernel(FilterArgs f) {
   pdl_wait();
-  pdl_trigger();
   constexpr int NW = FT_T / 32, WSPAN = FT_SEG / NW;   // 1024 slots per warp
   __shared__ unsigned lkey[NW][FT_WCAP];
   __shared__ int32_t lpos[NW][FT_WCAP];
@@ -800,7 +808,6 @@ __global__ void __launch_bounds__(FT_T) topk_filter_kernel(FilterArgs f) {
 constexpr int FN_T = 256;
 __global__ void __launch_bounds__(FN_T) topk_final_kernel(FilterArgs f) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ unsigned fsm[];   // keys [n] | positions [n]
   __shared__ SelectSmem sm;
   __shared__ unsigned seg_base[129];
@@ -881,7 +888,6 @@ __global__ void __launch_bounds__(FN_T) topk_final_kernel(FilterArgs f) {
 
 __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ unsigned keys_sm[];
   __shared__ SelectSmem sm;
   const TopkArgs& a = c.a;
@@ -908,7 +914,6 @@ __global__ void __launch_bounds__(TK_T) topk_chunk_kernel(TopkChunkArgs c) {
 
 __global__ void __launch_bounds__(TK_T) topk_merge_kernel(TopkChunkArgs c) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ unsigned keys_sm[];
   __shared__ SelectSmem sm;
   const TopkArgs& a = c.a;
@@ -940,7 +945,6 @@ struct HsiArgs {
 
 __global__ void __launch_bounds__(TK_T) hsi_kernel(HsiArgs a) {
   pdl_wait();
-  pdl_trigger();
   extern __shared__ unsigned bkeys[];
   __shared__ SelectSmem sm;
   const int row = blockIdx.x, i = row % a.Tq;
