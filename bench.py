@@ -499,8 +499,9 @@ def run_ours(args, wl, rank, world, local_rank):
 
 def run_e2e(st, args, stream):
     """Same step measured through the C ABI with host inputs and outputs: each step copies
-    its inputs (queries, indexer queries/weights, new hidden states, newest window row) from
-    pinned host memory and reads every layer's output back.  As a server would, steps are
+    its inputs (every layer's queries, indexer queries/weights, new hidden states, newest window
+    row) from pinned host memory and reads the step's result, the last layer's output, back
+    (the other layers' outputs are what a model's next layers consume on the device).  As a server would, steps are
     pipelined over two device copies of the per-step inputs and outputs (caches and weights
     shared): step s + 1's inputs go up on one copy stream and step s - 1's outputs come down
     on another while step s computes; events keep each buffer's uses in order.  Every step's
@@ -532,9 +533,9 @@ def run_e2e(st, args, stream):
         h.copy_(row)
         host_in.append(("swa_row", h))
         h2d += row.numel() * row.element_size()
-        ho = torch.empty_like(g["out"], device="cpu").pin_memory()
-        host_out.append(ho)
-        d2h += g["out"].numel() * g["out"].element_size()
+    g = st.layers[-1]
+    host_out.append(torch.empty_like(g["out"], device="cpu").pin_memory())
+    d2h += g["out"].numel() * g["out"].element_size()
 
     def dev_inputs(si):
         out = []
@@ -574,7 +575,7 @@ def run_e2e(st, args, stream):
         for u, down in enumerate(downs):
             with torch.cuda.stream(down):
                 down.wait_event(computed[si])
-                for j, (h, g) in enumerate(zip(host_out, sets[si])):
+                for j, (h, g) in enumerate(zip(host_out, sets[si][-1:])):
                     if j % NC == u:
                         h.copy_(g["out"], non_blocking=True)
                 out_read[si][u].record(down)
@@ -598,7 +599,8 @@ def run_e2e(st, args, stream):
     ms = max(e0.elapsed_time(e1), wall * 1e3) / args.steps
     return {"value": st.wl["B"] / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipelined": "two device copies of the step's inputs/outputs; copies on their own streams"}
+            "pipelined": "two device copies of the step's inputs/outputs; copies on their own streams",
+            "d2h": "the step's result: the last layer's output"}
 
 
 def main():
