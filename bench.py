@@ -34,6 +34,9 @@ WORKLOADS = {
     "decode40": dict(B=64, C=131072, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
     # a small stand-in for quick checks (not a bench line)
     "small": dict(B=4, C=8192, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
+    # the headline step with the HSI variant of 8-entry blocks, 2048 candidate blocks per
+    # pool (16 384 entries); a measured variant, not the headline
+    "decode40_hsi8": dict(B=64, C=131072, H=64, hidden=4096, k=512, window=128, blk=8, nb=2048),
     # the headline batch at an 8K context: every attention launch has the headline shape
     # (64 rows x (512 + 128) rows x 64 heads) with a few GB of caches, small enough for a
     # full profiler capture (not a bench line)
@@ -472,7 +475,8 @@ def run_ours(args, wl, rank, world, local_rank):
         "metric": METRIC, "value": job_throughput(B, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"csa2_decode_40layer_b{B}_ctx{wl['C']}", "batch": B,
+        "config": {"workload": f"csa2_decode_40layer_b{B}_ctx{wl['C']}" +
+                               (f"_hsi{wl['nb']}x{wl['blk']}" if wl["blk"] != 64 else ""), "batch": B,
                    "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
                    "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
                    "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",

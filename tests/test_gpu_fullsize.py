@@ -11,6 +11,8 @@ Workloads covered (all at their stated sizes):
     Full (m = 1, 131072 entries, block maxima), Reindex over a 64-block pool, HSI, attention
     over 512 + 128 rows with 64 heads, the per-step compressor.
   * decoder-group decode, batch 32 at 65536 entries: Full with block maxima, Reindex.
+  * the HSI variant with 8-entry blocks: Reindex over 2048-block (16 384-entry) pools and HSI
+    over 64 x 16 384 blocks.
   * long-context decode, batch 4, 524288 entries (m = 2): indexer and attention.
   * encoder prefill, 16384 tokens, 8192 entries: compressor, index keys, causal indexer,
     attention.
@@ -166,6 +168,38 @@ def test_reindex_pool_full_size_sampled_rows(B, n_entries, rows):
         so = _oracle_row_scores(qi64[b, 0], w64[b, 0], c_b, s_b)
         mask = R.pool_mask(cand[b], n_entries, blk, n_entries)
         Hp.check_topk_row(topk[b, 0], so, mask, k, f"sequence {b}")
+
+
+def test_reindex_8_key_block_pools_full_size_sampled_rows():
+    # 64 sequences x 131072 entries, pools of 2048 blocks of 8 entries (16 384 entries)
+    ops = _ops()
+    B, n_entries, nb, blk, k, seed = 64, 131072, 2048, 8, 512, 9350
+    codes, scales = _device_index_cache(seed, 3, B, n_entries)
+    qi, qi64 = Hp.bf16_input(seed, 1, (B, 1, 32, 128), 1.28)
+    w, w64 = Hp.f32_input(seed, 2, (B, 1, 32), 1.28)
+    cand = _pool(seed, B, n_entries // blk, nb)
+    topk = ops.indexer_score_topk(qi, w, n_entries - 1, codes, scales, n_entries, 1, k,
+                                  cand=Hp.to_dev(cand.reshape(B, 1, nb), torch.int32), blk=blk)
+    torch.cuda.synchronize()
+    _ok()
+    topk = topk.cpu().numpy()
+    del codes, scales
+    for b in (11, 52):
+        c_b, s_b = _host_index_rows(seed, 3, b, n_entries, n_entries)
+        so = _oracle_row_scores(qi64[b, 0], w64[b, 0], c_b, s_b)
+        mask = R.pool_mask(cand[b], n_entries, blk, n_entries)
+        Hp.check_topk_row(topk[b, 0], so, mask, k, f"sequence {b}")
+
+
+def test_hsi_8_key_blocks_full_size():
+    # block maxima of 64 sequences x 16 384 blocks of 8 entries, 2048 candidates each
+    ops = _ops()
+    B, n_entries, blk, nb = 64, 131072, 8, 2048
+    bm, bm64 = Hp.f32_input(9410, 1, (B, 1, n_entries // blk))
+    cand = ops.hsi_candidates(bm, n_entries - 1, n_entries, 1, blk, nb).cpu().numpy()
+    _ok()
+    for b in range(0, B, 9):
+        np.testing.assert_array_equal(cand[b, 0], R.hsi_candidates(bm64[b, 0], n_entries, blk, nb))
 
 
 def test_hsi_full_size():

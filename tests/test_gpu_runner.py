@@ -148,3 +148,16 @@ def test_runner_config1_single_full_layer():
     g, o = make_stack(kv_src, idx_src, ratio, B, T, 0, 0, hidden, H, seed0=0)
     runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, T, 0, H, hidden, k, 64, 64)
     compare(kv_src, idx_src, ratio, g, o, B, T, 0, k, 64, 64, topks, cands)
+
+
+def test_runner_decode_hsi_8_key_blocks():
+    """The HSI variant with 8-entry blocks and 2048 candidate blocks (16 384-entry pools):
+    decoder Full m = 1 builds the pool, a Reindex layer rescores inside it, a Reuse layer
+    reads its selection; 20 000 entries so the pool is a real subset."""
+    kv_src, idx_src, ratio = [0, 0, 0], [0, 1, 1], [1, 0, 0]
+    B, Tq, hidden, H, k, blk, nb = 1, 1, 128, 8, 512, 8, 2048
+    C = 20000
+    q_pos0 = C - 1
+    g, o = make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, q_pos0, hidden, H, seed0=900)
+    runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, Tq, q_pos0, H, hidden, k, blk, nb)
+    compare(kv_src, idx_src, ratio, g, o, B, Tq, q_pos0, k, blk, nb, topks, cands)
