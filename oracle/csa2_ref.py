@@ -138,6 +138,25 @@ def quant_query(q_idx):
     return fp4.dequantize_rows(codes, scales)
 
 
+MAIN_KV_BLOCK = 16
+
+
+def main_kv_fp4(kv):
+    """FP4 main-KV entries [..., 512] -> (codes [..., 256], scales [..., 32]).
+
+    [P3] section 六: a main-KV entry takes 288 bytes; section 七 "FP4 Main KV": E2M1 data,
+    channel groups share an E4M3 scale, dequantised before the attention.  READING: groups of
+    16 channels (256 B codes + 32 one-byte scales = 288 B), the indexer keys' rounding rules,
+    quantising the stored entry (its bf16 value; decisions in float32, the kernel's precision).
+    """
+    return fp4.quantize_rows(np.asarray(kv, dtype=np.float64).astype(np.float32), block=MAIN_KV_BLOCK)
+
+
+def main_kv_dequant(codes, scales):
+    """FP4 main-KV entries back to float64 (what the attention reads)."""
+    return fp4.dequantize_rows(codes, scales)
+
+
 # ---- stage 3: lightning indexer, top-k, HSI -----------------------------------------------
 def indexer_scores(q_hat, w, k_hat):
     """I[s] = sum_j w[j] * ReLU(q_hat[j] . k_hat[s]).

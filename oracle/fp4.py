@@ -1,8 +1,12 @@
-"""FP4 (E2M1) codes with one E4M3 scale per 32 values -- oracle side.
+"""FP4 (E2M1) codes with one E4M3 scale per block of values -- oracle side.
 
 Storage format of the indexer keys: [P1] section "indexer K 改由 main KV 投影"
 (FP4, one scale per 32 dims) and [P3] section 六 "890 B/Token 是怎样算出来的"
 (68 bytes per indexer-K entry: 128 four-bit codes = 64 B plus 4 one-byte scales).
+The main KV entries use the same element formats with 16-value blocks: [P3] section 六
+(288 bytes per main-KV entry) and section 七 "FP4 Main KV" (E2M1 data, channel groups
+sharing an E4M3 scale).  READING: 288 = 256 B of codes + 32 one-byte scales, i.e. groups
+of 16 of the 512 channels.
 
 Element formats follow the OCP 8-bit floating point spec (E4M3, "FN" variant:
 bias 7, no infinities, S.1111.111 is NaN, largest finite 448) and the OCP
@@ -75,15 +79,15 @@ def e2m1_value(code):
     return np.where(code & 8, -1.0, 1.0) * E2M1_MAG[code & 7]
 
 
-def quantize_rows(v):
-    """Quantise float32 rows v[..., D] (D a multiple of 32).
+def quantize_rows(v, block=BLOCK):
+    """Quantise float32 rows v[..., D] (D a multiple of `block`).
 
-    Returns (codes uint8 [..., D/2], scales uint8 [..., D/32]).
+    Returns (codes uint8 [..., D/2], scales uint8 [..., D/block]).
     """
     v = np.asarray(v, dtype=np.float32)
     d = v.shape[-1]
-    assert d % BLOCK == 0
-    blocks = v.reshape(v.shape[:-1] + (d // BLOCK, BLOCK))
+    assert d % block == 0
+    blocks = v.reshape(v.shape[:-1] + (d // block, block))
     amax = np.max(np.abs(blocks), axis=-1)                       # float32, exact
     s_f32 = amax / np.float32(6.0)                               # IEEE float32 divide
     sb = e4m3_rne(s_f32.astype(np.float64))
@@ -110,9 +114,11 @@ def unpack_codes(packed):
 
 
 def dequantize_rows(packed, scales):
-    """codes/scales -> float64 values (code value times block scale, exact)."""
+    """codes/scales -> float64 values (code value times block scale, exact); the block
+    size is the row length over the number of scales."""
     codes = unpack_codes(packed)
     vals = e2m1_value(codes)
     d = vals.shape[-1]
     s = e4m3_value(scales)
-    return (vals.reshape(vals.shape[:-1] + (d // BLOCK, BLOCK)) * s[..., None]).reshape(vals.shape)
+    block = d // s.shape[-1]
+    return (vals.reshape(vals.shape[:-1] + (d // block, block)) * s[..., None]).reshape(vals.shape)

@@ -116,3 +116,61 @@ def test_dequantised_error_bound(seed):
     half_step = np.where(u > 4, 1.0, np.where(u > 2, 0.5, np.where(u > 0.5, 0.25, 0.25)))
     sat = u > 6
     assert np.all((np.abs(v - vh) <= half_step * sc + 1e-12) | sat)
+
+
+# ---------------------------------------------------------------- FP4 main KV (16-channel groups)
+def test_main_kv_entry_takes_the_pages_288_bytes():
+    # [P3] section 六: one main-KV entry is about 288 bytes (512 channels)
+    from oracle import csa2_ref as R
+    codes, scales = R.main_kv_fp4(np.linspace(-3, 3, 2 * 512).reshape(2, 512))
+    assert codes.shape == (2, 256) and scales.shape == (2, 32)
+    assert codes.shape[-1] + scales.shape[-1] == 288
+
+
+def test_main_kv_groups_are_16_channels_and_independent():
+    from oracle import csa2_ref as R
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal(512).astype(np.float32)
+    c0, s0 = R.main_kv_fp4(v)
+    w = v.copy()
+    w[16:32] *= np.float32(8.0)              # only channel group 1 changes
+    c1, s1 = R.main_kv_fp4(w)
+    assert s1[1] != s0[1]
+    np.testing.assert_array_equal(np.delete(s1, 1), np.delete(s0, 1))
+    np.testing.assert_array_equal(c1[:8], c0[:8])
+    np.testing.assert_array_equal(c1[16:], c0[16:])
+    # codes are unchanged by the exact power-of-two rescaling (scale moves by 2^3)
+    np.testing.assert_array_equal(c1[8:16], c0[8:16])
+
+
+def test_main_kv_representable_groups_round_trip_exactly():
+    # a group whose values are E2M1 grid points times 2^e, with max magnitude 6 * 2^e,
+    # has scale 2^e exactly and decodes to itself
+    from oracle import csa2_ref as R
+    from oracle import fp4
+    rng = np.random.default_rng(6)
+    rows = []
+    for g in range(32):
+        e = int(rng.integers(-6, 7))
+        mag = fp4.E2M1_MAG[rng.integers(0, 8, 16)]
+        mag[int(rng.integers(0, 16))] = 6.0
+        sign = np.where(rng.integers(0, 2, 16) == 1, -1.0, 1.0)
+        rows.append(mag * sign * 2.0 ** e)
+    v = np.concatenate(rows)
+    codes, scales = R.main_kv_fp4(v)
+    np.testing.assert_array_equal(R.main_kv_dequant(codes, scales), v)
+
+
+def test_main_kv_error_within_half_the_grid_gap_times_the_scale():
+    from oracle import csa2_ref as R
+    from oracle import fp4
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal((50, 512)) * np.exp(rng.standard_normal((50, 512)))).astype(np.float32)
+    codes, scales = R.main_kv_fp4(v)
+    d = R.main_kv_dequant(codes, scales).reshape(50, 32, 16)
+    s = fp4.e4m3_value(scales)[..., None]
+    amax = np.abs(v.reshape(50, 32, 16)).max(-1, keepdims=True)
+    # E2M1 gaps are at most 2 (between 4 and 6); the scale's own rounding adds at most
+    # 1/16 relative, and values above 6 s saturate by at most amax - 6 s
+    bound = 1.0 * s + np.maximum(amax - 6 * s, 0.0) + 1e-12
+    assert np.all(np.abs(d - v.reshape(50, 32, 16)) <= bound)
