@@ -51,6 +51,8 @@ struct AttnArgs {
   float scale;
   uint16_t* out;            // [rows, H, 512]
   float* lse;               // [rows, H]
+  const uint8_t* kv_codes;  // FP4 main KV [B, n_cap, 256] (NULL: kv holds bf16 entries)
+  const uint8_t* kv_scales; // [B, n_cap, 32]
 };
 
 __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
   float* Obuf = reinterpret_cast<float*>(KV);
   __shared__ const uint16_t* row_src[AF_SLOTS][AF_CH];
+  __shared__ int row_e[AF_SLOTS][AF_CH];                 // FP4 rows: cache row index, -1 none
   __shared__ unsigned long long row_mask[AF_SLOTS];
   __shared__ __align__(8) uint64_t kv_full[AF_SLOTS], kv_empty[AF_SLOTS];
   __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready;
@@ -317,6 +320,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     // other's announcement.  Thread t < 48 of a group holds the selected entry of row t of
     // the group's next chunk, loaded one chunk ahead.
     const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
+    const bool fp4 = a.kv_codes != nullptr;
     auto topk_at = [&](int c) -> int {
       const int j = c * AF_CH + gt;
       return (gt < AF_CH && c < n_ch && j >= nw && j < n_mine) ? a.topk[size_t(row) * a.k + k0 + (j - nw)] : -1;
@@ -338,11 +342,17 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
           src = a.swa + (size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0)) * 512;
         } else if (j < n_mine) {
           if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
-          if (e >= 0 && e < a.n_entries) { okr = 1; src = a.kv + (size_t(b) * a.n_cap + e) * 512; }
+          if (e >= 0 && e < a.n_entries) {
+            okr = 1;
+            if (!fp4) src = a.kv + (size_t(b) * a.n_cap + e) * 512;
+          }
         }
         const unsigned m0 = __ballot_sync(0xffffffffu, okr);
         if (okw) {
-          if (gt < AF_CH) row_src[s][gt] = okr ? src : nullptr;
+          if (gt < AF_CH) {
+            row_src[s][gt] = okr ? src : nullptr;
+            row_e[s][gt] = (okr && fp4 && j >= nw) ? int(size_t(b) * a.n_cap + e) : -1;
+          }
           if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[gw] = m0;
         }
       }
@@ -351,15 +361,53 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       uint8_t* dst = KV + s * AF_KV_BYTES;
       // 48 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are read eight
       // at a time before their copies (an asynchronous copy orders the loads after it)
+      // FP4 main KV: the chunk's rows from r_fp4 on are entries (the window rows come first)
+      const int r_fp4 = fp4 ? max(0, min(AF_CH, nw - c * AF_CH)) : AF_CH;
 #pragma unroll 1
       for (int r0 = 0; r0 < AF_CH; r0 += 8) {
-        const uint16_t* sp[8];
+        if (r0 + 8 <= r_fp4) {
+          const uint16_t* sp[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) sp[u] = row_src[s][r0 + u];
+          for (int u = 0; u < 8; ++u) sp[u] = row_src[s][r0 + u];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u, gt * 8, AF_CH),
-                           sp[u] ? sp[u] + gt * 8 : a.swa, sp[u] ? 16u : 0u);
+          for (int u = 0; u < 8; ++u)
+            umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u, gt * 8, AF_CH),
+                             sp[u] ? sp[u] + gt * 8 : a.swa, sp[u] ? 16u : 0u);
+        } else {
+          // piece gt of each row: channels 8 gt .. 8 gt + 7 = code bytes 4 gt .. 4 gt + 3 and
+          // the scale of group gt / 2; all eight rows' loads go out before any conversion
+          uint32_t cw[8], sbv[8];
+          int ri[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) ri[u] = row_e[s][r0 + u];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const size_t rr = size_t(ri[u] >= 0 ? ri[u] : 0);
+            cw[u] = reinterpret_cast<const uint32_t*>(a.kv_codes + rr * 256)[gt];
+            sbv[u] = a.kv_scales[rr * 32 + (gt >> 1)];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int r = r0 + u;
+            uint8_t* d16 = dst + umma::kmajor_sw128_offset(r, gt * 8, AF_CH);
+            if (r < r_fp4) {   // a window row of this 8-row group
+              const uint16_t* sp = row_src[s][r];
+              umma::cp_async16(d16, sp ? sp + gt * 8 : a.swa, sp ? 16u : 0u);
+              continue;
+            }
+            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            if (ri[u] >= 0) {
+              const float sc = e4m3_value(sbv[u]);
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                    e2m1_value((cw[u] >> (8 * x)) & 15u) * sc, e2m1_value((cw[u] >> (8 * x + 4)) & 15u) * sc);
+                wv[x] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+            }
+            *reinterpret_cast<uint4*>(d16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
       }
       {   // while this chunk is in flight: the rows of the group's next chunk into L2
         const int j = (c + 2) * AF_CH + gt;
@@ -368,7 +416,12 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
           if (j < nw) {
             pf = a.swa + (size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0)) * 512;
           } else if (e_next >= 0 && e_next < a.n_entries) {
-            pf = a.kv + (size_t(b) * a.n_cap + e_next) * 512;
+            if (fp4) {
+              prefetch_l2(a.kv_codes + (size_t(b) * a.n_cap + e_next) * 256, 256);
+              prefetch_l2(a.kv_scales + (size_t(b) * a.n_cap + e_next) * 32, 32);
+            } else {
+              pf = a.kv + (size_t(b) * a.n_cap + e_next) * 512;
+            }
           }
           if (pf) prefetch_l2(pf, 1024);
         }
@@ -692,14 +745,25 @@ size_t csa2_sparse_attn_workspace_size(int B, int Tq, int H, int k, int window) 
   return 0;   // partial results are merged on chip
 }
 
-int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
-                     int n_cap, int n_entries, const int32_t* topk, int k, const void* swa_kv,
-                     int S, int swa_pos0, int window, const float* sink, float scale, void* out,
-                     float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// csa2_sparse_attn (bf16 entries in kv_cache) and csa2_sparse_attn_fp4kv (FP4 entries in
+// kv_codes / kv_scales, H = 64 only).
+int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
+                     const uint8_t* kv_codes, const uint8_t* kv_scales, int n_cap, int n_entries,
+                     const int32_t* topk, int k, const void* swa_kv, int S, int swa_pos0,
+                     int window, const float* sink, float scale, void* out, float* lse_out,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  const bool fp4 = kv_codes != nullptr || kv_scales != nullptr;
   if (!q || !swa_kv || !out) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: null tensor pointer");
   if (k < 0 || k > CSA2_MAX_TOPK) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k=%d out of [0, 2048]", k);
-  if (k > 0 && (!topk || !kv_cache))
-    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k > 0 needs topk and kv_cache");
+  if (k > 0 && (!topk || (fp4 ? (!kv_codes || !kv_scales) : !kv_cache)))
+    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k > 0 needs topk and the cache entries");
+  if (fp4 && H != 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_fp4kv: H=%d (64 heads only)", H);
+  if ((kv_codes && !aligned16(kv_codes)) || (kv_scales && !aligned16(kv_scales)))
+    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_fp4kv: pointers must be 16-byte aligned");
   if (B <= 0 || Tq <= 0 || H <= 0 || H > 128 || q_pos0 < 0)
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: bad shape B=%d Tq=%d H=%d q_pos0=%d", B, Tq, H, q_pos0);
   if (k > 0 && (n_entries < 0 || n_cap < n_entries || n_cap <= 0))
@@ -722,7 +786,7 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
   if (rows * n_hg > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
   AttnArgs aa{(const uint16_t*)q, int(rows), Tq, H, q_pos0, n_hg, (const uint16_t*)kv_cache,
               n_cap, n_entries, topk, k, (const uint16_t*)swa_kv, S, swa_pos0, window, sink,
-              scale, (uint16_t*)out, lse_out};
+              scale, (uint16_t*)out, lse_out, kv_codes, kv_scales};
   cudaStream_t st = (cudaStream_t)stream;
   if (H == 64) {
     // tensor-core path: a cluster of n_split CTAs per row (enough CTAs to cover the SMs),
@@ -760,6 +824,31 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "sparse_attn launch");
   return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
+                     int n_cap, int n_entries, const int32_t* topk, int k, const void* swa_kv,
+                     int S, int swa_pos0, int window, const float* sink, float scale, void* out,
+                     float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
+  return sparse_attn_impl(q, B, Tq, H, q_pos0, kv_cache, nullptr, nullptr, n_cap, n_entries, topk,
+                          k, swa_kv, S, swa_pos0, window, sink, scale, out, lse_out, workspace,
+                          ws_bytes, stream);
+}
+
+int csa2_sparse_attn_fp4kv(const void* q, int B, int Tq, int H, int q_pos0,
+                           const uint8_t* kv_codes, const uint8_t* kv_scales, int n_cap,
+                           int n_entries, const int32_t* topk, int k, const void* swa_kv, int S,
+                           int swa_pos0, int window, const float* sink, float scale, void* out,
+                           float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
+  if (!kv_codes || !kv_scales)
+    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_fp4kv: null FP4 cache pointer");
+  return sparse_attn_impl(q, B, Tq, H, q_pos0, nullptr, kv_codes, kv_scales, n_cap, n_entries,
+                          topk, k, swa_kv, S, swa_pos0, window, sink, scale, out, lse_out,
+                          workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

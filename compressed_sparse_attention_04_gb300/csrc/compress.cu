@@ -17,6 +17,8 @@
 //   proj_gemm_kernel   SIMT fallback of the same product
 //   compress_epilogue  per entry: softmax-pool over the group, RMSNorm, RoPE, stores
 //   index_k_kernel     per entry: 512 -> 128 projection, RoPE, FP4 quantisation
+//   main_kv_fp4_kernel per entry: the stored main-KV entry as FP4 (E2M1 codes, one E4M3
+//                      scale per 16 channels: 288 bytes)
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -388,6 +390,45 @@ __global__ void __launch_bounds__(512) index_k_kernel(const float* __restrict__ 
   }
 }
 
+// FP4 main-KV entries: one warp per entry, lane l owns channels 16 l .. 16 l + 15 (one
+// scale group): E4M3 scale = nearest-even(amax / 6) saturating, E2M1 codes nearest-even of
+// v / scale (float32 divides), element 2 i in the low nibble of byte i.
+__global__ void __launch_bounds__(256) main_kv_fp4_kernel(const uint16_t* __restrict__ kv, int B,
+                                                          int n_cap, int entry0, int G,
+                                                          uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long e = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= (long long)B * G) return;
+  const long long b = e / G, g = e % G;
+  const size_t row = size_t(b) * n_cap + size_t(entry0 + g);
+  const uint4* src = reinterpret_cast<const uint4*>(kv + row * 512 + 16 * lane);
+  const uint4 w0 = src[0], w1 = src[1];
+  const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float v[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    v[2 * u] = __uint_as_float(wd[u] << 16);
+    v[2 * u + 1] = __uint_as_float(wd[u] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * u]), fabsf(v[2 * u + 1])));
+  }
+  const uint32_t sb = e4m3_rne_satfinite(__fdiv_rn(amax, 6.0f));
+  uint32_t packed[2] = {0u, 0u};
+  if (sb != 0u) {
+    const float sc = e4m3_value(sb);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float q = __fdiv_rn(v[u], sc);
+      const uint32_t c = ((__float_as_uint(q) >> 31) << 3) | e2m1_rne_mag(fabsf(q));
+      packed[u >> 3] |= c << (4 * (u & 7));
+    }
+  }
+  *reinterpret_cast<uint2*>(codes + row * 256 + 8 * lane) = make_uint2(packed[0], packed[1]);
+  scales[row * 32 + lane] = uint8_t(sb);
+}
+
 }  // namespace
 }  // namespace csa2
 
@@ -479,6 +520,27 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, con
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_k_quant launch");
+  return CSA2_OK;
+}
+
+int csa2_main_kv_quant_fp4(const void* kv_cache, int B, int n_cap, int entry0, int G,
+                           uint8_t* codes, uint8_t* scales, void* stream) {
+  if (!kv_cache || !codes || !scales)
+    return fail(CSA2_ERR_INVALID_ARG, "main_kv_quant_fp4: null tensor pointer");
+  if (B <= 0 || G < 0 || entry0 < 0 || n_cap <= 0 || (long long)entry0 + G > n_cap)
+    return fail(CSA2_ERR_INVALID_ARG, "main_kv_quant_fp4: bad shape B=%d G=%d entry0=%d n_cap=%d",
+                B, G, entry0, n_cap);
+  if (!aligned16(kv_cache) || !aligned16(codes) || !aligned16(scales))
+    return fail(CSA2_ERR_INVALID_ARG, "main_kv_quant_fp4: pointers must be 16-byte aligned");
+  if ((long long)B * G > (1ll << 34))
+    return fail(CSA2_ERR_UNSUPPORTED, "main_kv_quant_fp4: too many entries for one call");
+  if (G == 0) return CSA2_OK;
+  const long long blocks = ((long long)B * G + 7) / 8;
+  CSA2_LAUNCH("main_kv_fp4 launch", main_kv_fp4_kernel, unsigned(blocks), 256, 0, (cudaStream_t)stream,
+              (const uint16_t*)kv_cache, B, n_cap, entry0, G, codes, scales);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "main_kv_quant_fp4 launch");
   return CSA2_OK;
 }
 

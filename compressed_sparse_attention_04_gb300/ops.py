@@ -84,6 +84,18 @@ def index_k_quant(kv_pre, entry0, m, w_ik, codes, scales, k_out=None, rope_base=
             "csa2_index_k_quant")
 
 
+def main_kv_quant_fp4(kv_cache, entry0, G, codes, scales):
+    """FP4 main KV: rows entry0 .. entry0+G-1 of kv_cache [B, n_cap, 512] (bf16) into
+    codes [B, n_cap, 256] / scales [B, n_cap, 32] (u8)."""
+    lib = L.load()
+    B, n_cap = kv_cache.shape[:2]
+    _req(kv_cache, torch.bfloat16, (B, n_cap, ENTRY), "kv_cache")
+    _req(codes, torch.uint8, (B, n_cap, ENTRY // 2), "codes")
+    _req(scales, torch.uint8, (B, n_cap, ENTRY // 16), "scales")
+    L.check(lib.csa2_main_kv_quant_fp4(_p(kv_cache), B, n_cap, entry0, G, _p(codes), _p(scales),
+                                       _stream(kv_cache.device)), "csa2_main_kv_quant_fp4")
+
+
 def indexer_score_topk(q_idx, w, q_pos0, codes, scales, n_entries, m, k, cand=None, blk=64,
                        topk_out=None, blockmax_out=None, scores_out=None, workspace=None):
     """Stage 3: returns topk [B, Tq, k] (int32, ascending, -1 padded)."""
@@ -130,8 +142,9 @@ def hsi_candidates(blockmax, q_pos0, n_entries, m, blk, nb, cand_out=None):
 
 
 def sparse_attn(q, q_pos0, kv_cache, n_entries, topk, swa_kv, swa_pos0, window=128, sink=None,
-                scale=ENTRY ** -0.5, out=None, lse_out=None):
-    """Stage 4: returns out bf16 [B, Tq, H, 512]."""
+                scale=ENTRY ** -0.5, out=None, lse_out=None, kv_fp4=None):
+    """Stage 4: returns out bf16 [B, Tq, H, 512].  kv_fp4 = (codes, scales): FP4 main-KV
+    entries (csa2_sparse_attn_fp4kv) in place of the bf16 kv_cache."""
     lib = L.load()
     B, Tq, H, _ = q.shape
     _req(q, torch.bfloat16, (B, Tq, H, ENTRY), "q")
@@ -139,8 +152,13 @@ def sparse_attn(q, q_pos0, kv_cache, n_entries, topk, swa_kv, swa_pos0, window=1
     if topk is not None:
         k = topk.shape[2]
         _req(topk, torch.int32, (B, Tq, k), "topk")
-        n_cap = kv_cache.shape[1]
-        _req(kv_cache, torch.bfloat16, (B, n_cap, ENTRY), "kv_cache")
+        if kv_fp4 is not None:
+            n_cap = kv_fp4[0].shape[1]
+            _req(kv_fp4[0], torch.uint8, (B, n_cap, ENTRY // 2), "kv codes")
+            _req(kv_fp4[1], torch.uint8, (B, n_cap, ENTRY // 16), "kv scales")
+        else:
+            n_cap = kv_cache.shape[1]
+            _req(kv_cache, torch.bfloat16, (B, n_cap, ENTRY), "kv_cache")
     S = swa_kv.shape[1]
     _req(swa_kv, torch.bfloat16, (B, S, ENTRY), "swa_kv")
     if sink is not None:
@@ -152,6 +170,13 @@ def sparse_attn(q, q_pos0, kv_cache, n_entries, topk, swa_kv, swa_pos0, window=1
         _req(lse_out, torch.float32, (B, Tq, H), "lse_out")
     need = lib.csa2_sparse_attn_workspace_size(B, Tq, H, k, window)
     buf = _ws(need, q.device)
+    if kv_fp4 is not None:
+        L.check(lib.csa2_sparse_attn_fp4kv(_p(q), B, Tq, H, q_pos0, _p(kv_fp4[0]), _p(kv_fp4[1]),
+                                           n_cap, n_entries, _p(topk), k, _p(swa_kv), S, swa_pos0,
+                                           window, _p(sink), scale, _p(out), _p(lse_out),
+                                           _ws_ptr(buf), need, _stream(q.device)),
+                "csa2_sparse_attn_fp4kv")
+        return out
     L.check(lib.csa2_sparse_attn(_p(q), B, Tq, H, q_pos0, _p(kv_cache if k else None), n_cap,
                                  n_entries, _p(topk), k, _p(swa_kv), S, swa_pos0, window, _p(sink),
                                  scale, _p(out), _p(lse_out), _ws_ptr(buf), need,

@@ -112,6 +112,20 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m,
                        int n_cap, float* k_out, void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * FP4 main KV.  [P3 §六] (a main-KV entry takes 288 bytes) and [P3 §七 FP4 Main KV]
+ * (E2M1 data, channel groups sharing an E4M3 scale, dequantised before the attention).
+ * READING: groups of 16 channels, 256 B of codes + 32 scales per 512-channel entry, the
+ * index keys' rounding rules applied to each stored (bf16) entry.
+ *
+ *   kv_cache bf16 [B, n_cap, 512]: rows entry0 .. entry0+G-1 of each sequence are read
+ *   codes    u8 [B, n_cap, 256] (channel 2i in the low nibble of byte i), scales u8
+ *            [B, n_cap, 32] (E4M3 bits): the same rows written, other rows untouched
+ * Returns CSA2_ERR_INVALID_ARG for null or unaligned pointers and bad shapes.
+ * ------------------------------------------------------------------------------- */
+int csa2_main_kv_quant_fp4(const void* kv_cache, int B, int n_cap, int entry0, int G,
+                           uint8_t* codes, uint8_t* scales, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Stage 3 -- lightning-indexer scores and causal top-k.  [P1 §indexer K 改由 main KV
  * 投影] (scoring unchanged from V4: I[t,s] = sum_j w[t,j] * ReLU(q_hat[t,j] . k_hat[s]),
  * 32 heads x 128, top-512), [P2 §Indexer], [P2 §CSA2-ReIndex].
@@ -200,6 +214,17 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
                      int S, int swa_pos0, int window, const float* sink, float scale,
                      void* out, float* lse_out, void* workspace, size_t ws_bytes,
                      void* stream);
+
+/* The same attention over FP4 main-KV entries (csa2_main_kv_quant_fp4's planes):
+ *   kv_codes u8 [B, n_cap, 256], kv_scales u8 [B, n_cap, 32] in place of kv_cache; each
+ *   selected entry is dequantised (code value x group scale, exact in bf16's range) into
+ *   the same bf16 tile the attention reads; window rows stay bf16.  H must be 64
+ *   (CSA2_ERR_UNSUPPORTED otherwise).  Other arguments and errors as csa2_sparse_attn. */
+int csa2_sparse_attn_fp4kv(const void* q, int B, int Tq, int H, int q_pos0,
+                           const uint8_t* kv_codes, const uint8_t* kv_scales, int n_cap,
+                           int n_entries, const int32_t* topk, int k, const void* swa_kv, int S,
+                           int swa_pos0, int window, const float* sink, float scale, void* out,
+                           float* lse_out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Stage 5 -- Full / Reindex / Reuse layer runtime.  [P1 §一层全局注意力算四样东西],

@@ -58,6 +58,15 @@ def index_cache_input(seed, stream, B, n_cap, zero_scale_every=97):
     return codes, scales
 
 
+def main_kv_fp4_input(seed, stream, B, n_cap):
+    """Random FP4 main-KV entries: every code equally likely, one E4M3 scale per 16
+    channels in 0x28..0x37 (0.25 .. 0.94: entries of unit size, like the bf16 cache)."""
+    r = np.ascontiguousarray(u32_input(seed, stream, B * n_cap * 72).reshape(B, n_cap, 72))
+    codes = np.ascontiguousarray(r[..., :64]).view(np.uint8).reshape(B, n_cap, 256)
+    sbytes = np.ascontiguousarray(r[..., 64:]).view(np.uint8).reshape(B, n_cap, 32)
+    return codes.copy(), (0x28 + sbytes % 16).astype(np.uint8)
+
+
 # ------------------------------------------------------------------ comparisons
 def check_topk_row(gpu, scores, valid, k, what=""):
     """Compare one GPU top-k row against the oracle under the tie rule.

@@ -387,3 +387,47 @@ def test_prefill_compressor_and_index_k_full_size_sampled_entries():
         sf, cf = Hp.check_codes(codes[0, e][None, None], scl[0, e][None, None], k_o)
         flips += sf + cf
     assert flips <= 4, flips
+
+
+# ---------------------------------------------------------------- FP4 main KV
+def _device_main_kv_fp4(seed, stream, B, n_cap):
+    """Device copy of helpers.main_kv_fp4_input (same words, same bytes)."""
+    from synth import gpu as sg
+    r = torch.empty(B * n_cap * 72, dtype=torch.int32, device="cuda")
+    sg.fill_u32(r, seed, stream)
+    r8 = r.view(torch.uint8).view(B, n_cap, 288)
+    codes = r8[..., :256].contiguous()
+    scales = (0x28 + (r8[..., 256:] % 16)).to(torch.uint8).contiguous()
+    return codes, scales
+
+
+def _host_main_kv_rows(seed, stream, b, n_cap, entries):
+    out = []
+    for e in entries:
+        w = synth.uniform_u32(seed, stream, (b * n_cap + int(e)) * 72, 72)
+        by = np.ascontiguousarray(w).view(np.uint8)
+        out.append(R.main_kv_dequant(by[None, :256], (0x28 + by[None, 256:] % 16).astype(np.uint8))[0])
+    return np.stack(out) if out else np.zeros((0, 512))
+
+
+def test_sparse_attention_fp4kv_full_size_sampled_rows():
+    # 40-layer decode shape with FP4 main-KV entries: 64 rows x (512 entries + 128 window rows)
+    from synth import gpu as sg
+    ops = _ops()
+    B, n_cap, q_pos0, H, k, W, S, seed = 64, 65536, 131071, 64, 512, 128, 256, 9660
+    swa_pos0 = q_pos0 - S + 1
+    q = sg.fill_normal(torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device="cuda"), seed, 1, 0, 1.28)
+    codes, scales = _device_main_kv_fp4(seed, 2, B, n_cap)
+    swa = sg.fill_normal(torch.empty(B, S, 512, dtype=torch.bfloat16, device="cuda"), seed, 3)
+    tk = _spread_topk(B, 1, k, n_cap)
+    out = ops.sparse_attn(q, q_pos0, None, n_cap, Hp.to_dev(tk, torch.int32), swa, swa_pos0,
+                          window=W, kv_fp4=(codes, scales))
+    torch.cuda.synchronize()
+    _ok()
+    g = Hp.bf16_of(out)
+    for b in (0, 29, 63):
+        q64 = R.bf16_to_f64(synth.normal_bf16_bits(seed, 1, b * H * 512, H * 512, 1.28)).reshape(H, 512)
+        swa_b = R.bf16_to_f64(synth.normal_bf16_bits(seed, 3, b * S * 512, S * 512)).reshape(S, 512)
+        rows_ = np.concatenate([_host_main_kv_rows(seed, 2, b, n_cap, tk[b, 0]),
+                                R.attention_rows(np.zeros((0, 512)), [], swa_b, swa_pos0, q_pos0, W)])
+        Hp.check_attention(g[b, 0], R.sparse_attention(q64, rows_, R.ATTN_SCALE, None), f"sequence {b}")

@@ -454,3 +454,59 @@ def test_sparse_attn_out_of_range_index_is_reported_and_skipped():
     assert ops.last_device_status() == 0          # cleared after reading
     rows = R.attention_rows(kv64[0], [5, 50], swa64[0], 0, 127, 128)
     Hp.check_attention(Hp.bf16_of(out)[0, 0], R.sparse_attention(q64[0, 0], rows))
+
+
+# ---------------------------------------------------------------- FP4 main KV
+def test_main_kv_quant_fp4_bit_exact():
+    """The quantiser reads the stored bf16 entries; both sides decide in float32, so every
+    code and scale matches; rows outside the range stay untouched."""
+    ops = _ops()
+    B, n_cap, entry0, G = 3, 300, 7, 250
+    v = synth.normal_f32(61, 1, 0, B * n_cap * 512).reshape(B, n_cap, 512)
+    v *= np.exp2((synth.uniform_u32(61, 2, 0, B * n_cap * 32) % 24).astype(np.float32) - 12.0).reshape(
+        B, n_cap, 32).repeat(16, axis=-1)                    # groups spanning 2^-12 .. 2^11
+    bits = synth.f32_to_bf16_bits(v.astype(np.float32))
+    kv = Hp.to_dev(bits.view(np.int16), torch.int16).view(torch.bfloat16)
+    codes = torch.zeros(B, n_cap, 256, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(B, n_cap, 32, dtype=torch.uint8, device="cuda")
+    ops.main_kv_quant_fp4(kv, entry0, G, codes, scales)
+    torch.cuda.synchronize()
+    _ok()
+    oc, os_ = R.main_kv_fp4(R.bf16_to_f64(bits[:, entry0:entry0 + G]))
+    np.testing.assert_array_equal(codes[:, entry0:entry0 + G].cpu().numpy(), oc)
+    np.testing.assert_array_equal(scales[:, entry0:entry0 + G].cpu().numpy(), os_)
+    assert not codes[:, :entry0].any() and not codes[:, entry0 + G:].any()
+    assert not scales[:, :entry0].any() and not scales[:, entry0 + G:].any()
+
+
+@pytest.mark.parametrize("B,Tq,q_pos0,n_entries,k,S,swa_pos0", [
+    (2, 1, 131071, 3000, 512, 128, 131071 - 127),   # decode: 512 entries + 128 window rows
+    (1, 40, 0, 20, 128, 40, 0),                     # prefill, window clipped at 0
+    (3, 2, 500, 700, 300, 200, 370),                # odd sizes, masked slots
+])
+def test_sparse_attn_fp4kv_parity(B, Tq, q_pos0, n_entries, k, S, swa_pos0):
+    ops = _ops()
+    H, seed = 64, 130 + n_entries
+    q, q64 = Hp.bf16_input(seed, 1, (B, Tq, H, 512), 1.28)
+    codes, scales = Hp.main_kv_fp4_input(seed, 2, B, n_entries)
+    swa, swa64 = Hp.bf16_input(seed, 3, (B, S, 512))
+    topk_np = _topk_input(seed, B, Tq, k, n_entries)
+    lse = torch.empty(B, Tq, H, dtype=torch.float32, device="cuda")
+    out = ops.sparse_attn(q, q_pos0, None, n_entries, Hp.to_dev(topk_np, torch.int32), swa, swa_pos0,
+                          window=128, lse_out=lse,
+                          kv_fp4=(Hp.to_dev(codes, torch.uint8), Hp.to_dev(scales, torch.uint8)))
+    torch.cuda.synchronize()
+    _ok()
+    g = Hp.bf16_of(out)
+    lse = lse.cpu().numpy()
+    kv64 = R.main_kv_dequant(codes, scales)
+    for b in range(B):
+        for i in range(Tq):
+            t = q_pos0 + i
+            rows = R.attention_rows(kv64[b], topk_np[b, i], swa64[b], swa_pos0, t)
+            Hp.check_attention(g[b, i], R.sparse_attention(q64[b, i], rows, R.ATTN_SCALE, None),
+                               f"row {b},{i}")
+            lg = (q64[b, i] @ rows.T) * R.ATTN_SCALE
+            mx = lg.max(axis=1)
+            np.testing.assert_allclose(lse[b, i], np.log(np.exp(lg - mx[:, None]).sum(1)) + mx,
+                                       rtol=1e-4, atol=1e-4)
