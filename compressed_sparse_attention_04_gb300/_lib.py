@@ -49,6 +49,8 @@ SIGNATURES = {
     "csa2_compress_workspace_size": (sz, [i32, i32, i32, i32]),
     "csa2_compress": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, vp, f32, f32, vp, i32, vp,
                             vp, sz, vp]),
+    "csa2_compress_chunk": (i32, [vp, i32, i32, i32, i32, i32, vp, vp, vp, f32, f32, vp, vp, i32,
+                                  vp, vp, sz, vp]),
     "csa2_index_k_quant": (i32, [vp, i32, i32, i32, i32, vp, f32, vp, vp, i32, vp, vp]),
     "csa2_main_kv_quant_fp4": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
     "csa2_indexer_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),

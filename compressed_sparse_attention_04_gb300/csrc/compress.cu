@@ -205,26 +205,46 @@ int proj_splits(int M, int K, int Nout) {
   return s;
 }
 
-// One block of 512 threads per entry (b, g): thread t < 128 of split group sg = tid / 128
-// sums channels 4t..4t+3 of splits [sg * n / 4, (sg + 1) * n / 4) of the n_split partial
-// products (split-K), all its loads in flight together; group 0 then adds the four group sums
-// in group order and finishes the entry (the summation order is fixed: deterministic).
+// One block of 512 threads per entry: thread t < 128 of split group sg = tid / 128 sums
+// channels 4t..4t+3 of splits [sg * n / 4, (sg + 1) * n / 4) of the n_split partial products
+// (split-K), all its loads in flight together; group 0 then adds the four group sums in group
+// order and finishes the entry (the summation order is fixed: deterministic).
+// A chunk holds tokens pos0 .. pos0+T-1 of each sequence (rows b*T .. b*T+T-1 of P).  Per
+// sequence, block r < n_ent writes entry pos0/m + r; with head = 1 (m = 2, pos0 odd) block 0
+// completes the group whose first token the previous chunk left in `state`.  With tail = 1 (the
+// chunk ends inside a group) the last token's kv and gate sums go to state: from block 0 when
+// head = 1 (which reads the old state first: one block per sequence touches it), else from an
+// extra block r = n_ent.
 __global__ void __launch_bounds__(512) compress_epilogue_kernel(
-    const float* __restrict__ P, int n_split, size_t split_stride, int Nout, int B, int T, int m,
-    int pos0, int G,
+    const float* __restrict__ P, int n_split, size_t split_stride, int Nout, int T, int m,
+    int pos0, int n_ent, int head, int tail,
     const float* __restrict__ norm_w, float eps, const RopeTurns rt, uint16_t* __restrict__ kv_cache,
-    int n_cap, float* __restrict__ kv_pre) {
+    int n_cap, float* __restrict__ kv_pre, float* __restrict__ state) {
   pdl_wait();
   __shared__ float4 part[3][128][4];   // groups 1..3: their sums per thread
-  const int e = blockIdx.x, b = e / G, g = e % G, t = threadIdx.x & 127, sg = threadIdx.x >> 7;
-  const size_t row0 = size_t(b) * T + size_t(g) * m;
-  // channels 4t..4t+3 of up to m = 2 rows, projection (kv) and gate (z) halves
-  const int nv = m == 1 ? 1 : 4;   // float4 vectors per split: kv0 | z0 kv1 z1
+  const int per = n_ent + (tail && !head ? 1 : 0);
+  const int b = blockIdx.x / per, r = blockIdx.x % per, t = threadIdx.x & 127, sg = threadIdx.x >> 7;
+  const bool from_state = head && r == 0, to_state = r == n_ent, stash_too = from_state && tail;
+  // first token of this block's group (row of P); for from_state, the group's second token
+  const size_t row0 = to_state ? size_t(b) * T + T - 1
+                               : size_t(b) * T + (from_state ? 0 : head + size_t(r - head) * m);
+  // channels 4t..4t+3 of up to m = 2 rows, projection (kv) and gate (z) halves:
+  // vectors kv0 z0 kv1 z1 (m = 1: kv0 only)
+  int v_lo = 0, v_hi = m == 1 ? 1 : 4;
   size_t off[4];
   off[0] = row0 * Nout + 4 * t;
   off[1] = row0 * Nout + 512 + 4 * t;
   off[2] = (row0 + 1) * Nout + 4 * t;
   off[3] = (row0 + 1) * Nout + 512 + 4 * t;
+  if (to_state) {
+    v_hi = 2;
+  } else if (from_state) {   // kv1 z1 from row 0; kv0 z0 from the tail row, if any
+    v_lo = stash_too ? 0 : 2;
+    off[2] = off[0];
+    off[3] = off[1];
+    off[0] = (size_t(b) * T + T - 1) * Nout + 4 * t;
+    off[1] = off[0] + 512;
+  }
   const int sp0 = sg * n_split / 4, sp1 = (sg + 1) * n_split / 4;
   float4 acc[4];
 #pragma unroll
@@ -235,14 +255,14 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int v = 0; v < 4; ++v)
-        ld[q][v] = (base + q < sp1 && v < nv)
+        ld[q][v] = (base + q < sp1 && v >= v_lo && v < v_hi)
                        ? *reinterpret_cast<const float4*>(P + off[v] + size_t(base + q) * split_stride)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        if (base + q >= sp1 || v >= nv) continue;
+        if (base + q >= sp1 || v < v_lo || v >= v_hi) continue;
         acc[v].x += ld[q][v].x; acc[v].y += ld[q][v].y; acc[v].z += ld[q][v].z; acc[v].w += ld[q][v].w;
       }
   }
@@ -259,6 +279,21 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
       const float4 o = part[q][t][v];
       acc[v].x += o.x; acc[v].y += o.y; acc[v].z += o.z; acc[v].w += o.w;
     }
+  if (to_state) {
+    *reinterpret_cast<float4*>(state + size_t(b) * 1024 + 4 * t) = acc[0];
+    *reinterpret_cast<float4*>(state + size_t(b) * 1024 + 512 + 4 * t) = acc[1];
+    return;
+  }
+  if (from_state) {
+    float4* sp = reinterpret_cast<float4*>(state + size_t(b) * 1024 + 4 * t);
+    const float4 k0 = sp[0], z0 = sp[128];
+    if (stash_too) {
+      sp[0] = acc[0];
+      sp[128] = acc[1];
+    }
+    acc[0] = k0;
+    acc[1] = z0;
+  }
   float pooled[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -293,10 +328,10 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
   for (int u = 0; u < 4; ++u) y[u] = norm_w[4 * t + u] * (pooled[u] * inv);
   if (kv_pre) {
     float4 v = make_float4(y[0], y[1], y[2], y[3]);
-    *reinterpret_cast<float4*>(kv_pre + size_t(e) * 512 + 4 * t) = v;
+    *reinterpret_cast<float4*>(kv_pre + (size_t(b) * n_ent + r) * 512 + 4 * t) = v;
   }
   if (4 * t >= 448) {
-    const long long pos = (long long)pos0 + (long long)g * m;
+    const long long pos = (long long)(pos0 / m + r) * m;   // the group's first token
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr) {
       const int i = (4 * t - 448) / 2 + pr;
@@ -312,7 +347,7 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
   uint2 st;
   st.x = *reinterpret_cast<uint32_t*>(&lo);
   st.y = *reinterpret_cast<uint32_t*>(&hi);
-  const size_t crow = size_t(b) * n_cap + size_t(pos0 / m) + g;
+  const size_t crow = size_t(b) * n_cap + size_t(pos0 / m) + r;
   *reinterpret_cast<uint2*>(kv_cache + crow * 512 + 4 * t) = st;
 }
 
@@ -434,6 +469,65 @@ __global__ void __launch_bounds__(256) main_kv_fp4_kernel(const uint16_t* __rest
 
 using namespace csa2;
 
+namespace {
+
+// Shared body of the compressor entry points: tokens pos0 .. pos0+T-1 of B sequences, any
+// pos0 when `state` is given (m = 2), else pos0 % m == 0 and a trailing partial group ignored.
+int compress_impl(const char* who, const void* x, int B, int T, int hidden, int m, int pos0,
+                  const void* w_kv, const void* w_gate, const float* norm_w, float eps,
+                  float rope_base, float* state, void* kv_cache, int n_cap, float* kv_pre,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  if (m != 1 && m != 2) return fail(CSA2_ERR_UNSUPPORTED, "%s: m must be 1 or 2 (got %d)", who, m);
+  if (!x || !w_kv || !norm_w || !kv_cache)
+    return fail(CSA2_ERR_INVALID_ARG, "%s: null tensor pointer", who);
+  if ((m == 1) != (w_gate == nullptr))
+    return fail(CSA2_ERR_INVALID_ARG, "%s: w_gate must be NULL exactly when m == 1", who);
+  if (B <= 0 || T <= 0 || hidden <= 0 || hidden % 64 != 0)
+    return fail(CSA2_ERR_INVALID_ARG, "%s: bad shape B=%d T=%d hidden=%d", who, B, T, hidden);
+  if (pos0 < 0 || (!state && pos0 % m != 0))
+    return fail(CSA2_ERR_INVALID_ARG, "%s: pos0=%d must be >= 0 and a multiple of m", who, pos0);
+  const int head = (state && pos0 % m != 0) ? 1 : 0;
+  const int tail = (state && ((long long)pos0 + T) % m != 0) ? 1 : 0;
+  const int n_ent = state ? int(((long long)pos0 + T) / m - pos0 / m) : T / m;
+  if (n_cap <= 0 || (long long)pos0 / m + n_ent > n_cap)
+    return fail(CSA2_ERR_INVALID_ARG, "%s: entries %d..%d exceed n_cap=%d", who, pos0 / m,
+                pos0 / m + n_ent - 1, n_cap);
+  if (!(eps >= 0.f) || !(rope_base > 0.f))
+    return fail(CSA2_ERR_INVALID_ARG, "%s: bad eps / rope_base", who);
+  if (!aligned16(x) || !aligned16(w_kv) || (w_gate && !aligned16(w_gate)) || !aligned16(norm_w) ||
+      !aligned16(kv_cache) || (kv_pre && !aligned16(kv_pre)) || (state && !aligned16(state)))
+    return fail(CSA2_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", who);
+  if ((long long)B * T > (1ll << 30))
+    return fail(CSA2_ERR_UNSUPPORTED, "%s: B*T too large for one call", who);
+  const size_t need = csa2_compress_workspace_size(B, T, hidden, m);
+  if (!workspace || ws_bytes < need || !aligned256(workspace))
+    return fail(CSA2_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-aligned", who, need);
+  if (n_ent + tail == 0) return CSA2_OK;   // (n_ent == 0 implies head == 0)
+  cudaStream_t st = (cudaStream_t)stream;
+  const int M = B * T, nout = (m == 1) ? 512 : 1024;
+  float* P = static_cast<float*>(workspace);
+  int splits = 1;
+  if (hidden % 256 == 0) {
+    splits = proj_splits(M, hidden, nout);
+    cudaError_t e0 = cudaFuncSetAttribute(proj_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          int(PU_SMEM));
+    if (e0 != cudaSuccess) return cuda_fail(e0, "compress: shared memory attribute");
+    dim3 grid(nout / PU_TILE, ceil_div(M, PU_TILE), splits);
+    CSA2_LAUNCH("proj_umma launch", proj_umma_kernel, grid, PU_T, PU_SMEM, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, hidden / splits, P);
+  } else {
+    dim3 grid(nout / GN, ceil_div(M, GM));
+    CSA2_LAUNCH("proj_gemm launch", proj_gemm_kernel, grid, GT, 0, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, P);
+  }
+  note_launch();
+  CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel, B * (n_ent + (tail && !head ? 1 : 0)), 512, 0, st, P, splits, size_t(M) * nout, nout, T, m, pos0, n_ent, head, tail, norm_w, eps, rope_turns(rope_base), (uint16_t*)kv_cache, n_cap, kv_pre, state);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "compress launch");
+  return CSA2_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t csa2_compress_workspace_size(int B, int T, int hidden, int m) {
@@ -448,52 +542,18 @@ int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0, cons
                   const void* w_gate, const float* norm_w, float eps, float rope_base,
                   void* kv_cache, int n_cap, float* kv_pre, void* workspace, size_t ws_bytes,
                   void* stream) {
-  if (m != 1 && m != 2) return fail(CSA2_ERR_UNSUPPORTED, "compress: m must be 1 or 2 (got %d)", m);
-  if (!x || !w_kv || !norm_w || !kv_cache)
-    return fail(CSA2_ERR_INVALID_ARG, "compress: null tensor pointer");
-  if ((m == 1) != (w_gate == nullptr))
-    return fail(CSA2_ERR_INVALID_ARG, "compress: w_gate must be NULL exactly when m == 1");
-  if (B <= 0 || T <= 0 || hidden <= 0 || hidden % 64 != 0)
-    return fail(CSA2_ERR_INVALID_ARG, "compress: bad shape B=%d T=%d hidden=%d", B, T, hidden);
-  if (pos0 < 0 || pos0 % m != 0)
-    return fail(CSA2_ERR_INVALID_ARG, "compress: pos0=%d must be >= 0 and a multiple of m", pos0);
-  const int G = T / m;
-  if (n_cap <= 0 || (long long)pos0 / m + G > n_cap)
-    return fail(CSA2_ERR_INVALID_ARG, "compress: entries %d..%d exceed n_cap=%d", pos0 / m,
-                pos0 / m + G - 1, n_cap);
-  if (!(eps >= 0.f) || !(rope_base > 0.f))
-    return fail(CSA2_ERR_INVALID_ARG, "compress: bad eps / rope_base");
-  if (!aligned16(x) || !aligned16(w_kv) || (w_gate && !aligned16(w_gate)) || !aligned16(norm_w) ||
-      !aligned16(kv_cache) || (kv_pre && !aligned16(kv_pre)))
-    return fail(CSA2_ERR_INVALID_ARG, "compress: pointers must be 16-byte aligned");
-  if ((long long)B * T > (1ll << 30))
-    return fail(CSA2_ERR_UNSUPPORTED, "compress: B*T too large for one call");
-  const size_t need = csa2_compress_workspace_size(B, T, hidden, m);
-  if (!workspace || ws_bytes < need || !aligned256(workspace))
-    return fail(CSA2_ERR_WORKSPACE, "compress: workspace needs %zu bytes, 256-aligned", need);
-  if (G == 0) return CSA2_OK;
-  cudaStream_t st = (cudaStream_t)stream;
-  const int M = B * T, nout = (m == 1) ? 512 : 1024;
-  float* P = static_cast<float*>(workspace);
-  int splits = 1;
-  if (hidden % 256 == 0) {
-    splits = proj_splits(M, hidden, nout);
-    cudaError_t e0 = cudaFuncSetAttribute(proj_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          int(PU_SMEM));
-    if (e0 != cudaSuccess) return cuda_fail(e0, "compress: shared memory attribute");
-    dim3 grid(nout / PU_TILE, ceil_div(M, PU_TILE), splits);
-    CSA2_LAUNCH("proj_umma launch", proj_umma_kernel, grid, PU_T, PU_SMEM, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, hidden / splits, P);
-    note_launch();
-  } else {
-    dim3 grid(nout / GN, ceil_div(M, GM));
-    CSA2_LAUNCH("proj_gemm launch", proj_gemm_kernel, grid, GT, 0, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, P);
-    note_launch();
-  }
-  CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel, B * G, 512, 0, st, P, splits, size_t(M) * nout, nout, B, T, m, pos0, G, norm_w, eps, rope_turns(rope_base), (uint16_t*)kv_cache, n_cap, kv_pre);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "compress launch");
-  return CSA2_OK;
+  return compress_impl("compress", x, B, T, hidden, m, pos0, w_kv, w_gate, norm_w, eps, rope_base,
+                       nullptr, kv_cache, n_cap, kv_pre, workspace, ws_bytes, stream);
+}
+
+int csa2_compress_chunk(const void* x, int B, int T, int hidden, int m, int pos0, const void* w_kv,
+                        const void* w_gate, const float* norm_w, float eps, float rope_base,
+                        float* state, void* kv_cache, int n_cap, float* kv_pre, void* workspace,
+                        size_t ws_bytes, void* stream) {
+  if (m == 2 && !state) return fail(CSA2_ERR_INVALID_ARG, "compress_chunk: m == 2 needs a state buffer");
+  if (m == 1 && state) return fail(CSA2_ERR_INVALID_ARG, "compress_chunk: state must be NULL when m == 1");
+  return compress_impl("compress_chunk", x, B, T, hidden, m, pos0, w_kv, w_gate, norm_w, eps,
+                       rope_base, state, kv_cache, n_cap, kv_pre, workspace, ws_bytes, stream);
 }
 
 int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, const void* w_ik,

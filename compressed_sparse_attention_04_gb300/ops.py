@@ -68,6 +68,37 @@ def compress(x, w_kv, w_gate, norm_w, m, pos0, kv_cache, kv_pre=None, eps=1e-6, 
     return kv_pre
 
 
+def compress_chunk(x, w_kv, w_gate, norm_w, m, pos0, kv_cache, state=None, kv_pre=None, eps=1e-6,
+                   rope_base=10000.0, workspace=None):
+    """Stage 1 over tokens pos0 .. pos0+T-1 (x bf16 [B, T, hidden]) with the group state
+    carried across calls (m == 2: state f32 [B, 1024]).  Writes entries pos0 // m ..
+    (pos0 + T) // m - 1; returns kv_pre (f32 [B, that many, 512])."""
+    lib = L.load()
+    B, T, hid = x.shape
+    _req(x, torch.bfloat16, (B, T, hid), "x")
+    _req(w_kv, torch.bfloat16, (ENTRY, hid), "w_kv")
+    if w_gate is not None:
+        _req(w_gate, torch.bfloat16, (ENTRY, hid), "w_gate")
+    _req(norm_w, torch.float32, (ENTRY,), "norm_w")
+    n_cap = kv_cache.shape[1]
+    _req(kv_cache, torch.bfloat16, (B, n_cap, ENTRY), "kv_cache")
+    if m == 2:
+        if state is None:
+            raise ValueError("state: m == 2 needs a float32 [B, 1024] state buffer")
+        _req(state, torch.float32, (B, 2 * ENTRY), "state")
+    n = (pos0 + T) // m - pos0 // m
+    if kv_pre is None:
+        kv_pre = torch.empty(B, n, ENTRY, dtype=torch.float32, device=x.device)
+    _req(kv_pre, torch.float32, (B, n, ENTRY), "kv_pre")
+    need = lib.csa2_compress_workspace_size(B, T, hid, m)
+    buf = workspace if workspace is not None else _ws(need, x.device)
+    L.check(lib.csa2_compress_chunk(_p(x), B, T, hid, m, pos0, _p(w_kv), _p(w_gate), _p(norm_w),
+                                    eps, rope_base, _p(state), _p(kv_cache), n_cap, _p(kv_pre),
+                                    _ws_ptr(buf), need, _stream(x.device)),
+            "csa2_compress_chunk")
+    return kv_pre
+
+
 def index_k_quant(kv_pre, entry0, m, w_ik, codes, scales, k_out=None, rope_base=10000.0):
     """Stage 2 into codes [B, n_cap, 64] / scales [B, n_cap, 4]."""
     lib = L.load()

@@ -92,6 +92,26 @@ int csa2_compress(const void* x, int B, int T, int hidden, int m, int pos0,
                   float rope_base, void* kv_cache, int n_cap, float* kv_pre,
                   void* workspace, size_t ws_bytes, void* stream);
 
+/* csa2_compress with the group state carried across calls: decode one token at a time, or
+ * prefill in chunks of any length.  The pages pool each group of m tokens on its own, so a
+ * token that is not its group's last can only be held back until the group completes.
+ * Tokens pos0 .. pos0+T-1 of every sequence (any pos0 >= 0, any T >= 1) produce exactly the
+ * entries csa2_compress writes for whole groups: entries pos0/m .. (pos0+T)/m - 1 (integer
+ * division), i.e. every group whose last token is in this chunk.
+ *   m == 2: state f32 [B, 1024], caller-owned, 16-byte aligned.  When pos0 is odd, the group
+ *           (pos0-1)/2 is completed from state (its first token, left by the call that ended
+ *           at pos0-1) and this chunk's first token.  When pos0+T is odd, the chunk's last
+ *           token's kv and score rows (float32, 2 x 512 per sequence) are written to state.
+ *           Calls that share a state must follow one another in position order on one stream.
+ *   m == 1: every token completes its entry; state must be NULL.
+ *   x       bf16 [B, T, hidden];  kv_pre f32 [B, n, 512] or NULL, n = (pos0+T)/m - pos0/m.
+ * Workspace: csa2_compress_workspace_size(B, T, hidden, m).  (pos0+T)/m <= n_cap.
+ * Errors as csa2_compress; a state left by another position is not detected. */
+int csa2_compress_chunk(const void* x, int B, int T, int hidden, int m, int pos0,
+                        const void* w_kv, const void* w_gate, const float* norm_w, float eps,
+                        float rope_base, float* state, void* kv_cache, int n_cap,
+                        float* kv_pre, void* workspace, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------
  * Stage 2 -- indexer key.  [P1 §indexer K 改由 main KV 投影]: k = W_IK . kv_pre
  * (512 -> 128) from the entry BEFORE its RoPE, then RoPE on k's dims 64..127 at the

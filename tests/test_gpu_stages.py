@@ -89,6 +89,71 @@ def test_compress_parity(B, T, hidden, m, pos0, n_cap):
     assert torch.all(cache[:, untouched.cuda()] == 7.0)
 
 
+@pytest.mark.parametrize("B,T,hidden,m,pos0,n_cap,chunks", [
+    (5, 6, 512, 2, 2, 16, [1] * 6),              # decode: one token per call, split-K projection
+    (3, 4, 320, 2, 131070, 65538, [1] * 4),      # hidden not a multiple of 256: plain projection
+    (4, 3, 4096, 1, 9, 20, [1] * 3),             # m = 1: every token completes its entry
+    (2, 41, 256, 2, 4, 40, [3, 1, 2, 7, 1, 1, 9, 16, 1]),   # prefill chunks cutting groups
+    (3, 130, 4096, 2, 0, 80, [129, 1]),          # chunk ends inside a group; next completes it
+])
+def test_compress_chunk_matches_batch(B, T, hidden, m, pos0, n_cap, chunks):
+    """The compressor fed in chunks (down to one token per call), with the group state carried
+    between calls, writes the entries the oracle's compressor gives over whole groups."""
+    assert sum(chunks) == T
+    ops = _ops()
+    seed = 31 + T + m
+    x, x64 = Hp.bf16_input(seed, 1, (B, T, hidden))
+    wkv, wkv64 = Hp.bf16_input(seed, 2, (512, hidden), 0.02)
+    wg, wg64 = Hp.bf16_input(seed, 3, (512, hidden), 0.02) if m == 2 else (None, None)
+    gam, gam64 = Hp.f32_input(seed, 4, (512,), 0.1)
+    gam = gam + 1.0
+    gam64 = gam64 + 1.0
+    cache = torch.full((B, n_cap, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    state = torch.zeros(B, 1024, dtype=torch.float32, device="cuda") if m == 2 else None
+    pres = []
+    t0 = 0
+    for c in chunks:
+        p0 = pos0 + t0
+        before = cache.clone()
+        pre = ops.compress_chunk(x[:, t0:t0 + c].contiguous(), wkv, wg, gam, m, p0, cache,
+                                 state=state)
+        torch.cuda.synchronize()
+        _ok()
+        first, last = p0 // m, (p0 + c) // m          # entries this chunk completes
+        assert pre.shape[1] == last - first
+        pres.append(pre.cpu().numpy())
+        changed = set(torch.any(cache != before, dim=-1).any(dim=0).nonzero().flatten().tolist())
+        assert changed <= set(range(first, last))
+        t0 += c
+    kv_o, pre_o = R.compress(x64, wkv64, wg64, gam64.astype(np.float64), m, pos0)
+    G = T // m
+    Hp.check_compress_f32(np.concatenate(pres, axis=1)[:, :G], pre_o, "kv_pre (chunked)")
+    e0 = pos0 // m
+    got = Hp.bf16_of(cache[:, e0:e0 + G])
+    exp = R.bf16_to_f64(R.f64_to_bf16_bits(kv_o))
+    rms = np.sqrt(np.mean(exp * exp, axis=-1, keepdims=True))
+    bound = np.abs(exp) * 2.0 ** -7 + Hp.COMPRESS_REL * np.maximum(np.abs(exp), rms)
+    assert np.all(np.abs(got - exp) <= bound), "chunked entry beyond rounding + 1e-3 relative"
+    assert np.mean(got == exp) > 0.99
+    untouched = torch.ones(n_cap, dtype=torch.bool)
+    untouched[e0:e0 + G] = False
+    assert torch.all(cache[:, untouched.cuda()] == 7.0)
+
+
+def test_compress_chunk_rejects_bad_state():
+    ops = _ops()
+    x = torch.zeros(2, 1, 256, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(512, 256, dtype=torch.bfloat16, device="cuda")
+    gam = torch.ones(512, dtype=torch.float32, device="cuda")
+    cache = torch.zeros(2, 4, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):   # m = 2 needs a state buffer
+        ops.compress_chunk(x, w, w, gam, 2, 0, cache, state=None)
+    with pytest.raises(RuntimeError):   # entry 4 lies beyond the 4-entry cache
+        ops.compress_chunk(x, w, w, gam, 2, 9, cache, state=torch.zeros(2, 1024, device="cuda"))
+    with pytest.raises(RuntimeError):   # m = 1 carries no state
+        ops.compress_chunk(x, w, None, gam, 1, 0, cache, state=torch.zeros(2, 1024, device="cuda"))
+
+
 # ---------------------------------------------------------------- stage 2
 def _wide_range_kv(seed, B, G):
     """float32 entries whose 32-blocks span subnormal scales to saturation, with planted
