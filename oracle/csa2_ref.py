@@ -12,6 +12,7 @@ the value is first rounded to float32, the precision the GPU decides it in.
 import numpy as np
 
 from . import fp4
+from . import fp8
 
 # ---- constants / readings -------------------------------------------------------------
 D_ENTRY = 512        # main-KV entry width, K = V            [P1 §一层全局注意力算四样东西]
@@ -155,6 +156,19 @@ def main_kv_fp4(kv):
 def main_kv_dequant(codes, scales):
     """FP4 main-KV entries back to float64 (what the attention reads)."""
     return fp4.dequantize_rows(codes, scales)
+
+
+def swa_kv_fp8(rows):
+    """FP8 window-KV rows [..., 512] (bf16 values) -> (codes [..., 512], scales [..., 8]).
+
+    [P3] section 七: the window KV stays FP8.  READING (the format is not given): E4M3
+    elements, one power-of-two scale per 64 channels (fp8.py states the rules)."""
+    return fp8.quantize_rows(rows)
+
+
+def swa_kv_dequant(codes, scales):
+    """FP8 window-KV rows back to float64 (what the attention reads)."""
+    return fp8.dequantize_rows(codes, scales)
 
 
 # ---- stage 3: lightning indexer, top-k, HSI -----------------------------------------------
