@@ -53,6 +53,7 @@ SIGNATURES = {
                                   vp, vp, sz, vp]),
     "csa2_index_k_quant": (i32, [vp, i32, i32, i32, i32, vp, f32, vp, vp, i32, vp, vp]),
     "csa2_main_kv_quant_fp4": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
+    "csa2_swa_kv_quant_fp8": (i32, [vp, i32, i32, i32, i32, vp, vp, vp]),
     "csa2_indexer_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
     "csa2_indexer_score_topk": (i32, [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, vp, i32,
                                       i32, i32, vp, vp, vp, vp, sz, vp]),
@@ -65,6 +66,8 @@ SIGNATURES = {
                                i32, vp, f32, vp, vp, vp, sz, vp]),
     "csa2_sparse_attn_fp4kv": (i32, [vp, i32, i32, i32, i32, vp, vp, i32, i32, vp, i32, vp, i32,
                                      i32, i32, vp, f32, vp, vp, vp, sz, vp]),
+    "csa2_sparse_attn_ex": (i32, [vp, i32, i32, i32, i32, vp, vp, vp, i32, i32, vp, i32, vp, vp,
+                                  vp, i32, i32, i32, vp, f32, vp, vp, vp, sz, vp]),
     "csa2_runner_create": (i32, [i32, vp, vp, vp, i32, i32, C.POINTER(vp)]),
     "csa2_runner_destroy": (None, [vp]),
     "csa2_runner_layer_mode": (i32, [vp, i32]),

@@ -53,6 +53,8 @@ struct AttnArgs {
   float* lse;               // [rows, H]
   const uint8_t* kv_codes;  // FP4 main KV [B, n_cap, 256] (NULL: kv holds bf16 entries)
   const uint8_t* kv_scales; // [B, n_cap, 32]
+  const uint8_t* swa_codes; // FP8 window KV [B, S, 512] (NULL: swa holds bf16 rows)
+  const uint8_t* swa_scales;// [B, S, 8]
 };
 
 __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
   float* Obuf = reinterpret_cast<float*>(KV);
   __shared__ const uint16_t* row_src[AF_SLOTS][AF_CH];
-  __shared__ int row_e[AF_SLOTS][AF_CH];                 // FP4 rows: cache row index, -1 none
+  __shared__ int row_e[AF_SLOTS][AF_CH];   // quantised rows: FP8 window / FP4 cache row, -1 none
   __shared__ unsigned long long row_mask[AF_SLOTS];
   __shared__ __align__(8) uint64_t kv_full[AF_SLOTS], kv_empty[AF_SLOTS];
   __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready;
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     // other's announcement.  Thread t < 48 of a group holds the selected entry of row t of
     // the group's next chunk, loaded one chunk ahead.
     const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
-    const bool fp4 = a.kv_codes != nullptr;
+    const bool fp4 = a.kv_codes != nullptr, fp8w = a.swa_codes != nullptr;
     auto topk_at = [&](int c) -> int {
       const int j = c * AF_CH + gt;
       return (gt < AF_CH && c < n_ch && j >= nw && j < n_mine) ? a.topk[size_t(row) * a.k + k0 + (j - nw)] : -1;
@@ -334,24 +336,28 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       {   // row sources (both warps of the group, whole warps for the ballot)
         const int j = c * AF_CH + gt;
         int okr = 0;
-        const uint16_t* src = a.swa;   // any valid address for zero-filled copies
+        const uint16_t* src = a.q;   // any valid address for zero-filled copies
+        int qrow = -1;               // row of a quantised source
         if (gt >= AF_CH) {
           // (lanes past the chunk only complete the ballot)
         } else if (j < nw) {
           okr = 1;
-          src = a.swa + (size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0)) * 512;
+          const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
+          if (fp8w) qrow = int(wr);
+          else src = a.swa + wr * 512;
         } else if (j < n_mine) {
           if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
           if (e >= 0 && e < a.n_entries) {
             okr = 1;
-            if (!fp4) src = a.kv + (size_t(b) * a.n_cap + e) * 512;
+            if (fp4) qrow = int(size_t(b) * a.n_cap + e);
+            else src = a.kv + (size_t(b) * a.n_cap + e) * 512;
           }
         }
         const unsigned m0 = __ballot_sync(0xffffffffu, okr);
         if (okw) {
           if (gt < AF_CH) {
             row_src[s][gt] = okr ? src : nullptr;
-            row_e[s][gt] = (okr && fp4 && j >= nw) ? int(size_t(b) * a.n_cap + e) : -1;
+            row_e[s][gt] = qrow;
           }
           if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[gw] = m0;
         }
@@ -361,48 +367,74 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       uint8_t* dst = KV + s * AF_KV_BYTES;
       // 48 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are read eight
       // at a time before their copies (an asynchronous copy orders the loads after it)
-      // FP4 main KV: the chunk's rows from r_fp4 on are entries (the window rows come first)
-      const int r_fp4 = fp4 ? max(0, min(AF_CH, nw - c * AF_CH)) : AF_CH;
+      // the chunk's rows below r_w are window rows (they come first), the rest entries; a
+      // group of eight rows goes through 16-byte asynchronous copies when all its rows are
+      // bf16, else row by row (FP8 window rows, FP4 entries: loaded, dequantised, stored)
+      const int r_w = max(0, min(AF_CH, nw - c * AF_CH));
 #pragma unroll 1
       for (int r0 = 0; r0 < AF_CH; r0 += 8) {
-        if (r0 + 8 <= r_fp4) {
+        const bool all_bf16 = r0 + 8 <= r_w ? !fp8w : (r0 >= r_w ? !fp4 : !(fp8w || fp4));
+        if (all_bf16) {
           const uint16_t* sp[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) sp[u] = row_src[s][r0 + u];
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u, gt * 8, AF_CH),
-                             sp[u] ? sp[u] + gt * 8 : a.swa, sp[u] ? 16u : 0u);
+                             sp[u] ? sp[u] + gt * 8 : a.q, sp[u] ? 16u : 0u);
         } else {
-          // piece gt of each row: channels 8 gt .. 8 gt + 7 = code bytes 4 gt .. 4 gt + 3 and
-          // the scale of group gt / 2; all eight rows' loads go out before any conversion
-          uint32_t cw[8], sbv[8];
+          // piece gt of each row: channels 8 gt .. 8 gt + 7, i.e. FP4 code bytes 4 gt ..
+          // 4 gt + 3 with the scale of group gt / 2, or FP8 code bytes 8 gt .. 8 gt + 7 with
+          // the scale of group gt / 8; all eight rows' loads go out before any conversion
+          uint2 cw[8];
+          uint32_t sbv[8];
           int ri[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) ri[u] = row_e[s][r0 + u];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const size_t rr = size_t(ri[u] >= 0 ? ri[u] : 0);
-            cw[u] = reinterpret_cast<const uint32_t*>(a.kv_codes + rr * 256)[gt];
-            sbv[u] = a.kv_scales[rr * 32 + (gt >> 1)];
+            cw[u] = make_uint2(0u, 0u);
+            sbv[u] = 0u;
+            if (r0 + u < r_w) {
+              if (fp8w) {
+                cw[u] = reinterpret_cast<const uint2*>(a.swa_codes + rr * 512)[gt];
+                sbv[u] = a.swa_scales[rr * 8 + (gt >> 3)];
+              }
+            } else if (fp4) {
+              cw[u].x = reinterpret_cast<const uint32_t*>(a.kv_codes + rr * 256)[gt];
+              sbv[u] = a.kv_scales[rr * 32 + (gt >> 1)];
+            }
           }
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int r = r0 + u;
+            const bool win = r < r_w;
             uint8_t* d16 = dst + umma::kmajor_sw128_offset(r, gt * 8, AF_CH);
-            if (r < r_fp4) {   // a window row of this 8-row group
+            if (win ? !fp8w : !fp4) {   // a bf16 row of this 8-row group
               const uint16_t* sp = row_src[s][r];
-              umma::cp_async16(d16, sp ? sp + gt * 8 : a.swa, sp ? 16u : 0u);
+              umma::cp_async16(d16, sp ? sp + gt * 8 : a.q, sp ? 16u : 0u);
               continue;
             }
             uint32_t wv[4] = {0u, 0u, 0u, 0u};
             if (ri[u] >= 0) {
-              const float sc = e4m3_value(sbv[u]);
+              if (win) {   // E4M3 x 2^(byte - 127), exact in bf16
+                const float sc = __uint_as_float(sbv[u] << 23);
 #pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                    e2m1_value((cw[u] >> (8 * x)) & 15u) * sc, e2m1_value((cw[u] >> (8 * x + 4)) & 15u) * sc);
-                wv[x] = *reinterpret_cast<const uint32_t*>(&h2);
+                for (int x = 0; x < 4; ++x) {
+                  const uint32_t w = x < 2 ? cw[u].x : cw[u].y, sh = 16 * (x & 1);
+                  const __nv_bfloat162 h2 = __floats2bfloat162_rn(e4m3_value((w >> sh) & 0xFFu) * sc,
+                                                                  e4m3_value((w >> (sh + 8)) & 0xFFu) * sc);
+                  wv[x] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+              } else {     // E2M1 x E4M3 scale, exact in bf16
+                const float sc = e4m3_value(sbv[u]);
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                  const __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                      e2m1_value((cw[u].x >> (8 * x)) & 15u) * sc, e2m1_value((cw[u].x >> (8 * x + 4)) & 15u) * sc);
+                  wv[x] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
               }
             }
             *reinterpret_cast<uint4*>(d16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -414,7 +446,12 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
         if (gt < AF_CH && c + 2 < n_ch && j < n_mine) {
           const uint16_t* pf = nullptr;
           if (j < nw) {
-            pf = a.swa + (size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0)) * 512;
+            const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
+            if (fp8w) {   // (the 8 scale bytes: too short for a bulk prefetch)
+              prefetch_l2(a.swa_codes + wr * 512, 512);
+            } else {
+              pf = a.swa + wr * 512;
+            }
           } else if (e_next >= 0 && e_next < a.n_entries) {
             if (fp4) {
               prefetch_l2(a.kv_codes + (size_t(b) * a.n_cap + e_next) * 256, 256);
@@ -749,21 +786,32 @@ size_t csa2_sparse_attn_workspace_size(int B, int Tq, int H, int k, int window) 
 
 namespace {
 
-// csa2_sparse_attn (bf16 entries in kv_cache) and csa2_sparse_attn_fp4kv (FP4 entries in
-// kv_codes / kv_scales, H = 64 only).
+// All attention entry points: main-KV entries in bf16 (kv_cache) or FP4 (kv_codes /
+// kv_scales), window rows in bf16 (swa_kv) or FP8 (swa_codes / swa_scales); the quantised
+// formats run on the 64-head tensor-core kernel only.
 int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
                      const uint8_t* kv_codes, const uint8_t* kv_scales, int n_cap, int n_entries,
-                     const int32_t* topk, int k, const void* swa_kv, int S, int swa_pos0,
-                     int window, const float* sink, float scale, void* out, float* lse_out,
-                     void* workspace, size_t ws_bytes, void* stream) {
+                     const int32_t* topk, int k, const void* swa_kv, const uint8_t* swa_codes,
+                     const uint8_t* swa_scales, int S, int swa_pos0, int window,
+                     const float* sink, float scale, void* out, float* lse_out, void* workspace,
+                     size_t ws_bytes, void* stream) {
   const bool fp4 = kv_codes != nullptr || kv_scales != nullptr;
-  if (!q || !swa_kv || !out) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: null tensor pointer");
+  const bool fp8w = swa_codes != nullptr || swa_scales != nullptr;
+  if (!q || !out) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: null tensor pointer");
+  if (fp8w ? (!swa_codes || !swa_scales || swa_kv) : !swa_kv)
+    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: give the window rows either as bf16 or as FP8 codes + scales");
+  if (fp4 && (!kv_codes || !kv_scales || kv_cache))
+    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: give the entries either as bf16 or as FP4 codes + scales");
   if (k < 0 || k > CSA2_MAX_TOPK) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k=%d out of [0, 2048]", k);
   if (k > 0 && (!topk || (fp4 ? (!kv_codes || !kv_scales) : !kv_cache)))
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k > 0 needs topk and the cache entries");
-  if (fp4 && H != 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_fp4kv: H=%d (64 heads only)", H);
-  if ((kv_codes && !aligned16(kv_codes)) || (kv_scales && !aligned16(kv_scales)))
-    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_fp4kv: pointers must be 16-byte aligned");
+  if ((fp4 || fp8w) && H != 64)
+    return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: quantised entries or rows need H = 64 (got %d)", H);
+  if ((kv_codes && !aligned16(kv_codes)) || (kv_scales && !aligned16(kv_scales)) ||
+      (swa_codes && !aligned16(swa_codes)) || (swa_scales && !aligned16(swa_scales)))
+    return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: pointers must be 16-byte aligned");
+  if ((fp4 && (long long)B * n_cap > 0x7FFFFFFFll) || (fp8w && (long long)B * S > 0x7FFFFFFFll))
+    return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: quantised cache above 2^31 rows");
   if (B <= 0 || Tq <= 0 || H <= 0 || H > 128 || q_pos0 < 0)
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: bad shape B=%d Tq=%d H=%d q_pos0=%d", B, Tq, H, q_pos0);
   if (k > 0 && (n_entries < 0 || n_cap < n_entries || n_cap <= 0))
@@ -778,7 +826,7 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
                 first_lo, last_t, swa_pos0, (long long)swa_pos0 + S);
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: bad scale");
   if (!aligned16(q) || (kv_cache && !aligned16(kv_cache)) || (topk && !aligned16(topk)) ||
-      !aligned16(swa_kv) || !aligned16(out) || (sink && !aligned16(sink)) ||
+      (swa_kv && !aligned16(swa_kv)) || !aligned16(out) || (sink && !aligned16(sink)) ||
       (lse_out && !aligned16(lse_out)))
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: pointers must be 16-byte aligned");
   const long long rows = (long long)B * Tq;
@@ -786,7 +834,7 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
   if (rows * n_hg > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
   AttnArgs aa{(const uint16_t*)q, int(rows), Tq, H, q_pos0, n_hg, (const uint16_t*)kv_cache,
               n_cap, n_entries, topk, k, (const uint16_t*)swa_kv, S, swa_pos0, window, sink,
-              scale, (uint16_t*)out, lse_out, kv_codes, kv_scales};
+              scale, (uint16_t*)out, lse_out, kv_codes, kv_scales, swa_codes, swa_scales};
   cudaStream_t st = (cudaStream_t)stream;
   if (H == 64) {
     // tensor-core path: a cluster of n_split CTAs per row (enough CTAs to cover the SMs),
@@ -835,8 +883,8 @@ int csa2_sparse_attn(const void* q, int B, int Tq, int H, int q_pos0, const void
                      int S, int swa_pos0, int window, const float* sink, float scale, void* out,
                      float* lse_out, void* workspace, size_t ws_bytes, void* stream) {
   return sparse_attn_impl(q, B, Tq, H, q_pos0, kv_cache, nullptr, nullptr, n_cap, n_entries, topk,
-                          k, swa_kv, S, swa_pos0, window, sink, scale, out, lse_out, workspace,
-                          ws_bytes, stream);
+                          k, swa_kv, nullptr, nullptr, S, swa_pos0, window, sink, scale, out,
+                          lse_out, workspace, ws_bytes, stream);
 }
 
 int csa2_sparse_attn_fp4kv(const void* q, int B, int Tq, int H, int q_pos0,
@@ -847,8 +895,19 @@ int csa2_sparse_attn_fp4kv(const void* q, int B, int Tq, int H, int q_pos0,
   if (!kv_codes || !kv_scales)
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_fp4kv: null FP4 cache pointer");
   return sparse_attn_impl(q, B, Tq, H, q_pos0, nullptr, kv_codes, kv_scales, n_cap, n_entries,
-                          topk, k, swa_kv, S, swa_pos0, window, sink, scale, out, lse_out,
-                          workspace, ws_bytes, stream);
+                          topk, k, swa_kv, nullptr, nullptr, S, swa_pos0, window, sink, scale, out,
+                          lse_out, workspace, ws_bytes, stream);
+}
+
+int csa2_sparse_attn_ex(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
+                        const uint8_t* kv_codes, const uint8_t* kv_scales, int n_cap,
+                        int n_entries, const int32_t* topk, int k, const void* swa_kv,
+                        const uint8_t* swa_codes, const uint8_t* swa_scales, int S, int swa_pos0,
+                        int window, const float* sink, float scale, void* out, float* lse_out,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  return sparse_attn_impl(q, B, Tq, H, q_pos0, kv_cache, kv_codes, kv_scales, n_cap, n_entries,
+                          topk, k, swa_kv, swa_codes, swa_scales, S, swa_pos0, window, sink, scale,
+                          out, lse_out, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -179,6 +179,15 @@ __device__ __forceinline__ uint32_t fp4_quant_lane(float v, uint32_t& scale_byte
   return sign | e2m1_rne_mag(fabsf(u));
 }
 
+// FP8 window-KV group scale: the smallest k >= -126 with amax <= 448 * 2^k.  With amax =
+// 1.m * 2^(E-127) and 448 = 1.75 * 2^8: k = E - 135, plus one when 1.m > 1.75 (mantissa
+// field above 0x600000); zero and subnormal amax give -126.
+__device__ __forceinline__ int fp8_scale_exp(float amax) {
+  const uint32_t bits = __float_as_uint(amax), E = bits >> 23, mant = bits & 0x7FFFFFu;
+  const int k = E == 0 ? -126 : int(E) - 135 + (mant > 0x600000u ? 1 : 0);
+  return k < -126 ? -126 : k;
+}
+
 // RoPE angles.  Pair i (of 32) of the last 64 dims turns by pos * theta_i, theta_i =
 // base^(-i/32).  t.f[i] holds theta_i / (2 pi) as a 64-bit binary fraction (computed on the
 // host in extended precision), so the wrapping 64-bit product pos * t.f[i] is the angle's

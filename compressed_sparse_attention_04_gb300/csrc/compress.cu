@@ -19,6 +19,8 @@
 //   index_k_kernel     per entry: 512 -> 128 projection, RoPE, FP4 quantisation
 //   main_kv_fp4_kernel per entry: the stored main-KV entry as FP4 (E2M1 codes, one E4M3
 //                      scale per 16 channels: 288 bytes)
+//   swa_kv_fp8_kernel  per window row: FP8 (E4M3 codes, one power-of-two scale per 64
+//                      channels: 520 bytes)
 #include "common.cuh"
 #include "umma.cuh"
 
@@ -425,6 +427,45 @@ __global__ void __launch_bounds__(512) index_k_kernel(const float* __restrict__ 
   }
 }
 
+// FP8 window-KV rows: one warp per row, lane l owns channels 16 l .. 16 l + 15; four lanes
+// form a 64-channel scale group.  Scale 2^k with k = fp8_scale_exp(group amax) (stored as
+// k + 127), codes sign << 7 | E4M3 nearest-even of |v| * 2^-k (an exact product).
+__global__ void __launch_bounds__(256) swa_kv_fp8_kernel(const uint16_t* __restrict__ swa, int B,
+                                                         int S, int row0, int n_rows,
+                                                         uint8_t* __restrict__ codes,
+                                                         uint8_t* __restrict__ scales) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long e = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= (long long)B * n_rows) return;   // whole warps leave together
+  const long long b = e / n_rows, r = e % n_rows;
+  const size_t row = size_t(b) * S + size_t(row0 + r);
+  const uint4* src = reinterpret_cast<const uint4*>(swa + row * 512 + 16 * lane);
+  const uint4 w0 = src[0], w1 = src[1];
+  const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  float v[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    v[2 * u] = __uint_as_float(wd[u] << 16);
+    v[2 * u + 1] = __uint_as_float(wd[u] & 0xFFFF0000u);
+    amax = fmaxf(amax, fmaxf(fabsf(v[2 * u]), fabsf(v[2 * u + 1])));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int k = fp8_scale_exp(amax);
+  const float inv = __uint_as_float(uint32_t(127 - k) << 23);   // 2^-k, k in [-126, 120]
+  uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float q = v[u] * inv;
+    const uint32_t c = ((__float_as_uint(q) >> 31) << 7) | e4m3_rne_satfinite(fabsf(q));
+    out[u >> 2] |= c << (8 * (u & 3));
+  }
+  *reinterpret_cast<uint4*>(codes + row * 512 + 16 * lane) = make_uint4(out[0], out[1], out[2], out[3]);
+  if ((lane & 3) == 0) scales[row * 8 + (lane >> 2)] = uint8_t(k + 127);
+}
+
 // FP4 main-KV entries: one warp per entry, lane l owns channels 16 l .. 16 l + 15 (one
 // scale group): E4M3 scale = nearest-even(amax / 6) saturating, E2M1 codes nearest-even of
 // v / scale (float32 divides), element 2 i in the low nibble of byte i.
@@ -580,6 +621,27 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m, con
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "index_k_quant launch");
+  return CSA2_OK;
+}
+
+int csa2_swa_kv_quant_fp8(const void* swa_kv, int B, int S, int row0, int n_rows,
+                          uint8_t* codes, uint8_t* scales, void* stream) {
+  if (!swa_kv || !codes || !scales)
+    return fail(CSA2_ERR_INVALID_ARG, "swa_kv_quant_fp8: null tensor pointer");
+  if (B <= 0 || n_rows < 0 || row0 < 0 || S <= 0 || (long long)row0 + n_rows > S)
+    return fail(CSA2_ERR_INVALID_ARG, "swa_kv_quant_fp8: bad shape B=%d rows %d..+%d S=%d",
+                B, row0, n_rows, S);
+  if (!aligned16(swa_kv) || !aligned16(codes) || !aligned16(scales))
+    return fail(CSA2_ERR_INVALID_ARG, "swa_kv_quant_fp8: pointers must be 16-byte aligned");
+  if ((long long)B * n_rows > (1ll << 34))
+    return fail(CSA2_ERR_UNSUPPORTED, "swa_kv_quant_fp8: too many rows for one call");
+  if (n_rows == 0) return CSA2_OK;
+  const long long blocks = ((long long)B * n_rows + 7) / 8;
+  CSA2_LAUNCH("swa_kv_fp8 launch", swa_kv_fp8_kernel, unsigned(blocks), 256, 0, (cudaStream_t)stream,
+              (const uint16_t*)swa_kv, B, S, row0, n_rows, codes, scales);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "swa_kv_quant_fp8 launch");
   return CSA2_OK;
 }
 

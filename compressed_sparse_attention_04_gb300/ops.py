@@ -127,6 +127,18 @@ def main_kv_quant_fp4(kv_cache, entry0, G, codes, scales):
                                        _stream(kv_cache.device)), "csa2_main_kv_quant_fp4")
 
 
+def swa_kv_quant_fp8(swa_kv, row0, n_rows, codes, scales):
+    """FP8 window KV: rows row0 .. row0+n_rows-1 of swa_kv [B, S, 512] (bf16) into
+    codes [B, S, 512] / scales [B, S, 8] (u8)."""
+    lib = L.load()
+    B, S = swa_kv.shape[:2]
+    _req(swa_kv, torch.bfloat16, (B, S, ENTRY), "swa_kv")
+    _req(codes, torch.uint8, (B, S, ENTRY), "codes")
+    _req(scales, torch.uint8, (B, S, ENTRY // 64), "scales")
+    L.check(lib.csa2_swa_kv_quant_fp8(_p(swa_kv), B, S, row0, n_rows, _p(codes), _p(scales),
+                                      _stream(swa_kv.device)), "csa2_swa_kv_quant_fp8")
+
+
 def indexer_score_topk(q_idx, w, q_pos0, codes, scales, n_entries, m, k, cand=None, blk=64,
                        topk_out=None, blockmax_out=None, scores_out=None, workspace=None):
     """Stage 3: returns topk [B, Tq, k] (int32, ascending, -1 padded)."""
@@ -173,9 +185,10 @@ def hsi_candidates(blockmax, q_pos0, n_entries, m, blk, nb, cand_out=None):
 
 
 def sparse_attn(q, q_pos0, kv_cache, n_entries, topk, swa_kv, swa_pos0, window=128, sink=None,
-                scale=ENTRY ** -0.5, out=None, lse_out=None, kv_fp4=None):
+                scale=ENTRY ** -0.5, out=None, lse_out=None, kv_fp4=None, swa_fp8=None):
     """Stage 4: returns out bf16 [B, Tq, H, 512].  kv_fp4 = (codes, scales): FP4 main-KV
-    entries (csa2_sparse_attn_fp4kv) in place of the bf16 kv_cache."""
+    entries in place of the bf16 kv_cache; swa_fp8 = (codes, scales): FP8 window rows in
+    place of the bf16 swa_kv (which is then None)."""
     lib = L.load()
     B, Tq, H, _ = q.shape
     _req(q, torch.bfloat16, (B, Tq, H, ENTRY), "q")
@@ -190,8 +203,15 @@ def sparse_attn(q, q_pos0, kv_cache, n_entries, topk, swa_kv, swa_pos0, window=1
         else:
             n_cap = kv_cache.shape[1]
             _req(kv_cache, torch.bfloat16, (B, n_cap, ENTRY), "kv_cache")
-    S = swa_kv.shape[1]
-    _req(swa_kv, torch.bfloat16, (B, S, ENTRY), "swa_kv")
+    if swa_fp8 is not None:
+        if swa_kv is not None:
+            raise ValueError("swa_kv: give the window rows either as bf16 or as FP8, not both")
+        S = swa_fp8[0].shape[1]
+        _req(swa_fp8[0], torch.uint8, (B, S, ENTRY), "swa codes")
+        _req(swa_fp8[1], torch.uint8, (B, S, ENTRY // 64), "swa scales")
+    else:
+        S = swa_kv.shape[1]
+        _req(swa_kv, torch.bfloat16, (B, S, ENTRY), "swa_kv")
     if sink is not None:
         _req(sink, torch.float32, (H,), "sink")
     if out is None:
@@ -201,6 +221,15 @@ def sparse_attn(q, q_pos0, kv_cache, n_entries, topk, swa_kv, swa_pos0, window=1
         _req(lse_out, torch.float32, (B, Tq, H), "lse_out")
     need = lib.csa2_sparse_attn_workspace_size(B, Tq, H, k, window)
     buf = _ws(need, q.device)
+    if swa_fp8 is not None:
+        kc, ks = kv_fp4 if kv_fp4 is not None else (None, None)
+        L.check(lib.csa2_sparse_attn_ex(_p(q), B, Tq, H, q_pos0,
+                                        _p(kv_cache if (k and kv_fp4 is None) else None), _p(kc),
+                                        _p(ks), n_cap, n_entries, _p(topk), k, _p(None),
+                                        _p(swa_fp8[0]), _p(swa_fp8[1]), S, swa_pos0, window,
+                                        _p(sink), scale, _p(out), _p(lse_out), _ws_ptr(buf), need,
+                                        _stream(q.device)), "csa2_sparse_attn_ex")
+        return out
     if kv_fp4 is not None:
         L.check(lib.csa2_sparse_attn_fp4kv(_p(q), B, Tq, H, q_pos0, _p(kv_fp4[0]), _p(kv_fp4[1]),
                                            n_cap, n_entries, _p(topk), k, _p(swa_kv), S, swa_pos0,

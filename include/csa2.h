@@ -145,6 +145,19 @@ int csa2_index_k_quant(const float* kv_pre, int B, int G, int entry0, int m,
 int csa2_main_kv_quant_fp4(const void* kv_cache, int B, int n_cap, int entry0, int G,
                            uint8_t* codes, uint8_t* scales, void* stream);
 
+/* FP8 window KV.  [P3 §七 FP4 Main KV]: the window (SWA) KV is more sensitive to
+ * quantisation and stays FP8.  READING (the pages give no format): OCP E4M3 elements with
+ * one power-of-two scale per 64 channels (8 per row; the last group is the 64 RoPE dims).
+ * For a group with largest magnitude amax: k = the smallest integer >= -126 with
+ * amax <= 448 * 2^k, stored as the byte k + 127; code = signbit(v) << 7 | E4M3
+ * nearest-even of |v| * 2^-k (an exact product, never saturating).  520 bytes per row.
+ *
+ *   swa_kv bf16 [B, S, 512]: rows row0 .. row0+n_rows-1 of each sequence are read
+ *   codes  u8 [B, S, 512], scales u8 [B, S, 8]: the same rows written, others untouched
+ * Returns CSA2_ERR_INVALID_ARG for null or unaligned pointers and bad shapes. */
+int csa2_swa_kv_quant_fp8(const void* swa_kv, int B, int S, int row0, int n_rows,
+                          uint8_t* codes, uint8_t* scales, void* stream);
+
 /* ---------------------------------------------------------------------------------
  * Stage 3 -- lightning-indexer scores and causal top-k.  [P1 §indexer K 改由 main KV
  * 投影] (scoring unchanged from V4: I[t,s] = sum_j w[t,j] * ReLU(q_hat[t,j] . k_hat[s]),
@@ -245,6 +258,21 @@ int csa2_sparse_attn_fp4kv(const void* q, int B, int Tq, int H, int q_pos0,
                            int n_entries, const int32_t* topk, int k, const void* swa_kv, int S,
                            int swa_pos0, int window, const float* sink, float scale, void* out,
                            float* lse_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* The same attention with each operand in any stored format: the entries as bf16
+ * (kv_cache, kv_codes = kv_scales = NULL) or FP4 (kv_codes u8 [B, n_cap, 256] + kv_scales
+ * u8 [B, n_cap, 32], kv_cache = NULL); the window rows as bf16 (swa_kv, swa_codes =
+ * swa_scales = NULL) or FP8 (swa_codes u8 [B, S, 512] + swa_scales u8 [B, S, 8] from
+ * csa2_swa_kv_quant_fp8, swa_kv = NULL).  Quantised rows are dequantised exactly into the
+ * bf16 tile the attention reads.  Any quantised operand needs H == 64
+ * (CSA2_ERR_UNSUPPORTED otherwise); giving both forms, or neither, of an operand is
+ * CSA2_ERR_INVALID_ARG.  Other arguments and errors as csa2_sparse_attn. */
+int csa2_sparse_attn_ex(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
+                        const uint8_t* kv_codes, const uint8_t* kv_scales, int n_cap,
+                        int n_entries, const int32_t* topk, int k, const void* swa_kv,
+                        const uint8_t* swa_codes, const uint8_t* swa_scales, int S,
+                        int swa_pos0, int window, const float* sink, float scale, void* out,
+                        float* lse_out, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------
  * Stage 5 -- Full / Reindex / Reuse layer runtime.  [P1 §一层全局注意力算四样东西],

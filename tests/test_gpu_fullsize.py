@@ -431,3 +431,29 @@ def test_sparse_attention_fp4kv_full_size_sampled_rows():
         rows_ = np.concatenate([_host_main_kv_rows(seed, 2, b, n_cap, tk[b, 0]),
                                 R.attention_rows(np.zeros((0, 512)), [], swa_b, swa_pos0, q_pos0, W)])
         Hp.check_attention(g[b, 0], R.sparse_attention(q64, rows_, R.ATTN_SCALE, None), f"sequence {b}")
+
+
+def test_sparse_attention_fp4kv_fp8_window_full_size_sampled_rows():
+    # the pages' stored formats at the 40-layer decode shape: FP4 main-KV entries and FP8
+    # window rows (generator rows quantised by the oracle on the host), 64 rows x (512 + 128)
+    from synth import gpu as sg
+    ops = _ops()
+    B, n_cap, q_pos0, H, k, W, S, seed = 64, 65536, 131071, 64, 512, 128, 256, 9661
+    swa_pos0 = q_pos0 - S + 1
+    q = sg.fill_normal(torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device="cuda"), seed, 1, 0, 1.28)
+    codes, scales = _device_main_kv_fp4(seed, 2, B, n_cap)
+    wbits = synth.normal_bf16_bits(seed, 3, 0, B * S * 512).reshape(B, S, 512)
+    wc, ws = R.swa_kv_fp8(R.bf16_to_f64(wbits))
+    tk = _spread_topk(B, 1, k, n_cap)
+    out = ops.sparse_attn(q, q_pos0, None, n_cap, Hp.to_dev(tk, torch.int32), None, swa_pos0,
+                          window=W, kv_fp4=(codes, scales),
+                          swa_fp8=(Hp.to_dev(wc, torch.uint8), Hp.to_dev(ws, torch.uint8)))
+    torch.cuda.synchronize()
+    _ok()
+    g = Hp.bf16_of(out)
+    for b in (0, 37, 63):
+        q64 = R.bf16_to_f64(synth.normal_bf16_bits(seed, 1, b * H * 512, H * 512, 1.28)).reshape(H, 512)
+        swa_b = R.swa_kv_dequant(wc[b], ws[b])
+        rows_ = np.concatenate([_host_main_kv_rows(seed, 2, b, n_cap, tk[b, 0]),
+                                R.attention_rows(np.zeros((0, 512)), [], swa_b, swa_pos0, q_pos0, W)])
+        Hp.check_attention(g[b, 0], R.sparse_attention(q64, rows_, R.ATTN_SCALE, None), f"sequence {b}")

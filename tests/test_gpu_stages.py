@@ -544,6 +544,112 @@ def test_main_kv_quant_fp4_bit_exact():
     assert not scales[:, :entry0].any() and not scales[:, entry0 + G:].any()
 
 
+def test_swa_kv_quant_fp8_bit_exact():
+    """Window rows to FP8: the scale exponent and every E4M3 code match the oracle bit for
+    bit (the element decision is on an exact product); rows outside the range untouched."""
+    ops = _ops()
+    B, S, row0, n = 3, 200, 5, 180
+    v = synth.normal_f32(62, 1, 0, B * S * 512).reshape(B, S, 512)
+    v *= np.exp2((synth.uniform_u32(62, 2, 0, B * S * 8) % 40).astype(np.float32) - 20.0).reshape(
+        B, S, 8).repeat(64, axis=-1)                      # groups spanning 2^-20 .. 2^19
+    v[0, 10, 64:128] = 0.0                                # an all-zero group
+    v[1, 11, :64] = 0.0
+    v[1, 11, 3] = 448.0 * 2.0 ** -5                       # amax exactly on a power-of-two bound
+    v[2, 12, 128:192] *= 2.0 ** -110                      # bf16 subnormal elements
+    bits = synth.f32_to_bf16_bits(v.astype(np.float32))
+    swa = Hp.to_dev(bits.view(np.int16), torch.int16).view(torch.bfloat16)
+    codes = torch.zeros(B, S, 512, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(B, S, 8, dtype=torch.uint8, device="cuda")
+    ops.swa_kv_quant_fp8(swa, row0, n, codes, scales)
+    torch.cuda.synchronize()
+    _ok()
+    oc, os_ = R.swa_kv_fp8(R.bf16_to_f64(bits[:, row0:row0 + n]))
+    np.testing.assert_array_equal(scales[:, row0:row0 + n].cpu().numpy(), os_)
+    np.testing.assert_array_equal(codes[:, row0:row0 + n].cpu().numpy(), oc)
+    assert not codes[:, :row0].any() and not codes[:, row0 + n:].any()
+    assert not scales[:, :row0].any() and not scales[:, row0 + n:].any()
+
+
+def _swa_fp8_input(seed, stream, B, S):
+    """Window rows as FP8: generator bf16 rows quantised by the oracle (host side)."""
+    bits = synth.normal_bf16_bits(seed, stream, 0, B * S * 512).reshape(B, S, 512)
+    codes, scales = R.swa_kv_fp8(R.bf16_to_f64(bits))
+    return codes, scales
+
+
+@pytest.mark.parametrize("B,Tq,q_pos0,n_entries,k,S,swa_pos0,main", [
+    (2, 1, 131071, 3000, 512, 128, 131071 - 127, "fp4"),   # decode, the pages' stored formats
+    (2, 1, 131071, 3000, 512, 128, 131071 - 127, "bf16"),  # FP8 window, bf16 entries
+    (1, 40, 0, 20, 128, 40, 0, "fp4"),                     # prefill, window clipped at 0
+    (3, 2, 500, 700, 300, 200, 370, "bf16"),               # odd sizes, masked slots
+    (2, 3, 1000, 0, 0, 140, 870, None),                    # window only (k = 0)
+])
+def test_sparse_attn_fp8_window_parity(B, Tq, q_pos0, n_entries, k, S, swa_pos0, main):
+    ops = _ops()
+    H, seed = 64, 170 + n_entries
+    q, q64 = Hp.bf16_input(seed, 1, (B, Tq, H, 512), 1.28)
+    wc, ws = _swa_fp8_input(seed, 3, B, S)
+    swa64 = R.swa_kv_dequant(wc, ws)
+    kv_fp4, kv, kv64, topk = None, None, None, None
+    topk_np = np.zeros((B, Tq, 0), np.int32)
+    if main == "fp4":
+        codes, scales = Hp.main_kv_fp4_input(seed, 2, B, n_entries)
+        kv_fp4 = (Hp.to_dev(codes, torch.uint8), Hp.to_dev(scales, torch.uint8))
+        kv64 = R.main_kv_dequant(codes, scales)
+    elif main == "bf16":
+        kv, kv64 = Hp.bf16_input(seed, 2, (B, n_entries, 512))
+    if main is not None:
+        topk_np = _topk_input(seed, B, Tq, k, n_entries)
+        topk = Hp.to_dev(topk_np, torch.int32)
+    lse = torch.empty(B, Tq, H, dtype=torch.float32, device="cuda")
+    out = ops.sparse_attn(q, q_pos0, kv, n_entries, topk, None, swa_pos0, window=128, lse_out=lse,
+                          kv_fp4=kv_fp4,
+                          swa_fp8=(Hp.to_dev(wc, torch.uint8), Hp.to_dev(ws, torch.uint8)))
+    torch.cuda.synchronize()
+    _ok()
+    g = Hp.bf16_of(out)
+    lse = lse.cpu().numpy()
+    for b in range(B):
+        for i in range(Tq):
+            t = q_pos0 + i
+            ent = kv64[b] if kv64 is not None else np.zeros((0, 512))
+            rows = R.attention_rows(ent, topk_np[b, i], swa64[b], swa_pos0, t)
+            Hp.check_attention(g[b, i], R.sparse_attention(q64[b, i], rows, R.ATTN_SCALE, None),
+                               f"row {b},{i}")
+            lg = (q64[b, i] @ rows.T) * R.ATTN_SCALE
+            mx = lg.max(axis=1)
+            np.testing.assert_allclose(lse[b, i], np.log(np.exp(lg - mx[:, None]).sum(1)) + mx,
+                                       rtol=1e-4, atol=1e-4)
+
+
+def test_sparse_attn_ex_rejects_ambiguous_operands():
+    ops = _ops()
+    from compressed_sparse_attention_04_gb300 import _lib as L
+    lib = L.load()
+    q = torch.zeros(1, 1, 64, 512, dtype=torch.bfloat16, device="cuda")
+    swa = torch.zeros(1, 8, 512, dtype=torch.bfloat16, device="cuda")
+    wc = torch.zeros(1, 8, 512, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(1, 8, 8, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    p = lambda t: ops._p(t)
+    # both forms of the window rows
+    st = lib.csa2_sparse_attn_ex(p(q), 1, 1, 64, 7, p(None), p(None), p(None), 0, 0, p(None), 0,
+                                 p(swa), p(wc), p(ws), 8, 0, 8, p(None), 0.05, p(out), p(None),
+                                 p(None), 0, ops._stream(q.device))
+    assert st == L.ERR_INVALID_ARG
+    # neither form
+    st = lib.csa2_sparse_attn_ex(p(q), 1, 1, 64, 7, p(None), p(None), p(None), 0, 0, p(None), 0,
+                                 p(None), p(None), p(None), 8, 0, 8, p(None), 0.05, p(out), p(None),
+                                 p(None), 0, ops._stream(q.device))
+    assert st == L.ERR_INVALID_ARG
+    # quantised rows need 64 heads
+    q32 = torch.zeros(1, 1, 32, 512, dtype=torch.bfloat16, device="cuda")
+    st = lib.csa2_sparse_attn_ex(p(q32), 1, 1, 32, 7, p(None), p(None), p(None), 0, 0, p(None), 0,
+                                 p(None), p(wc), p(ws), 8, 0, 8, p(None), 0.05, p(q32), p(None),
+                                 p(None), 0, ops._stream(q.device))
+    assert st == L.ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("B,Tq,q_pos0,n_entries,k,S,swa_pos0", [
     (2, 1, 131071, 3000, 512, 128, 131071 - 127),   # decode: 512 entries + 128 window rows
     (1, 40, 0, 20, 128, 40, 0),                     # prefill, window clipped at 0
