@@ -205,6 +205,10 @@ constexpr uint32_t AF_Q_BYTES = 64 * 1024;
 constexpr uint32_t AF_P_SBO = (AF_CH / 8) * 128;
 constexpr uint32_t AF_P_BYTES = 8 * AF_P_SBO;          // 6 KB per P buffer
 constexpr uint32_t AF_SMEM = AF_SLOTS * AF_KV_BYTES + AF_Q_BYTES + 2 * AF_P_BYTES + 1024;
+// Quantised rows (FP4 entries, FP8 window rows) are loaded into registers as 16-byte pieces,
+// at most AF_PC per copy thread and round (one round per chunk of FP4 entries, two for a
+// chunk of FP8 window rows), then dequantised into the tile.
+constexpr int AF_PC = 12;
 constexpr int AF_HALF = AF_CH / 2;                     // rows per lane (two lanes per head)
 // S: 2 buffers x 2 K-halves x 64 columns (the two halves are independent accumulators so
 // that consecutive MMAs do not wait on each other); O^T: 4 x 64 columns
@@ -234,6 +238,66 @@ __device__ __forceinline__ float fast_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Read-only global loads kept in program order with the other volatile statements (the
+// slot wait), so that they are in flight while the copy thread waits for a free slot.
+__device__ __forceinline__ uint4 ld_v4_early(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_u16_early(const uint8_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_u8_early(const uint8_t* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+// Named barrier over n threads.
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+// Channels 8g .. 8g + 7 of an FP8 window row as bf16: E4M3 code bytes (channel 8g + i in
+// byte i) times the group's 2^(scale byte - 127).  Pairs go through the E4M3x2 -> f16x2
+// conversion (exact), then float32, then bf16 (exact: 4 significant bits).
+__device__ __forceinline__ uint4 fp8_piece_bf16(uint2 codes, uint32_t scale_byte) {
+  const float sc = __uint_as_float(scale_byte << 23);
+  uint32_t w[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const uint16_t pair = uint16_t(((x < 2 ? codes.x : codes.y) >> (16 * (x & 1))) & 0xFFFFu);
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * sc, f.y * sc);
+    w[x] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+// Channels 8g .. 8g + 7 of an FP4 entry as bf16: E2M1 codes (channel 8g + 2i in the low
+// nibble of byte i) times the group's E4M3 scale; the f16 product is exact (at most 6
+// significant bits, 2^-10 .. 2688), and so is its bf16 value.
+__device__ __forceinline__ uint4 fp4_piece_bf16(uint32_t codes, uint32_t scale_byte) {
+  uint32_t s2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(s2) : "h"(uint16_t(scale_byte)));
+  const __half sc = __low2half(*reinterpret_cast<const __half2*>(&s2));
+  const __half2 sc2 = __halves2half2(sc, sc);
+  uint32_t w[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2) : "r"((codes >> (8 * x)) & 0xFFu));
+    const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&h2), sc2);
+    const float2 f = __half22float2(prod);
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x, f.y);
+    w[x] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 // Bring `bytes` (a multiple of 16) at p into L2 without waiting for them.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
@@ -255,21 +319,26 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool v) {
   return r != 0;
 }
 
+// Marks a quantised row among the bf16 row sources.
+#define kQuantRow (reinterpret_cast<const uint16_t*>(uintptr_t(16)))
+
+template <bool QNT>   // QNT: FP4 entries and / or FP8 window rows
 __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
+  constexpr int NS = AF_SLOTS;
   pdl_wait();
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* KV = base;                                   // AF_SLOTS x 48 rows (K-major SW128)
-  uint8_t* Qs = base + AF_SLOTS * AF_KV_BYTES;          // 64 heads (K-major SW128)
+  uint8_t* KV = base;                                   // NS x 48 rows (K-major SW128)
+  uint8_t* Qs = base + NS * AF_KV_BYTES;                // 64 heads (K-major SW128)
   uint8_t* Ps = Qs + AF_Q_BYTES;                        // 2 x P (64 heads x 64 rows, K-major)
   // after the last chunk: partial O^T tiles pushed by the cluster's CTAs to the tile's owner,
   // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
   float* Obuf = reinterpret_cast<float*>(KV);
-  __shared__ const uint16_t* row_src[AF_SLOTS][AF_CH];
-  __shared__ int row_e[AF_SLOTS][AF_CH];   // quantised rows: FP8 window / FP4 cache row, -1 none
-  __shared__ unsigned long long row_mask[AF_SLOTS];
-  __shared__ __align__(8) uint64_t kv_full[AF_SLOTS], kv_empty[AF_SLOTS];
+  __shared__ const uint16_t* row_src[NS][AF_CH];   // bf16 row sources (NULL: none)
+  __shared__ int row_e[2][AF_CH];                  // (QNT) per copy group: quantised rows, -1 none
+  __shared__ unsigned long long row_mask[NS];
+  __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
   __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready;
   __shared__ uint32_t tmem_slot;
   __shared__ float fac[64];                              // per-head factor (rescale / final)
@@ -293,7 +362,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   const float scale_log2 = a.scale * 1.4426950408889634f;
 
   if (tid == 0) {
-    for (int s = 0; s < AF_SLOTS; ++s) {
+    for (int s = 0; s < NS; ++s) {
       umma::mbar_init(&kv_full[s], 64);   // the 64 threads of the group that fills it
       umma::mbar_init(&kv_empty[s], 1);
     }
@@ -322,7 +391,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     // other's announcement.  Thread t < 48 of a group holds the selected entry of row t of
     // the group's next chunk, loaded one chunk ahead.
     const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
-    const bool fp4 = a.kv_codes != nullptr, fp8w = a.swa_codes != nullptr;
+    const bool fp4 = QNT && a.kv_codes != nullptr, fp8w = QNT && a.swa_codes != nullptr;
     auto topk_at = [&](int c) -> int {
       const int j = c * AF_CH + gt;
       return (gt < AF_CH && c < n_ch && j >= nw && j < n_mine) ? a.topk[size_t(row) * a.k + k0 + (j - nw)] : -1;
@@ -332,146 +401,150 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       const int s = c % AF_SLOTS;
       const int e = e_next;
       e_next = topk_at(c + 2);
-      bool okw = c < AF_SLOTS || umma::mbar_wait(&kv_empty[s], ((c / AF_SLOTS) - 1) & 1, &d_err_attn);
-      {   // row sources (both warps of the group, whole warps for the ballot)
-        const int j = c * AF_CH + gt;
-        int okr = 0;
-        const uint16_t* src = a.q;   // any valid address for zero-filled copies
-        int qrow = -1;               // row of a quantised source
-        if (gt >= AF_CH) {
-          // (lanes past the chunk only complete the ballot)
-        } else if (j < nw) {
+      // row gt of the chunk: a bf16 source, or the row of a quantised one (qrow), or none
+      const int j = c * AF_CH + gt;
+      int okr = 0;
+      const uint16_t* src = nullptr;
+      int qrow = -1;
+      if (gt >= AF_CH) {
+        // (lanes past the chunk only complete the ballot)
+      } else if (j < nw) {
+        okr = 1;
+        const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
+        if (fp8w) qrow = int(wr);
+        else src = a.swa + wr * 512;
+      } else if (j < n_mine) {
+        if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
+        if (e >= 0 && e < a.n_entries) {
           okr = 1;
-          const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
-          if (fp8w) qrow = int(wr);
-          else src = a.swa + wr * 512;
-        } else if (j < n_mine) {
-          if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
-          if (e >= 0 && e < a.n_entries) {
-            okr = 1;
-            if (fp4) qrow = int(size_t(b) * a.n_cap + e);
-            else src = a.kv + (size_t(b) * a.n_cap + e) * 512;
+          if (fp4) qrow = int(size_t(b) * a.n_cap + e);
+          else src = a.kv + (size_t(b) * a.n_cap + e) * 512;
+        }
+      }
+      const int r_w = max(0, min(AF_CH, nw - c * AF_CH));   // the chunk's window rows come first
+      // (QNT) the chunk's quantised rows as 16-byte pieces, 32 per FP8 window row and 16 per
+      // FP4 entry, window rows first; piece idx of the chunk goes to thread idx % 64, at most
+      // AF_PC per thread and round, held in registers from before the slot is free
+      const int pw = fp8w ? 32 : 0, pm = fp4 ? 16 : 0;
+      const int n_pc = r_w * pw + (AF_CH - r_w) * pm;
+      uint4 pc[AF_PC];
+      uint32_t psc[AF_PC];
+      auto piece_at = [&](int idx, int& r, int& p) {
+        if (idx < r_w * pw) {
+          r = idx >> 5;
+          p = idx & 31;
+        } else {
+          const int i2 = idx - r_w * pw;
+          r = r_w + (i2 >> 4);
+          p = i2 & 15;
+        }
+      };
+      auto load_round = [&](int base) {   // codes and the scales they need, all in flight
+#pragma unroll
+        for (int i = 0; i < AF_PC; ++i) {
+          const int idx = base + gt + 64 * i;
+          if (idx >= n_pc) break;
+          int r, p;
+          piece_at(idx, r, p);
+          const int qr = row_e[grp][r];
+          if (qr < 0) continue;
+          if (r < r_w) {
+            pc[i] = ld_v4_early(a.swa_codes + size_t(qr) * 512 + 16 * p);
+            psc[i] = ld_u8_early(a.swa_scales + size_t(qr) * 8 + (p >> 2));
+          } else {
+            pc[i] = ld_v4_early(a.kv_codes + size_t(qr) * 256 + 16 * p);
+            psc[i] = ld_u16_early(a.kv_scales + size_t(qr) * 32 + 2 * p);
           }
         }
+      };
+      uint8_t* dst = KV + s * AF_KV_BYTES;
+      auto store_round = [&](int base) {  // dequantised into the tile (exact in bf16)
+#pragma unroll
+        for (int i = 0; i < AF_PC; ++i) {
+          const int idx = base + gt + 64 * i;
+          if (idx >= n_pc) break;
+          int r, p;
+          piece_at(idx, r, p);
+          if (row_e[grp][r] < 0) continue;
+          if (r < r_w) {   // channels 16 p .. 16 p + 15, scale group p / 4
+            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 16 * p, AF_CH)) =
+                fp8_piece_bf16(make_uint2(pc[i].x, pc[i].y), psc[i]);
+            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 16 * p + 8, AF_CH)) =
+                fp8_piece_bf16(make_uint2(pc[i].z, pc[i].w), psc[i]);
+          } else {         // channels 32 p .. 32 p + 31, scale groups 2 p and 2 p + 1
+            const uint32_t s0 = psc[i] & 0xFFu, s1 = (psc[i] >> 8) & 0xFFu;
+            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p, AF_CH)) = fp4_piece_bf16(pc[i].x, s0);
+            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p + 8, AF_CH)) = fp4_piece_bf16(pc[i].y, s0);
+            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p + 16, AF_CH)) = fp4_piece_bf16(pc[i].z, s1);
+            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p + 24, AF_CH)) = fp4_piece_bf16(pc[i].w, s1);
+          }
+        }
+      };
+      if constexpr (QNT) {
+        named_bar(2 + grp, 64);   // the group's previous chunk no longer reads row_e[grp]
+        if (gt < AF_CH) row_e[grp][gt] = qrow;
+        named_bar(2 + grp, 64);
+        load_round(0);
+      }
+      bool okw = c < AF_SLOTS || umma::mbar_wait(&kv_empty[s], ((c / AF_SLOTS) - 1) & 1, &d_err_attn);
+      {   // row sources (both warps of the group, whole warps for the ballot)
         const unsigned m0 = __ballot_sync(0xffffffffu, okr);
         if (okw) {
-          if (gt < AF_CH) {
-            row_src[s][gt] = okr ? src : nullptr;
-            row_e[s][gt] = qrow;
-          }
+          if (gt < AF_CH) row_src[s][gt] = qrow >= 0 ? kQuantRow : src;
           if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[gw] = m0;
         }
       }
       // row sources ready; the group agrees on whether the slot wait succeeded
       if (!bar_and(2 + grp, 64, okw)) { ok = false; break; }
-      uint8_t* dst = KV + s * AF_KV_BYTES;
-      // 48 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are read eight
-      // at a time before their copies (an asynchronous copy orders the loads after it)
-      // the chunk's rows below r_w are window rows (they come first), the rest entries; a
-      // group of eight rows goes through 16-byte asynchronous copies when all its rows are
-      // bf16, else row by row (FP8 window rows, FP4 entries: loaded, dequantised, stored)
-      const int r_w = max(0, min(AF_CH, nw - c * AF_CH));
+      // bf16 rows: 48 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are
+      // read eight at a time before their copies (an asynchronous copy orders the loads after
+      // it); a row with no source is zero-filled, a quantised row is written below
 #pragma unroll 1
       for (int r0 = 0; r0 < AF_CH; r0 += 8) {
-        const bool all_bf16 = r0 + 8 <= r_w ? !fp8w : (r0 >= r_w ? !fp4 : !(fp8w || fp4));
-        if (all_bf16) {
-          const uint16_t* sp[8];
+        const uint16_t* sp[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) sp[u] = row_src[s][r0 + u];
+        for (int u2 = 0; u2 < 8; ++u2) sp[u2] = row_src[s][r0 + u2];
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u, gt * 8, AF_CH),
-                             sp[u] ? sp[u] + gt * 8 : a.q, sp[u] ? 16u : 0u);
-        } else {
-          // piece gt of each row: channels 8 gt .. 8 gt + 7, i.e. FP4 code bytes 4 gt ..
-          // 4 gt + 3 with the scale of group gt / 2, or FP8 code bytes 8 gt .. 8 gt + 7 with
-          // the scale of group gt / 8; all eight rows' loads go out before any conversion
-          uint2 cw[8];
-          uint32_t sbv[8];
-          int ri[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) ri[u] = row_e[s][r0 + u];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const size_t rr = size_t(ri[u] >= 0 ? ri[u] : 0);
-            cw[u] = make_uint2(0u, 0u);
-            sbv[u] = 0u;
-            if (r0 + u < r_w) {
-              if (fp8w) {
-                cw[u] = reinterpret_cast<const uint2*>(a.swa_codes + rr * 512)[gt];
-                sbv[u] = a.swa_scales[rr * 8 + (gt >> 3)];
-              }
-            } else if (fp4) {
-              cw[u].x = reinterpret_cast<const uint32_t*>(a.kv_codes + rr * 256)[gt];
-              sbv[u] = a.kv_scales[rr * 32 + (gt >> 1)];
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int r = r0 + u;
-            const bool win = r < r_w;
-            uint8_t* d16 = dst + umma::kmajor_sw128_offset(r, gt * 8, AF_CH);
-            if (win ? !fp8w : !fp4) {   // a bf16 row of this 8-row group
-              const uint16_t* sp = row_src[s][r];
-              umma::cp_async16(d16, sp ? sp + gt * 8 : a.q, sp ? 16u : 0u);
-              continue;
-            }
-            uint32_t wv[4] = {0u, 0u, 0u, 0u};
-            if (ri[u] >= 0) {
-              if (win) {   // E4M3 x 2^(byte - 127), exact in bf16
-                const float sc = __uint_as_float(sbv[u] << 23);
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                  const uint32_t w = x < 2 ? cw[u].x : cw[u].y, sh = 16 * (x & 1);
-                  const __nv_bfloat162 h2 = __floats2bfloat162_rn(e4m3_value((w >> sh) & 0xFFu) * sc,
-                                                                  e4m3_value((w >> (sh + 8)) & 0xFFu) * sc);
-                  wv[x] = *reinterpret_cast<const uint32_t*>(&h2);
-                }
-              } else {     // E2M1 x E4M3 scale, exact in bf16
-                const float sc = e4m3_value(sbv[u]);
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                  const __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                      e2m1_value((cw[u].x >> (8 * x)) & 15u) * sc, e2m1_value((cw[u].x >> (8 * x + 4)) & 15u) * sc);
-                  wv[x] = *reinterpret_cast<const uint32_t*>(&h2);
-                }
-              }
-            }
-            *reinterpret_cast<uint4*>(d16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-          }
+        for (int u2 = 0; u2 < 8; ++u2) {
+          if (QNT && sp[u2] == kQuantRow) continue;
+          umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u2, gt * 8, AF_CH),
+                           sp[u2] ? sp[u2] + gt * 8 : a.q, sp[u2] ? 16u : 0u);
+        }
+      }
+      if constexpr (QNT) {
+        store_round(0);
+        for (int base = 64 * AF_PC; base < n_pc; base += 64 * AF_PC) {   // (FP8 window chunks)
+          load_round(base);
+          store_round(base);
         }
       }
       {   // while this chunk is in flight: the rows of the group's next chunk into L2
-        const int j = (c + 2) * AF_CH + gt;
-        if (gt < AF_CH && c + 2 < n_ch && j < n_mine) {
-          const uint16_t* pf = nullptr;
-          if (j < nw) {
-            const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
-            if (fp8w) {   // (the 8 scale bytes: too short for a bulk prefetch)
-              prefetch_l2(a.swa_codes + wr * 512, 512);
-            } else {
-              pf = a.swa + wr * 512;
-            }
+        const int jn = (c + 2) * AF_CH + gt;
+        if (gt < AF_CH && c + 2 < n_ch && jn < n_mine) {
+          if (jn < nw) {
+            const size_t wr = size_t(b) * a.S + size_t(lo + w0 + jn - a.swa_pos0);
+            if (fp8w) prefetch_l2(a.swa_codes + wr * 512, 512);   // (8 scale bytes: too short)
+            else prefetch_l2(a.swa + wr * 512, 1024);
           } else if (e_next >= 0 && e_next < a.n_entries) {
+            const size_t er = size_t(b) * a.n_cap + e_next;
             if (fp4) {
-              prefetch_l2(a.kv_codes + (size_t(b) * a.n_cap + e_next) * 256, 256);
-              prefetch_l2(a.kv_scales + (size_t(b) * a.n_cap + e_next) * 32, 32);
+              prefetch_l2(a.kv_codes + er * 256, 256);
+              prefetch_l2(a.kv_scales + er * 32, 32);
             } else {
-              pf = a.kv + (size_t(b) * a.n_cap + e_next) * 512;
+              prefetch_l2(a.kv + er * 512, 1024);
             }
           }
-          if (pf) prefetch_l2(pf, 1024);
         }
       }
       if (c <= 1) {
         // the queries come with the first chunk of each group: heads 0..31 with chunk 0,
         // heads 32..63 with chunk 1 (all 64 with chunk 0 when there is no chunk 1)
-        const uint16_t* qrow = a.q + size_t(row) * 64 * 512;
+        const uint16_t* qrow_p = a.q + size_t(row) * 64 * 512;
         const int h0 = c == 0 ? 0 : 32, nh = (c == 0 && n_ch > 1) ? 32 : 64 - h0;
 #pragma unroll 4
         for (int rep = 0; rep < nh; ++rep) {
           const int uidx = rep * 64 + gt, h = h0 + (uidx >> 6), ch = uidx & 63;
-          umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow + h * 512 + ch * 8, 16u);
+          umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow_p + h * 512 + ch * 8, 16u);
         }
       }
       umma::cp_async_commit();
@@ -516,7 +589,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_empty[s]);
       constexpr unsigned half_bits = (1u << AF_HALF) - 1u;
-      const unsigned mask = unsigned(row_mask[c % AF_SLOTS] >> (half * AF_HALF)) & half_bits;
+      const unsigned mask = unsigned(row_mask[c % NS] >> (half * AF_HALF)) & half_bits;
       float cmx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) cmx[u] = -INFINITY;
@@ -556,7 +629,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       l += ((psx[0] + psx[1]) + (psx[2] + psx[3])) + ((psx[4] + psx[5]) + (psx[6] + psx[7]));
       // P buffer s is free once the products of chunk c - 2 have completed
       bool okp = c < 2 ||
-                 umma::mbar_wait(&kv_empty[(c - 2) % AF_SLOTS], ((c - 2) / AF_SLOTS) & 1, &d_err_attn);
+                 umma::mbar_wait(&kv_empty[(c - 2) % NS], ((c - 2) / NS) & 1, &d_err_attn);
       if (!bar_and(1, 128, okp)) { ok = false; break; }
       // P as the K-major B operand of O^T += C^T P^T (no swizzle): head h's 8-row runs are
       // 16-byte core-matrix rows; this lane writes its 24 rows as three of them
@@ -578,7 +651,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       if (bar_or(1, 128, need)) {
         // the previous chunk's products must have landed in O^T first
         const bool okr = __all_sync(0xffffffffu,
-                                    umma::mbar_wait(&kv_empty[(c - 1) % AF_SLOTS], ((c - 1) / AF_SLOTS) & 1,
+                                    umma::mbar_wait(&kv_empty[(c - 1) % NS], ((c - 1) / NS) & 1,
                                                     &d_err_attn));
         if (!bar_and(1, 128, okr)) { ok = false; break; }
         umma::fence_after();
@@ -613,8 +686,8 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 0);   // A = C^T (MN-major), B = P (K-major)
     const uint32_t kv0 = umma::smem_u32(KV), q0 = umma::smem_u32(Qs), p0 = umma::smem_u32(Ps);
     auto issue_s = [&](int c) {
-      const int s = c & 1, ks_ = c % AF_SLOTS;
-      if (!umma::mbar_wait(&kv_full[ks_], (c / AF_SLOTS) & 1, &d_err_attn)) return false;
+      const int s = c & 1, ks_ = c % NS;
+      if (!umma::mbar_wait(&kv_full[ks_], (c / NS) & 1, &d_err_attn)) return false;
       // the first S also needs the queries' second half, which comes with chunk 1
       if (c == 0 && n_ch > 1 && !umma::mbar_wait(&kv_full[1], 0, &d_err_attn)) return false;
       if (c >= 2 && !umma::mbar_wait(&s_empty[s], ((c >> 1) - 1) & 1, &d_err_attn)) return false;
@@ -641,7 +714,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     while (next_pv < n_ch) {
       if (next_s < n_ch && next_s <= next_pv + 1) {
         const int c = next_s, s = c & 1;
-        if (umma::mbar_test(&kv_full[c % AF_SLOTS], (c / AF_SLOTS) & 1) &&
+        if (umma::mbar_test(&kv_full[c % NS], (c / NS) & 1) &&
             (c != 0 || n_ch == 1 || umma::mbar_test(&kv_full[1], 0)) &&
             (c < 2 || umma::mbar_test(&s_empty[s], ((c >> 1) - 1) & 1))) {
           issue_s(c);
@@ -659,7 +732,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       ++next_pv;
       umma::fence_after();
       // the four dims tiles are independent accumulators: interleave them
-      const int ks_ = c % AF_SLOTS;
+      const int ks_ = c % NS;
       const uint64_t pa0 = umma::desc_sw128(kv0 + ks_ * AF_KV_BYTES, AF_ATOM, 1024);
       const uint64_t pb0 = desc_noswz(p0 + s * AF_P_BYTES, 128, AF_P_SBO);
 #pragma unroll
@@ -846,7 +919,9 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: device id");
     if (sms_cache[dev] == 0) {
-      e0 = cudaFuncSetAttribute(attn_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
+      e0 = cudaFuncSetAttribute(attn_flash_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(attn_flash_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
       if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
       if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
     }
@@ -861,8 +936,11 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     }
     if (rows * n_split > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
     AttnFlashArgs fa{aa, n_split};
-    e0 = launch_k(attn_flash_kernel, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1), AF_SMEM, st,
-                  unsigned(n_split), fa);
+    e0 = (fp4 || fp8w)
+             ? launch_k(attn_flash_kernel<true>, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1),
+                        AF_SMEM, st, unsigned(n_split), fa)
+             : launch_k(attn_flash_kernel<false>, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1),
+                        AF_SMEM, st, unsigned(n_split), fa);
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: launch");
     note_launch();
   } else {
