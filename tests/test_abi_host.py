@@ -117,6 +117,58 @@ def test_sparse_attn_validation(lib):
     assert call(a15=0.0) == L.ERR_INVALID_ARG
 
 
+def test_compress_chunk_validation(lib):
+    f = lib.csa2_compress_chunk
+    args = dict(x=_vp(FAKE), B=2, T=3, hidden=128, m=2, pos0=5, w_kv=_vp(FAKE), w_gate=_vp(FAKE),
+                norm_w=_vp(FAKE), eps=1e-6, base=1e4, state=_vp(FAKE), kv=_vp(FAKE), n_cap=4,
+                kv_pre=_vp(FAKE), ws=_vp(FAKE), wsb=0, st=_vp(0))
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(*a.values())
+
+    assert call(state=_vp(0)) == L.ERR_INVALID_ARG                       # m = 2 needs state
+    assert call(m=1, w_gate=_vp(0)) == L.ERR_INVALID_ARG                 # m = 1 carries none
+    assert call(state=_vp(FAKE + 8)) == L.ERR_INVALID_ARG                # misaligned state
+    assert call(pos0=7) == L.ERR_INVALID_ARG                             # completes entries 3, 4
+    assert call(pos0=-1) == L.ERR_INVALID_ARG
+    assert call() == L.ERR_WORKSPACE                                     # odd pos0 is fine
+    assert call(m=1, w_gate=_vp(0), state=_vp(0), pos0=1) == L.ERR_WORKSPACE
+
+
+def test_stored_format_quantiser_validation(lib):
+    q8 = lib.csa2_swa_kv_quant_fp8
+    assert q8(_vp(0), 2, 16, 0, 4, _vp(FAKE), _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
+    assert q8(_vp(FAKE), 2, 16, 10, 7, _vp(FAKE), _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG   # rows past S
+    assert q8(_vp(FAKE), 2, 16, 0, 4, _vp(FAKE), _vp(FAKE + 4), _vp(0)) == L.ERR_INVALID_ARG
+    assert q8(_vp(FAKE), 2, 16, 3, 0, _vp(FAKE), _vp(FAKE), _vp(0)) == L.OK   # nothing to do
+    q4 = lib.csa2_main_kv_quant_fp4
+    assert q4(_vp(FAKE), 2, 16, 10, 7, _vp(FAKE), _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
+    assert q4(_vp(FAKE), 0, 16, 0, 4, _vp(FAKE), _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
+
+
+def test_sparse_attn_ex_validation(lib):
+    f = lib.csa2_sparse_attn_ex
+    # 64 heads, FP4 entries and FP8 window rows
+    base = [_vp(FAKE), 1, 1, 64, 200, _vp(0), _vp(FAKE), _vp(FAKE), 64, 32, _vp(FAKE), 8,
+            _vp(0), _vp(FAKE), _vp(FAKE), 128, 73, 128, _vp(0), 0.05, _vp(FAKE), _vp(0), _vp(0), 0,
+            _vp(0)]
+
+    def call(**over):
+        a = list(base)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return f(*a)
+
+    assert call(a12=_vp(FAKE)) == L.ERR_INVALID_ARG                # window rows given twice
+    assert call(a13=_vp(0), a14=_vp(0)) == L.ERR_INVALID_ARG       # ... and not at all
+    assert call(a14=_vp(0)) == L.ERR_INVALID_ARG                   # codes without scales
+    assert call(a5=_vp(FAKE)) == L.ERR_INVALID_ARG                 # entries given twice
+    assert call(a3=32) == L.ERR_UNSUPPORTED                        # quantised rows need 64 heads
+    assert call(a14=_vp(FAKE + 8)) == L.ERR_INVALID_ARG            # misaligned scales
+    assert call(a16=74) == L.ERR_INVALID_ARG                       # window row 73 missing
+
+
 def _runner(lib, kv, idx, ratio, blk=64, nb=64):
     n = len(kv)
     arr = C.c_int32 * n
