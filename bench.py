@@ -37,6 +37,10 @@ WORKLOADS = {
     # the headline step with the HSI variant of 8-entry blocks, 2048 candidate blocks per
     # pool (16 384 entries); a measured variant, not the headline
     "decode40_hsi8": dict(B=64, C=131072, H=64, hidden=4096, k=512, window=128, blk=8, nb=2048),
+    # the headline step with the pages' stored formats: FP4 main KV (the Full layers quantise
+    # their new entries) and FP8 window rows; a measured variant, not the headline
+    "decode40_stored": dict(B=64, C=131072, H=64, hidden=4096, k=512, window=128, blk=64, nb=64,
+                            stored=True),
     # the headline batch at an 8K context: every attention launch has the headline shape
     # (64 rows x (512 + 128) rows x 64 heads) with a few GB of caches, small enough for a
     # full profiler capture (not a bench line)
@@ -171,6 +175,10 @@ class Stack:
             g["q"] = sg.fill_normal(torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev), s, 5, 0, 1.28)
             g["swa_kv"] = sg.fill_normal(torch.empty(B, W, 512, dtype=torch.bfloat16, device=dev), s, 8)
             g["swa_len"], g["swa_pos0"] = W, self.t - W + 1
+            if wl.get("stored"):
+                g["swa_codes"] = torch.empty(B, W, 512, dtype=torch.uint8, device=dev)
+                g["swa_scales"] = torch.empty(B, W, 8, dtype=torch.uint8, device=dev)
+                ops.swa_kv_quant_fp8(g["swa_kv"], 0, W, g["swa_codes"], g["swa_scales"])
             g["out"] = torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device=dev)
             if md in (1, 2):
                 g["q_idx"] = sg.fill_normal(torch.empty(B, 1, 32, 128, dtype=torch.bfloat16, device=dev), s, 6, 0, 1.28)
@@ -198,6 +206,10 @@ class Stack:
                     ops.compress(x, g["w_kv"], g["w_gate"], g["norm_w"], m, p0, g["kv_cache"],
                                  kv_pre=pre, workspace=gemm_ws)
                     ops.index_k_quant(pre, p0 // m, m, g["w_ik"], g["idx_codes"], g["idx_scales"])
+                if wl.get("stored"):
+                    g["kv_codes"] = torch.empty(B, n_cap, 256, dtype=torch.uint8, device=dev)
+                    g["kv_scales"] = torch.empty(B, n_cap, 32, dtype=torch.uint8, device=dev)
+                    ops.main_kv_quant_fp4(g["kv_cache"], 0, n_prefix // m, g["kv_codes"], g["kv_scales"])
                 xs = torch.empty(B, m, hid, dtype=torch.bfloat16, device=dev)
                 for b in range(B):
                     sg.fill_normal(xs[b], s, 1, (b * C + n_prefix) * hid)
@@ -221,13 +233,17 @@ class Stack:
         B, H, k, W, hid = wl["B"], wl["H"], wl["k"], wl["window"], wl["hidden"]
         md = self.modes[l]
         if stage == 5:
-            rows = (k if md != 0 else 0) + W
-            return B * rows * 1024 + 2 * B * H * 512 * 2 + (B * k * 4 if md != 0 else 0)
+            if wl.get("stored"):   # FP4 entries (288 B), FP8 window rows (520 B)
+                rows_bytes = (k * 288 if md != 0 else 0) + W * 520
+            else:
+                rows_bytes = ((k if md != 0 else 0) + W) * 1024
+            return B * rows_bytes + 2 * B * H * 512 * 2 + (B * k * 4 if md != 0 else 0)
         if md == 1:
             m = self.ratio[l]
             N = wl["C"] // m
             if stage == 0:
-                return (512 * hid * 2) * (2 if m == 2 else 1) + B * m * hid * 2 + B * 1024 + B * 2048
+                return ((512 * hid * 2) * (2 if m == 2 else 1) + B * m * hid * 2 + B * 1024 + B * 2048 +
+                        (B * (1024 + 288) if wl.get("stored") else 0))
             if stage == 1:
                 return 128 * 512 * 2 + B * 2048 + B * 68
             if stage == 2:
@@ -459,11 +475,11 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # end to end through the C ABI with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not wl.get("stored"):
         e2e = run_e2e(st, args, stream)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not wl.get("stored"):
         reps, total = time_oracle(wl)
         cpu = {"value": reps / total, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{reps} x one sequence of the decode step (all 40 layers, full-size "
@@ -476,9 +492,11 @@ def run_ours(args, wl, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"csa2_decode_40layer_b{B}_ctx{wl['C']}" +
-                               (f"_hsi{wl['nb']}x{wl['blk']}" if wl["blk"] != 64 else ""), "batch": B,
+                               (f"_hsi{wl['nb']}x{wl['blk']}" if wl["blk"] != 64 else "") +
+                               ("_fp4kv_fp8swa" if wl.get("stored") else ""), "batch": B,
                    "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
                    "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
+                   "kv_format": "fp4 main kv, fp8 window rows" if wl.get("stored") else "bf16",
                    "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",
                    "launch": "cuda_graph" if args.graph else "direct",
                    "timing": "headline pass without per-stage events; stage times from a second pass",
@@ -486,7 +504,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": STAGE_NAMES[dom], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": attention_traffic(st.modes) if STAGE_NAMES[dom] == "sparse_attn" and
-                                wl["C"] == 131072 and wl["B"] == 64 else None,
+                                wl["C"] == 131072 and wl["B"] == 64 and not wl.get("stored") else None,
                      "launches_timed": stage_launches[dom]},
         "hot_path_roofline": {"stages": [STAGE_NAMES[s] for s in hot], "achieved": hot_gbs,
                               "frac": hot_gbs / peak, "unit": "GB/s"},

@@ -189,6 +189,13 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
                            L.norm_w, p->eps, p->rope_base, L.kv_cache, L.n_cap,
                            reinterpret_cast<float*>(ws + w.kv_pre), ws + w.gemm, gemm_bytes, stream);
         if (st != CSA2_OK) return st;
+        if (L.kv_codes || L.kv_scales) {   // the new entries in the stored FP4 format too
+          if (!L.kv_codes || !L.kv_scales)
+            return fail(CSA2_ERR_INVALID_ARG, "layer %d: FP4 main KV needs codes and scales", l);
+          st = csa2_main_kv_quant_fp4(L.kv_cache, p->B, L.n_cap, L.x_pos0 / m, L.x_tokens / m,
+                                      L.kv_codes, L.kv_scales, stream);
+          if (st != CSA2_OK) return st;
+        }
         mark(r, l, 0, 1, stream);
         mark(r, l, 1, 0, stream);
         st = csa2_index_k_quant(reinterpret_cast<float*>(ws + w.kv_pre), p->B, L.x_tokens / m,
@@ -230,11 +237,17 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
     }
     // attention
     const void* kv = nullptr;
+    const uint8_t *kv_codes = nullptr, *kv_scales = nullptr;
     const int32_t* topk = nullptr;
     int k = 0, n_cap = 0, n_ent = 0;
     if (md != CSA2_MODE_SWA) {
       const int f = r->kv_src[l];
-      kv = io[f].kv_cache;
+      if (io[f].kv_codes) {
+        kv_codes = io[f].kv_codes;
+        kv_scales = io[f].kv_scales;
+      } else {
+        kv = io[f].kv_cache;
+      }
       n_cap = io[f].n_cap;
       n_ent = n_entries[f];
       topk = slot_topk;
@@ -245,9 +258,10 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
                     r->idx_src[l]);
     }
     mark(r, l, 5, 0, stream);
-    st = csa2_sparse_attn(L.q, p->B, p->Tq, p->H, p->q_pos0, kv, n_cap, n_ent, topk, k, L.swa_kv,
-                          L.swa_len, L.swa_pos0, p->window, L.sink, p->scale, L.out, nullptr,
-                          ws + w.attn, w.total - w.attn, stream);
+    st = csa2_sparse_attn_ex(L.q, p->B, p->Tq, p->H, p->q_pos0, kv, kv_codes, kv_scales, n_cap,
+                             n_ent, topk, k, L.swa_codes ? nullptr : L.swa_kv, L.swa_codes,
+                             L.swa_scales, L.swa_len, L.swa_pos0, p->window, L.sink, p->scale,
+                             L.out, nullptr, ws + w.attn, w.total - w.attn, stream);
     if (st != CSA2_OK) return st;
     mark(r, l, 5, 1, stream);
   }

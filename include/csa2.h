@@ -312,6 +312,16 @@ typedef struct {
   void* out;                   /* bf16 [B, Tq, H, 512] */
   int32_t* topk_out;           /* optional i32 [B, Tq, k]: index sources write here */
   int32_t* cand_out;           /* optional i32 [B, Tq, hsi_nb]: pool-building Full layer */
+  /* Optional stored formats ([P3 §六], [P3 §七 FP4 Main KV]).  Full: with kv_codes /
+   * kv_scales (u8 [B, n_cap, 256] / [B, n_cap, 32], FP4 as csa2_main_kv_quant_fp4) the step
+   * also writes the layer's new entries there, and every layer reading this KV attends over
+   * the FP4 entries (kv_cache still receives the bf16 entries).  Every layer: swa_codes /
+   * swa_scales (u8 [B, swa_len, 512] / [B, swa_len, 8], FP8 as csa2_swa_kv_quant_fp8) in
+   * place of swa_kv (which is then NULL).  Quantised operands need H == 64. */
+  uint8_t* kv_codes;
+  uint8_t* kv_scales;
+  const uint8_t* swa_codes;
+  const uint8_t* swa_scales;
   int x_tokens;
   int x_pos0;
   int n_cap;

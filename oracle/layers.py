@@ -90,7 +90,7 @@ def bytes_per_token(kv_src, idx_src, ratio, entry_bytes=356):
 
 
 def run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k, hsi_blk=64, hsi_nb=64,
-             window=R.WINDOW, scale=R.ATTN_SCALE, use_hsi=True):
+             window=R.WINDOW, scale=R.ATTN_SCALE, use_hsi=True, main_kv_fp4=False, swa_fp8=False):
     """One pass of all layers for Tq queries per sequence at positions q_pos0..
 
     ``layers[l]`` is a dict of float64 inputs:
@@ -99,6 +99,9 @@ def run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k, hsi_blk=64, hsi_n
                 gamma, w_ik, prev_kv [B,n0,512] (bf16-valued), prev_codes [B,n0,64],
                 prev_scales [B,n0,4] with n0 = x_pos0 // m
       Full / Reindex: q_idx [B,Tq,32,128], w_idx [B,Tq,32]
+    Stored formats ([P3] section 六 and section 七 "FP4 Main KV"): with main_kv_fp4 the
+    attention reads every main-KV entry through its FP4 form (csa2_ref.main_kv_fp4), with
+    swa_fp8 every window row through its FP8 form (csa2_ref.swa_kv_fp8).
     Returns (outs, trace): outs[l] = [B,Tq,H,512] float64; trace[l] holds the
     layer's top-k [B,Tq,k], its scores / competing masks per (b, i), and candidates for
     a Full layer that builds a pool.
@@ -169,8 +172,13 @@ def run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k, hsi_blk=64, hsi_n
                     kv_rows = np.zeros((0, R.D_ENTRY))
                 else:
                     kv_rows = caches[kv_src[l]][0][b]
+                    if main_kv_fp4:
+                        kv_rows = R.main_kv_dequant(*R.main_kv_fp4(kv_rows))
                     sel = slots["topk_idxs"][b, i]
-                rows = R.attention_rows(kv_rows, sel, L["swa"][b], L["swa_pos0"], t, window)
+                swa_rows = L["swa"][b]
+                if swa_fp8:
+                    swa_rows = R.swa_kv_dequant(*R.swa_kv_fp8(swa_rows))
+                rows = R.attention_rows(kv_rows, sel, swa_rows, L["swa_pos0"], t, window)
                 o[b, i] = R.sparse_attention(L["q"][b, i], rows, scale)
         outs.append(o)
         trace.append(tr)

@@ -22,10 +22,12 @@ def _built():
 
 
 def make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, n0_tokens, hidden, H, seed0, S_extra=0,
-               window=128):
+               window=128, stored_formats=False):
     """Per-layer inputs for both sides.  Full layers get hidden states for tokens
     0..q_pos0+Tq-1: the prefix 0..n0_tokens-1 is compressed beforehand (GPU: by the
-    stage calls; oracle: by its own compressor), the rest is the step's input."""
+    stage calls; oracle: by its own compressor), the rest is the step's input.
+    stored_formats: FP4 main KV and FP8 window rows; the prefix entries' FP4 form and the
+    window rows' FP8 form come from the oracle's quantisers on the host."""
     from compressed_sparse_attention_04_gb300 import ops
     gpu, orc = [], []
     T_all = q_pos0 + Tq
@@ -37,6 +39,10 @@ def make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, n0_tokens, hidden, H, seed
         q, q64 = Hp.bf16_input(s, 5, (B, Tq, H, 512), 1.28)
         swa, swa64 = Hp.bf16_input(s, 8, (B, S, 512))
         g = dict(q=q, swa_kv=swa, swa_len=S, swa_pos0=swa_pos0, out=torch.empty_like(q))
+        if stored_formats:
+            wc, ws_ = R.swa_kv_fp8(swa64)
+            g.update(swa_kv=None, swa_codes=Hp.to_dev(wc, torch.uint8),
+                     swa_scales=Hp.to_dev(ws_, torch.uint8))
         o = dict(q=q64, swa=swa64, swa_pos0=swa_pos0)
         if kv_src[l] == l or idx_src[l] == l:
             qi, qi64 = Hp.bf16_input(s, 6, (B, Tq, 32, 128), 1.28)
@@ -65,6 +71,12 @@ def make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, n0_tokens, hidden, H, seed
             kv_p, pre_p = R.compress(x64[:, : n0 * m], wkv64, wg64, np.ones(512), m)
             pos = m * np.arange(n0)
             c, sc = R.index_k_quant(R.index_k(pre_p, wik64, np.broadcast_to(pos, (B, n0))))
+            if stored_formats:
+                kc = np.zeros((B, n_cap, 256), np.uint8)
+                ks = np.zeros((B, n_cap, 32), np.uint8)
+                if n0 > 0:
+                    kc[:, :n0], ks[:, :n0] = R.main_kv_fp4(R.bf16_to_f64(R.f64_to_bf16_bits(kv_p)))
+                g.update(kv_codes=Hp.to_dev(kc, torch.uint8), kv_scales=Hp.to_dev(ks, torch.uint8))
             o.update(x=x64[:, n0 * m:], x_pos0=n0 * m, w_kv=wkv64, w_gate=wg64,
                      gamma=np.ones(512), w_ik=wik64,
                      prev_kv=R.bf16_to_f64(R.f64_to_bf16_bits(kv_p)), prev_codes=c,
@@ -101,9 +113,9 @@ def run_gpu(kv_src, idx_src, ratio, gpu_layers, B, Tq, q_pos0, H, hidden, k, blk
 
 
 def compare(kv_src, idx_src, ratio, gpu_layers, orc_layers, B, Tq, q_pos0, k, blk, nb, topks,
-            cands):
+            cands, stored_formats=False):
     outs, trace = Lr.run_step(kv_src, idx_src, ratio, orc_layers, B, Tq, q_pos0, k, hsi_blk=blk,
-                              hsi_nb=nb)
+                              hsi_nb=nb, main_kv_fp4=stored_formats, swa_fp8=stored_formats)
     modes = Lr.layer_modes(kv_src, idx_src)
     worst = 0.0
     for l, md in enumerate(modes):
@@ -161,3 +173,32 @@ def test_runner_decode_hsi_8_key_blocks():
     g, o = make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, q_pos0, hidden, H, seed0=900)
     runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, Tq, q_pos0, H, hidden, k, blk, nb)
     compare(kv_src, idx_src, ratio, g, o, B, Tq, q_pos0, k, blk, nb, topks, cands)
+
+
+def test_runner_decode_stored_formats():
+    """The pages' stored formats through the runner: FP4 main KV (the Full layers quantise
+    their new entries) and FP8 window rows, 64 heads, encoder-style Full m = 2 + Reuse and
+    decoder-style Full m = 1 + Reindex + Reuse."""
+    kv_src = [-1, 1, 1, 3, 3, 3]
+    idx_src = [-1, 1, 1, 3, 4, 4]
+    ratio = [0, 2, 0, 1, 0, 0]
+    B, Tq, hidden, H, k, blk, nb = 2, 1, 256, 64, 64, 16, 8
+    C = 900
+    q_pos0 = C - 1
+    g, o = make_stack(kv_src, idx_src, ratio, B, Tq, q_pos0, q_pos0 - 1, hidden, H, seed0=950,
+                      stored_formats=True)
+    runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, Tq, q_pos0, H, hidden, k, blk, nb)
+    # the step's new entries in FP4 against the oracle's quantiser of the oracle's own new
+    # entries (both from the seeded hidden states; the bf16 entries agree to within one bf16
+    # ulp, so a code may differ where that ulp crosses a rounding boundary)
+    for l in (1, 3):
+        m = ratio[l]
+        kv_new, _ = R.compress(o[l]["x"], o[l]["w_kv"], o[l]["w_gate"], o[l]["gamma"], m,
+                               o[l]["x_pos0"])
+        oc, os_ = R.main_kv_fp4(R.bf16_to_f64(R.f64_to_bf16_bits(kv_new)))
+        e0 = g[l]["x_pos0"] // m
+        e1 = e0 + kv_new.shape[1]
+        assert np.mean(g[l]["kv_codes"][:, e0:e1].cpu().numpy() == oc) > 0.98
+        assert np.mean(g[l]["kv_scales"][:, e0:e1].cpu().numpy() == os_) > 0.98
+    compare(kv_src, idx_src, ratio, g, o, B, Tq, q_pos0, k, blk, nb, topks, cands,
+            stored_formats=True)
