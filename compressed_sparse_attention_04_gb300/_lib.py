@@ -26,6 +26,7 @@ class LayerIO(C.Structure):
         ("q", vp), ("swa_kv", vp), ("sink", vp), ("out", vp),
         ("topk_out", vp), ("cand_out", vp),
         ("kv_codes", vp), ("kv_scales", vp), ("swa_codes", vp), ("swa_scales", vp),
+        ("compress_state", vp),
         ("x_tokens", i32), ("x_pos0", i32), ("n_cap", i32), ("swa_len", i32),
         ("swa_pos0", i32), ("reserved0", i32),
     ]

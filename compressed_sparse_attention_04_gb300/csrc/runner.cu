@@ -185,22 +185,31 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
       const int m = r->ratio[l];
       if (L.x_tokens > 0) {
         mark(r, l, 0, 0, stream);
-        st = csa2_compress(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv, L.w_gate,
-                           L.norm_w, p->eps, p->rope_base, L.kv_cache, L.n_cap,
-                           reinterpret_cast<float*>(ws + w.kv_pre), ws + w.gemm, gemm_bytes, stream);
+        // entries completed by this step's tokens: e0 .. e0 + g_new - 1 (with the group state a
+        // step may start or end inside a group; without it, only whole groups count)
+        const int e0 = L.x_pos0 / m;
+        const int g_new = L.compress_state ? (L.x_pos0 + L.x_tokens) / m - e0 : L.x_tokens / m;
+        st = L.compress_state
+                 ? csa2_compress_chunk(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv,
+                                       L.w_gate, L.norm_w, p->eps, p->rope_base, L.compress_state,
+                                       L.kv_cache, L.n_cap, reinterpret_cast<float*>(ws + w.kv_pre),
+                                       ws + w.gemm, gemm_bytes, stream)
+                 : csa2_compress(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv, L.w_gate,
+                                 L.norm_w, p->eps, p->rope_base, L.kv_cache, L.n_cap,
+                                 reinterpret_cast<float*>(ws + w.kv_pre), ws + w.gemm, gemm_bytes,
+                                 stream);
         if (st != CSA2_OK) return st;
         if (L.kv_codes || L.kv_scales) {   // the new entries in the stored FP4 format too
           if (!L.kv_codes || !L.kv_scales)
             return fail(CSA2_ERR_INVALID_ARG, "layer %d: FP4 main KV needs codes and scales", l);
-          st = csa2_main_kv_quant_fp4(L.kv_cache, p->B, L.n_cap, L.x_pos0 / m, L.x_tokens / m,
-                                      L.kv_codes, L.kv_scales, stream);
+          st = csa2_main_kv_quant_fp4(L.kv_cache, p->B, L.n_cap, e0, g_new, L.kv_codes, L.kv_scales,
+                                      stream);
           if (st != CSA2_OK) return st;
         }
         mark(r, l, 0, 1, stream);
         mark(r, l, 1, 0, stream);
-        st = csa2_index_k_quant(reinterpret_cast<float*>(ws + w.kv_pre), p->B, L.x_tokens / m,
-                                L.x_pos0 / m, m, L.w_ik, p->rope_base, L.idx_codes, L.idx_scales,
-                                L.n_cap, nullptr, stream);
+        st = csa2_index_k_quant(reinterpret_cast<float*>(ws + w.kv_pre), p->B, g_new, e0, m, L.w_ik,
+                                p->rope_base, L.idx_codes, L.idx_scales, L.n_cap, nullptr, stream);
         if (st != CSA2_OK) return st;
         mark(r, l, 1, 1, stream);
       }

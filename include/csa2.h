@@ -322,6 +322,11 @@ typedef struct {
   uint8_t* kv_scales;
   const uint8_t* swa_codes;
   const uint8_t* swa_scales;
+  /* Full, m == 2, optional: f32 [B, 1024] group state carried between steps (as in
+   * csa2_compress_chunk), so that a step may hand over any number of new tokens, down to one
+   * per sequence; without it x_pos0 must be a multiple of m and a trailing incomplete group is
+   * ignored. */
+  float* compress_state;
   int x_tokens;
   int x_pos0;
   int n_cap;

@@ -35,8 +35,8 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_struct_layouts_match_header():
-    # csa2_layer_io: 20 pointers + 6 ints; csa2_step_params: 8 ints + 4 floats
-    assert C.sizeof(L.LayerIO) == 20 * 8 + 6 * 4
+    # csa2_layer_io: 21 pointers + 6 ints; csa2_step_params: 8 ints + 4 floats
+    assert C.sizeof(L.LayerIO) == 21 * 8 + 6 * 4
     assert C.sizeof(L.StepParams) == 12 * 4
 
 

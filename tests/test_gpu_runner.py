@@ -202,3 +202,25 @@ def test_runner_decode_stored_formats():
         assert np.mean(g[l]["kv_scales"][:, e0:e1].cpu().numpy() == os_) > 0.98
     compare(kv_src, idx_src, ratio, g, o, B, Tq, q_pos0, k, blk, nb, topks, cands,
             stored_formats=True)
+
+
+def test_runner_streaming_compressor_one_token_per_step():
+    """Decode with m = 2 one token per step through the runner's group state: the first
+    step holds its token back (no new entry), the second completes the entry; both steps
+    match the oracle's step over the same tokens."""
+    kv_src, idx_src, ratio = [0, 0], [0, 0], [2, 0]
+    B, Tq, hidden, H, k = 2, 1, 128, 8, 32
+    P = 600                                            # first token of a new group
+    g, o = make_stack(kv_src, idx_src, ratio, B, Tq, P + 1, P, hidden, H, seed0=990, S_extra=1)
+    x2, x2_64 = g[0]["x"], o[0]["x"]                   # tokens P and P + 1
+    assert x2.shape[1] == 2 and g[0]["x_pos0"] == P
+    state = torch.zeros(B, 1024, dtype=torch.float32, device="cuda")
+    e_new = P // 2
+    for step, t in enumerate((P, P + 1)):
+        g[0].update(x=x2[:, step:step + 1].contiguous(), x_pos0=t, x_tokens=1, compress_state=state)
+        before = g[0]["kv_cache"][:, e_new].clone()
+        runner, topks, cands = run_gpu(kv_src, idx_src, ratio, g, B, Tq, t, H, hidden, k, 64, 64)
+        if step == 0:   # the group is incomplete: its entry is not written yet
+            assert torch.equal(g[0]["kv_cache"][:, e_new], before)
+        o1 = [dict(o[0], x=x2_64[:, : step + 1], x_pos0=P), o[1]]
+        compare(kv_src, idx_src, ratio, g, o1, B, Tq, t, k, 64, 64, topks, cands)
