@@ -285,42 +285,63 @@ struct StepCursor {
   __device__ int row(const ScoreArgs& a) const { return b * a.Tq + i; }
 };
 
-// One CTA per (query row, head), one warp per 32-dimension block: the FP4 query as the
-// MMA's B operand image (32 heads x 64 bytes, K-major, no swizzle) followed by its E4M3
-// block scales (4 bytes per head).  CTA 0 also writes the step prefix table.
-__global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep, int* prefix) {
+// One warp per (query row, head), grid-stride: the FP4 query as the MMA's B operand image
+// (32 heads x 64 bytes, K-major, no swizzle) followed by its E4M3 block scales (4 bytes per
+// head).  Lane l holds dims 4 l .. 4 l + 3, so lanes 8 b .. 8 b + 7 form 32-dim block b; the
+// block's scale and codes follow the same rules as fp4_quant_lane.  CTA 0 also writes the
+// step prefix table.
+__global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep, int* prefix,
+                                                     long long n_items) {
   pdl_wait();
   __shared__ int scan[32];
-  const int tid = threadIdx.x, blk4 = tid >> 5, lane = tid & 31;
-  const long long row = blockIdx.x >> 5;
-  const int h = blockIdx.x & 31;
-  const float v = bf16_to_f32(a.q_idx[size_t(row) * 32 * 128 + h * 128 + blk4 * 32 + lane]);
-  uint32_t sb;
-  const uint32_t code = fp4_quant_lane(v, sb);
-  // eight codes per 32-bit word (element 8 j + i in nibble i), words j = 0..3 -> 16 bytes
-  uint32_t word = code << (4 * (lane & 7));
-  word |= __shfl_xor_sync(0xffffffffu, word, 1);
-  word |= __shfl_xor_sync(0xffffffffu, word, 2);
-  word |= __shfl_xor_sync(0xffffffffu, word, 4);
-  const uint32_t w1 = __shfl_sync(0xffffffffu, word, 8), w2 = __shfl_sync(0xffffffffu, word, 16),
-                 w3 = __shfl_sync(0xffffffffu, word, 24);
-  uint8_t* out = qprep + size_t(row) * SU_QROW_BYTES;
-  if (lane == 0) {
-    *reinterpret_cast<uint4*>(out + fp4_chunk_off(h, blk4)) = make_uint4(word, w1, w2, w3);
-    out[SU_Q_BYTES + h * 4 + blk4] = uint8_t(sb);
+  const int tid = threadIdx.x, lane = tid & 31, blk = lane >> 3, l8 = lane & 7;
+  for (long long item = (long long)blockIdx.x * 4 + (tid >> 5); item < n_items;
+       item += (long long)gridDim.x * 4) {
+    const long long row = item >> 5;
+    const int h = int(item & 31);
+    const uint2 raw = *reinterpret_cast<const uint2*>(a.q_idx + size_t(row) * 32 * 128 + h * 128 + 4 * lane);
+    const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const uint32_t sb = e4m3_rne_satfinite(__fdiv_rn(amax, 6.0f));
+    // this lane's four codes: elements 4 l8 .. 4 l8 + 3 of the block = nibbles 4 (l8 & 1) ..
+    // 4 (l8 & 1) + 3 of the block's word l8 / 2 (element 8 j + i in nibble i of word j)
+    uint32_t part = 0u;
+    if (sb != 0u) {
+      const float sc = e4m3_value(sb);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float u = __fdiv_rn(v[e], sc);
+        part |= (((__float_as_uint(u) >> 31) << 3) | e2m1_rne_mag(fabsf(u))) << (4 * e);
+      }
+    }
+    const uint32_t word = (part << (16 * (l8 & 1))) | (__shfl_xor_sync(0xffffffffu, part, 1) << (16 * ((l8 & 1) ^ 1)));
+    const uint32_t w1 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 2);
+    const uint32_t w2 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 4);
+    const uint32_t w3 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 6);
+    uint8_t* out = qprep + size_t(row) * SU_QROW_BYTES;
+    if (l8 == 0) {
+      *reinterpret_cast<uint4*>(out + fp4_chunk_off(h, blk)) = make_uint4(word, w1, w2, w3);
+      out[SU_Q_BYTES + h * 4 + blk] = uint8_t(sb);
+    }
   }
   if (blockIdx.x == 0) {
+    // thread t sums the steps of rows [t per, (t + 1) per), one block scan of the 128 sums,
+    // then each thread writes its rows' offsets (one scan instead of Tq / 128 of them)
     const bool pool = a.cand != nullptr, bm = a.blockmax != nullptr;
-    int carry = 0;
-    for (int base = 0; base < a.Tq; base += 128) {
-      const int i = base + tid;
-      const int c = i < a.Tq ? row_steps(i, a.q_pos0, a.m, a.n_entries, a.row_len, pool, bm) : 0;
-      int tot;
-      const int ex = block_excl_scan<128>(c, scan, tot);
-      if (i < a.Tq) prefix[i] = carry + ex;
-      carry += tot;
+    const int per = (a.Tq + 127) / 128, i0 = tid * per, i1 = min(a.Tq, i0 + per);
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += row_steps(i, a.q_pos0, a.m, a.n_entries, a.row_len, pool, bm);
+    int tot;
+    int run = block_excl_scan<128>(mine, scan, tot);
+    for (int i = i0; i < i1; ++i) {
+      prefix[i] = run;
+      run += row_steps(i, a.q_pos0, a.m, a.n_entries, a.row_len, pool, bm);
     }
-    if (tid == 0) prefix[a.Tq] = carry;
+    if (tid == 0) prefix[a.Tq] = tot;
   }
 }
 
@@ -1137,7 +1158,9 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                    make_codes_map(&map1, codes, (long long)B * n_cap, 1) &&
                    make_codes_map(&map4, codes, (long long)B * n_cap, 4);
       if (sa.total_steps > 0) {
-        CSA2_LAUNCH("q_prep launch", q_prep_kernel, unsigned(rows * 32), 128, 0, st, sa, qprep, prefix);
+        const long long n_items = (long long)rows * 32, q_ctas = (n_items + 3) / 4;
+        CSA2_LAUNCH("q_prep launch", q_prep_kernel, unsigned(q_ctas < 4096 ? q_ctas : 4096), 128, 0, st, sa,
+                    qprep, prefix, n_items);
         note_launch();
         const long long grid = sa.total_steps < slots[dev] ? sa.total_steps : slots[dev];
         CSA2_LAUNCH("score_fp4 launch", score_fp4_kernel, unsigned(grid), SU_T, SU_SMEM, st, sa, map1, map4);
