@@ -23,6 +23,7 @@
 // 32; lane j scores row j of the tile; an online softmax keeps (max, sum) per head
 // and every lane accumulates 16 of the 512 output dims.
 #include <algorithm>
+#include <atomic>
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -913,22 +914,26 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     // tensor-core path: a cluster of n_split CTAs per row (enough CTAs to cover the SMs),
     // partial results merged through distributed shared memory
     (void)workspace; (void)ws_bytes;
-    static int sms_cache[64] = {0};
+    // per device, once: the kernels' shared-memory attribute and the SM count (cached only
+    // after both succeeded; concurrent first calls repeat the same settings)
+    static std::atomic<int> sms_cache[64];
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: device id");
-    if (sms_cache[dev] == 0) {
+    int sms = sms_cache[dev].load(std::memory_order_acquire);
+    if (sms == 0) {
       e0 = cudaFuncSetAttribute(attn_flash_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
       if (e0 == cudaSuccess)
         e0 = cudaFuncSetAttribute(attn_flash_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
-      if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms_cache[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
+      sms_cache[dev].store(sms, std::memory_order_release);
     }
     // CTAs per row: all CTAs in one wave, and the estimated time of a row's chunks (about
     // 1.5 us each, per CTA) plus the cluster merge (about 4 us) the smallest
     const int n_ch_max = ceil_div(k + window, AF_CH);
-    const int n_fit = std::max(1, std::min(int(sms_cache[dev] / rows), AF_MAX_SPLIT));
+    const int n_fit = std::max(1, std::min(int(sms / rows), AF_MAX_SPLIT));
     int n_split = 1;
     for (int n = 2; n <= n_fit; ++n) {
       const int t_n = 3 * ceil_div(n_ch_max, n) + 8, t_best = 3 * ceil_div(n_ch_max, n_split) + (n_split > 1 ? 8 : 0);

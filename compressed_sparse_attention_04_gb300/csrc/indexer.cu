@@ -25,6 +25,7 @@
 //   hsi_kernel     one CTA per query row: top-nb blocks with the newest block forced.
 #include <cuda.h>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "common.cuh"
@@ -1030,17 +1031,15 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+EncodeTiledFn encode_fn() {   // looked up once (thread-safe static initialisation)
+  static const EncodeTiledFn fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess && q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return EncodeTiledFn(nullptr);
+  }();
   return fn;
 }
 bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys, int nblk) {
@@ -1131,11 +1130,12 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
       sa.total_steps = per_seq * B;
       if (per_seq > (1ll << 31) - 1 || sa.total_steps > (1ll << 40))
         return fail(CSA2_ERR_UNSUPPORTED, "indexer: problem too large for one call");
-      static int slots[64] = {0};   // resident scoring CTAs per device
+      static std::atomic<int> slots[64];   // resident scoring CTAs per device (0: not yet known)
       int dev = 0;
       cudaError_t e0 = cudaGetDevice(&dev);
       if (e0 == cudaSuccess && (dev < 0 || dev >= 64)) return fail(CSA2_ERR_UNSUPPORTED, "indexer: device id");
-      if (e0 == cudaSuccess && slots[dev] == 0) {
+      int n_slots = e0 == cudaSuccess ? slots[dev].load(std::memory_order_acquire) : 0;
+      if (e0 == cudaSuccess && n_slots == 0) {
         e0 = cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(SU_SMEM));
         if (e0 == cudaSuccess)
@@ -1148,7 +1148,10 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
         if (e0 == cudaSuccess)
           e0 = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         const int per_cta = int(SU_SMEM) + 2048;   // + static shared memory and the reserved 1 KB
-        if (e0 == cudaSuccess) slots[dev] = sms * (smem_sm >= 2 * per_cta ? 2 : 1);
+        if (e0 == cudaSuccess) {
+          n_slots = sms * (smem_sm >= 2 * per_cta ? 2 : 1);
+          slots[dev].store(n_slots, std::memory_order_release);
+        }
       }
       if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: scorer attributes");
       CUtensorMap map1, map4;   // boxes of one block (pool steps) and four (dense steps)
@@ -1162,7 +1165,7 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
         CSA2_LAUNCH("q_prep launch", q_prep_kernel, unsigned(q_ctas < 4096 ? q_ctas : 4096), 128, 0, st, sa,
                     qprep, prefix, n_items);
         note_launch();
-        const long long grid = sa.total_steps < slots[dev] ? sa.total_steps : slots[dev];
+        const long long grid = sa.total_steps < n_slots ? sa.total_steps : n_slots;
         CSA2_LAUNCH("score_fp4 launch", score_fp4_kernel, unsigned(grid), SU_T, SU_SMEM, st, sa, map1, map4);
         note_launch();
       }
