@@ -413,3 +413,51 @@ def test_runner_reindex_with_full_pool_equals_full_topk():
     for i in range(Tq):
         nv = R.n_visible(q_pos0 + i, 1, 62)
         assert (nv - 1) // 8 in cand[0, i]
+
+
+def _fp4_exact_rows(rng, shape):
+    """Rows whose 16-channel groups are E2M1 values times an E4M3 scale with one element at
+    6 x scale: the FP4 main-KV quantiser reproduces them exactly."""
+    mags = fp4.E2M1_MAG
+    v = rng.choice(mags, size=shape + (512,)) * rng.choice([-1.0, 1.0], size=shape + (512,))
+    g = v.reshape(shape + (32, 16))
+    g[..., 0] = 6.0
+    scale = fp4.e4m3_value(rng.integers(0x18, 0x30, size=shape + (32,)))   # 2^-4 .. 0.875
+    return (g * scale[..., None]).reshape(shape + (512,))
+
+
+def _fp8_exact_rows(rng, shape):
+    """Rows whose 64-channel groups are E4M3 grid values times 2^k with one element in
+    (224, 448] x 2^k: the FP8 window quantiser reproduces them exactly."""
+    grid = fp4._E4M3_GRID
+    c = rng.integers(0, 127, size=shape + (8, 64))
+    c[..., 0] = rng.integers(0x70, 0x7F, size=shape + (8,))
+    k = rng.integers(-12, -8, size=shape + (8,))                          # |v| < 1.75
+    v = grid[c] * np.where(rng.random(c.shape) < 0.5, -1.0, 1.0) * np.exp2(k)[..., None]
+    return v.reshape(shape + (512,))
+
+
+def test_run_step_stored_formats_reduce_to_plain_on_representable_rows():
+    """[P3] section 七: attention reads FP4 entries and FP8 window rows after dequantisation;
+    on rows the two formats hold exactly, the stored-format step equals the plain step, and
+    moving one window value off the FP8 grid changes it."""
+    rng = _rng(21)
+    kv_src, idx_src, ratio = [-1, 1, 1], [-1, 1, 1], [0, 2, 0]
+    B, Tq = 2, 1
+    q_pos0 = 80                                     # token 80 starts a group: no new entry
+    layers = _tiny_stack_inputs(rng, kv_src, ratio, B, Tq, q_pos0, n0_tokens=80)
+    n0 = layers[1]["prev_kv"].shape[1]
+    layers[1]["prev_kv"] = _fp4_exact_rows(rng, (B, n0))
+    for L in layers:
+        L["swa"] = _fp8_exact_rows(rng, L["swa"].shape[:2])
+    assert layers[1]["x"].shape[1] == 1
+    plain, _ = Lr.run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k=8)
+    stored, _ = Lr.run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k=8,
+                            main_kv_fp4=True, swa_fp8=True)
+    for a, b in zip(plain, stored):
+        np.testing.assert_array_equal(a, b)
+    layers[0]["swa"][:, q_pos0, 5] += 1e-3 * np.sign(layers[0]["swa"][:, q_pos0, 5] + 0.5)  # off the grid
+    moved, _ = Lr.run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k=8,
+                           main_kv_fp4=True, swa_fp8=True)
+    plain2, _ = Lr.run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k=8)
+    assert not np.array_equal(moved[0], plain2[0])
