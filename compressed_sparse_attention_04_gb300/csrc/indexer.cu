@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
 // The MMA yields sum_blocks s_q s_k sum(e2m1 products) per (key, head) = q_hat . k_hat.
 constexpr int SU_TILE = 128;                 // keys per MMA tile (M)
 constexpr int SU_STEP = 256;                 // keys per pipeline step: two MMA tiles
-constexpr int SU_STEPS = 32;                 // steps per CTA (8192 keys)
 constexpr int SU_STAGES = 6;                 // code / scale ring (in steps)
 constexpr int SU_ND = 2;                     // TMEM accumulator buffers (in steps)
 constexpr int SU_T = 320;                    // 4 producer + 4 epilogue + 1 MMA + 1 copy warp
