@@ -57,22 +57,30 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def attention_kernel_hash(text):
+    """16 hex digits of SHA-256 over the kernel part of attention.cu: everything before its
+    first extern "C" block (the host entry points follow it), #include lines left out."""
+    import hashlib
+    head = text[:text.index('\nextern "C" {')]
+    body = "\n".join(l for l in head.splitlines() if not l.startswith("#include"))
+    return hashlib.sha256(body.encode()).hexdigest()[:16]
+
+
 def attention_traffic(modes):
     """DRAM bytes per attention launch, averaged over one step's layers, from the ncu record in
     profiles/attn_flash_b64_ctx8k.md (layers with a global branch read the headline shape,
-    window-only layers 128 rows).  None when the kernel source no longer matches the record
-    or the record is missing."""
-    import hashlib
+    window-only layers 128 rows).  None when the kernel code no longer matches the record or
+    the record is missing."""
     try:
         rec = {}
         with open(os.path.join(ROOT, "profiles", "attn_flash_b64_ctx8k.md")) as f:
             for line in f:
                 parts = line.strip().split(":")
-                if len(parts) == 2 and parts[0].startswith(("traffic_", "attention_source")):
+                if len(parts) == 2 and parts[0].startswith(("traffic_", "attention_kernel")):
                     rec[parts[0].strip()] = parts[1].strip()
-        with open(os.path.join(ROOT, "compressed_sparse_attention_04_gb300", "csrc", "attention.cu"), "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-        if rec.get("attention_source_sha256_16") != h:
+        with open(os.path.join(ROOT, "compressed_sparse_attention_04_gb300", "csrc", "attention.cu")) as f:
+            h = attention_kernel_hash(f.read())
+        if rec.get("attention_kernel_sha256_16") != h:
             return None
         full, win = int(rec["traffic_full_launch_bytes"]), int(rec["traffic_window_launch_bytes"])
         return sum(win if m == 0 else full for m in modes) / len(modes)
