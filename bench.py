@@ -337,6 +337,18 @@ def job_throughput(batch, world, ms):
 
 
 # ----------------------------------------------------------------------------- main arms
+def workload_config(wl, world):
+    """The `config` object both arms print: the workload's name and shape."""
+    return {"workload": f"csa2_decode_40layer_b{wl['B']}_ctx{wl['C']}" +
+                        (f"_hsi{wl['nb']}x{wl['blk']}" if wl["blk"] != 64 else "") +
+                        ("_fp4kv_fp8swa" if wl.get("stored") else ""),
+            "batch": wl["B"], "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
+            "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
+            "kv_format": "fp4 main kv, fp8 window rows" if wl.get("stored") else "bf16",
+            "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return 0
@@ -354,7 +366,7 @@ def run_reference(args, wl, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / reps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"csa2_decode_40layer_b{wl['B']}_ctx{wl['C']}", "parallelism": "replicas"},
+            "config": workload_config(wl, world),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": "one sequence of the decode step per timed step (B=1 of the "
                                        f"{wl['B']}-sequence batch, full-size caches)"},
@@ -499,16 +511,9 @@ def run_ours(args, wl, rank, world, local_rank):
         "metric": METRIC, "value": job_throughput(B, world, ms), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"csa2_decode_40layer_b{B}_ctx{wl['C']}" +
-                               (f"_hsi{wl['nb']}x{wl['blk']}" if wl["blk"] != 64 else "") +
-                               ("_fp4kv_fp8swa" if wl.get("stored") else ""), "batch": B,
-                   "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
-                   "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
-                   "kv_format": "fp4 main kv, fp8 window rows" if wl.get("stored") else "bf16",
-                   "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",
-                   "launch": "cuda_graph" if args.graph else "direct",
-                   "timing": "headline pass without per-stage events; stage times from a second pass",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": dict(workload_config(wl, world),
+                       launch="cuda_graph" if args.graph else "direct",
+                       timing="headline pass without per-stage events; stage times from a second pass"),
         "roofline": {"bound": "hbm", "kernel": STAGE_NAMES[dom], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": attention_traffic(st.modes) if STAGE_NAMES[dom] == "sparse_attn" and
