@@ -349,6 +349,48 @@ def workload_config(wl, world):
             "parallelism": "replicas" if world > 1 else "single"}
 
 
+def run_indexer_prefill(args):
+    """The indexer of the 16384-token encoder prefill on its own: 16384 queries x 8192 FP4
+    index keys (m = 2, causal), 32 heads x 128, top-512; W warm-up calls, then the median of
+    K (at least 10) CUDA-event timed calls.  One JSON line; not the bench line."""
+    import numpy as np
+    import torch
+    from compressed_sparse_attention_04_gb300 import build, ops
+    from synth import gpu as sg
+    build.build_all()
+    Tq, N, m, k, seed = 16384, 8192, 2, 512, 9500
+    codes = torch.empty(1, N, 64, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(1, N, 4, dtype=torch.uint8, device="cuda")
+    r = torch.empty(N * 68, dtype=torch.int32, device="cuda")
+    sg.fill_u32(r, seed, 3, 0)
+    r = r.view(1, N, 68)
+    codes[:] = (r[..., :64] & 0xFF).to(torch.uint8)
+    scales[:] = (0x18 + (r[..., 64:] & 0x3F)).to(torch.uint8)
+    qi = sg.fill_normal(torch.empty(1, Tq, 32, 128, dtype=torch.bfloat16, device="cuda"), seed, 1, 0, 1.28)
+    w = sg.fill_normal(torch.empty(1, Tq, 32, dtype=torch.float32, device="cuda"), seed, 2, 0, 1.28)
+    topk = torch.empty(1, Tq, k, dtype=torch.int32, device="cuda")
+    call = lambda: ops.indexer_score_topk(qi, w, 0, codes, scales, N, m, k, topk_out=topk)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(args.steps, 10)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert ops.last_device_status() == 0
+    pairs = sum(min((i + 1) // m, N) for i in range(Tq))
+    gflop = pairs * 32 * 128 * 2 / 1e9
+    ms = float(np.median(ts))
+    print(json.dumps({"metric": "indexer call (scores + top-k), 16384-token prefill", "ms_per_call": ms,
+                      "causal_pairs": pairs, "fp4_gflop": gflop,
+                      "note": "the scorer kernel's own time comes from the ncu launch list"}), flush=True)
+    return 0
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return 0
@@ -647,6 +689,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode40")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--indexer-prefill", action="store_true",
+                    help="time the indexer of the 16384-token prefill alone (one JSON line, not the bench line)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each timed step as a captured CUDA graph (measured 1.607 ms per step "
                          "against 1.587 ms for direct launches with programmatic dependent launch)")
@@ -654,6 +698,8 @@ def main():
     if args.warmup < 3:
         print("[bench] warm-up raised to 3 steps (minimum)", file=sys.stderr)
         args.warmup = 3
+    if args.indexer_prefill:
+        return run_indexer_prefill(args)
     wl = WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
