@@ -391,6 +391,57 @@ def run_indexer_prefill(args):
     return 0
 
 
+def run_attention_formats(args):
+    """The decode attention launch at the headline shape (64 rows x (512 entries + 128 window
+    rows) x 64 heads, 64K-entry caches) with each stored format: bf16, FP8 window rows, FP4
+    entries, both.  Per format: W warm-up launches, then the mean of 40 back-to-back launches
+    (CUDA events).  One JSON line; not the bench line."""
+    import torch
+    from compressed_sparse_attention_04_gb300 import build, ops
+    from synth import gpu as sg
+    build.build_all()
+    B, N, H, k, S = 64, 65536, 64, 512, 256
+    t = 131071
+    q = sg.fill_normal(torch.empty(B, 1, H, 512, dtype=torch.bfloat16, device="cuda"), 1, 1, 0, 1.28)
+    kv = sg.fill_normal(torch.empty(B, N, 512, dtype=torch.bfloat16, device="cuda"), 1, 2)
+    codes = torch.empty(B, N, 256, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(B, N, 32, dtype=torch.uint8, device="cuda")
+    ops.main_kv_quant_fp4(kv, 0, N, codes, scales)
+    swa = sg.fill_normal(torch.empty(B, S, 512, dtype=torch.bfloat16, device="cuda"), 1, 3)
+    wc = torch.empty(B, S, 512, dtype=torch.uint8, device="cuda")
+    wsc = torch.empty(B, S, 8, dtype=torch.uint8, device="cuda")
+    ops.swa_kv_quant_fp8(swa, 0, S, wc, wsc)
+    # 512 distinct ascending entries per row, spread over the cache
+    base = (torch.arange(k, device="cuda", dtype=torch.int64) * N) // k
+    off = (torch.arange(B, device="cuda", dtype=torch.int64) * 37) % (N // k)
+    topk = (base[None, :] + off[:, None]).to(torch.int32).view(B, 1, k).contiguous()
+    out = torch.empty(B, 1, H, 512, device="cuda", dtype=torch.bfloat16)
+    runs = {"bf16": lambda: ops.sparse_attn(q, t, kv, N, topk, swa, t - S + 1, out=out),
+            "fp8_window": lambda: ops.sparse_attn(q, t, kv, N, topk, None, t - S + 1, out=out,
+                                                  swa_fp8=(wc, wsc)),
+            "fp4_entries": lambda: ops.sparse_attn(q, t, None, N, topk, swa, t - S + 1, out=out,
+                                                   kv_fp4=(codes, scales)),
+            "fp4_entries_fp8_window": lambda: ops.sparse_attn(q, t, None, N, topk, None, t - S + 1,
+                                                              out=out, kv_fp4=(codes, scales),
+                                                              swa_fp8=(wc, wsc))}
+    res = {}
+    for name, f in runs.items():
+        for _ in range(args.warmup):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(40):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) * 1000 / 40
+    assert ops.last_device_status() == 0
+    print(json.dumps({"metric": "decode attention launch, 64 x (512 + 128) rows x 64 heads",
+                      "unit": "us per launch (back to back)", "per_format": res}), flush=True)
+    return 0
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return 0
@@ -691,6 +742,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--indexer-prefill", action="store_true",
                     help="time the indexer of the 16384-token prefill alone (one JSON line, not the bench line)")
+    ap.add_argument("--attention-formats", action="store_true",
+                    help="time the decode attention launch with each stored format (one JSON line)")
     ap.add_argument("--graph", action="store_true",
                     help="replay each timed step as a captured CUDA graph (measured 1.607 ms per step "
                          "against 1.587 ms for direct launches with programmatic dependent launch)")
@@ -700,6 +753,8 @@ def main():
         args.warmup = 3
     if args.indexer_prefill:
         return run_indexer_prefill(args)
+    if args.attention_formats:
+        return run_attention_formats(args)
     wl = WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
