@@ -73,12 +73,13 @@ def attention_traffic(modes):
     the record is missing."""
     try:
         rec = {}
-        with open(os.path.join(ROOT, "profiles", "attn_flash_b64_ctx8k.md")) as f:
+        with open(os.path.join(ROOT, "profiles", "attn_flash_b64_ctx8k.md"), encoding="utf-8") as f:
             for line in f:
                 parts = line.strip().split(":")
                 if len(parts) == 2 and parts[0].startswith(("traffic_", "attention_kernel")):
                     rec[parts[0].strip()] = parts[1].strip()
-        with open(os.path.join(ROOT, "compressed_sparse_attention_04_gb300", "csrc", "attention.cu")) as f:
+        with open(os.path.join(ROOT, "compressed_sparse_attention_04_gb300", "csrc", "attention.cu"),
+                  encoding="utf-8") as f:
             h = attention_kernel_hash(f.read())
         if rec.get("attention_kernel_sha256_16") != h:
             return None
