@@ -58,12 +58,19 @@ def peaks():
 
 
 def attention_kernel_hash(text):
-    """16 hex digits of SHA-256 over the kernel part of attention.cu: everything before its
-    first extern "C" block (the host entry points follow it), #include lines left out."""
+    """16 hex digits of SHA-256 over the kernel code of attention.cu: everything before its
+    first extern "C" block (the host entry points follow it), with #include lines, // comments
+    and blank lines left out."""
     import hashlib
     head = text[:text.index('\nextern "C" {')]
-    body = "\n".join(l for l in head.splitlines() if not l.startswith("#include"))
-    return hashlib.sha256(body.encode()).hexdigest()[:16]
+    code = []
+    for line in head.splitlines():
+        if line.startswith("#include"):
+            continue
+        line = line.split("//", 1)[0].rstrip()
+        if line:
+            code.append(line)
+    return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
 def attention_traffic(modes):

@@ -17,6 +17,10 @@
 // (512 dims x 64 heads) in TMEM, reading the SAME shared tile as the MN-major operand
 // (K = V).  The CTAs of a cluster combine their (max, sum, O) through distributed shared
 // memory; nothing intermediate goes to global memory.
+// Its second instantiation serves stored formats ([P3] §六, §七): FP4 entries (E2M1 with one
+// E4M3 scale per 16 channels) and / or FP8 window rows (E4M3 with one power-of-two scale per
+// 64 channels) are loaded into registers as 16-byte pieces before the ring slot is free and
+// dequantised exactly into the same bf16 tile.
 //
 // attn_simt_kernel (any H): one CTA per (query row, group of 8 heads), one warp per head.
 // Rows of A (top-k slots then window rows) stream through shared memory in tiles of

@@ -15,7 +15,9 @@
 //                      used when there are few rows, as in decode) are summed in fixed order
 //                      by the epilogue, so results do not depend on scheduling.
 //   proj_gemm_kernel   SIMT fallback of the same product
-//   compress_epilogue  per entry: softmax-pool over the group, RMSNorm, RoPE, stores
+//   compress_epilogue  per entry: softmax-pool over the group, RMSNorm, RoPE, stores; with a
+//                      group state (csa2_compress_chunk) also the entry a previous call's
+//                      token started and the stash of a group this call leaves open
 //   index_k_kernel     per entry: 512 -> 128 projection, RoPE, FP4 quantisation
 //   main_kv_fp4_kernel per entry: the stored main-KV entry as FP4 (E2M1 codes, one E4M3
 //                      scale per 16 channels: 288 bytes)

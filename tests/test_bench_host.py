@@ -36,7 +36,8 @@ def test_traffic_record_lookup():
     # a host-side edit after the first extern "C" block leaves the kernel hash unchanged
     i = src.index('\nextern "C" {')
     assert bench.attention_kernel_hash(src[:i] + src[i:] + "\n// host note\n") == h
-    assert bench.attention_kernel_hash("// kernel edit\n" + src) != h
+    assert bench.attention_kernel_hash("// a comment\n" + src) == h          # comments ignored
+    assert bench.attention_kernel_hash("static int edit;\n" + src) != h
 
 
 class _FakeStack:
