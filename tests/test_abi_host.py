@@ -197,3 +197,24 @@ def test_runner_modes_and_rejections(lib):
         assert st == L.ERR_INVALID_ARG, (kv_, idx_)
     assert _runner(lib, [0], [0], [3])[0] == L.ERR_UNSUPPORTED
     assert _runner(lib, [0], [0], [1], blk=48)[0] == L.ERR_UNSUPPORTED
+
+
+def _header_struct_fields(name):
+    """Field names of typedef struct { ... } name; in include/csa2.h, in order."""
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    m = re.search(r"typedef struct \{([^{}]*)\}\s*" + name + r"\s*;", src)
+    assert m, name
+    fields = []
+    for decl in m.group(1).split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        for part in decl.split(","):
+            fields.append(re.findall(r"[A-Za-z_][A-Za-z0-9_]*", part)[-1])
+    return fields
+
+
+def test_struct_field_order_matches_header():
+    assert [f for f, _ in L.LayerIO._fields_] == _header_struct_fields("csa2_layer_io")
+    assert [f for f, _ in L.StepParams._fields_] == _header_struct_fields("csa2_step_params")
