@@ -218,3 +218,36 @@ def _header_struct_fields(name):
 def test_struct_field_order_matches_header():
     assert [f for f, _ in L.LayerIO._fields_] == _header_struct_fields("csa2_layer_io")
     assert [f for f, _ in L.StepParams._fields_] == _header_struct_fields("csa2_step_params")
+
+
+def _header_prototypes():
+    """name -> list of parameter kinds ('ptr', 'int', 'float', 'size') from include/csa2.h."""
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(csa2_[a-z0-9_]+)\s*\(([^()]*)\)\s*;", src):
+        params = m.group(2).strip()
+        kinds = []
+        if params and params != "void":
+            for p in params.split(","):
+                p = p.strip()
+                if "*" in p:
+                    kinds.append("ptr")
+                elif re.search(r"\bsize_t\b", p):
+                    kinds.append("size")
+                elif re.search(r"\bfloat\b", p):
+                    kinds.append("float")
+                else:
+                    assert re.search(r"\b(int|int32_t|unsigned)\b", p), p
+                    kinds.append("int")
+        out[m.group(1)] = kinds
+    return out
+
+
+def test_ctypes_signatures_match_header_prototypes():
+    kind_of = {C.c_void_p: "ptr", C.c_int: "int", C.c_float: "float", C.c_size_t: "size"}
+    protos = _header_prototypes()
+    assert set(protos) == set(L.SIGNATURES)
+    for name, (_, argtypes) in L.SIGNATURES.items():
+        got = [kind_of.get(t, "ptr") for t in argtypes]   # POINTER(...) types are pointers
+        assert got == protos[name], name
