@@ -251,3 +251,14 @@ def test_ctypes_signatures_match_header_prototypes():
     for name, (_, argtypes) in L.SIGNATURES.items():
         got = [kind_of.get(t, "ptr") for t in argtypes]   # POINTER(...) types are pointers
         assert got == protos[name], name
+
+
+def test_library_exports_nothing_undeclared(lib):
+    import shutil
+    import subprocess
+    if not shutil.which("nm"):
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {w for line in out.splitlines() for w in line.split()[-1:] if w.startswith("csa2_")}
+    assert exported == set(_declared_functions())
