@@ -262,3 +262,38 @@ def test_library_exports_nothing_undeclared(lib):
                          check=True).stdout
     exported = {w for line in out.splitlines() for w in line.split()[-1:] if w.startswith("csa2_")}
     assert exported == set(_declared_functions())
+
+
+def test_plain_c_program_links_and_calls_the_library(lib, tmp_path):
+    """The boundary is usable from C: the header compiles as C99 and a C program linked
+    against libcsa2.so runs its host-only calls (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if not cc:
+        pytest.skip("no C compiler")
+    prog = tmp_path / "abi_check.c"
+    prog.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "csa2.h"
+int main(void) {
+  if (strncmp(csa2_version(), "csa2", 4) != 0) return 1;
+  if (strcmp(csa2_status_str(CSA2_ERR_WORKSPACE), "CSA2_ERR_WORKSPACE") != 0) return 2;
+  /* host-side validation: m = 3 is refused before any launch */
+  int st = csa2_compress((void*)16, 1, 2, 64, 3, 0, (void*)16, (void*)16, (float*)16, 1e-6f,
+                         1e4f, (void*)16, 4, NULL, NULL, 0, NULL);
+  if (st != CSA2_ERR_UNSUPPORTED) return 3;
+  if (csa2_last_error_message()[0] == 0) return 4;
+  printf("ok\n");
+  return 0;
+}
+''')
+    exe = tmp_path / "abi_check"
+    libdir = os.path.dirname(L.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(prog), "-L", libdir, "-lcsa2", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stderr)
