@@ -16,6 +16,8 @@ only module both sides use is the seeded input generator ``synth``.
 Parity-unpinned readings (the pages print no value that could confirm them):
 RMSNorm epsilon 1e-6; interleaved RoPE pairs; the ReLU form of the indexer
 score; the E4M3 scale rule amax/6 rounded to nearest-even; FP4 quantisation of
-indexer queries; the attention-sink form; the 1/sqrt(512) attention scale.
-Each is a single named constant or switch in ``csa2_ref``.
+indexer queries; the attention-sink form; the 1/sqrt(512) attention scale;
+the stored formats' group sizes (FP4 main KV: one E4M3 scale per 16 channels;
+FP8 window rows: one power-of-two scale per 64 channels, ``fp8.py``).
+Each is a single named constant or switch in ``csa2_ref`` / ``fp8``.
 """
