@@ -33,7 +33,9 @@ def bf16_to_f64(bits):
 
 def f64_to_bf16_bits(x):
     """Round float64 -> float32 -> bf16 (nearest-even both times), as the GPU stores
-    its float32 results."""
+    its float32 results.  Pinned by hand-worked values (ties both ways, signed zeros,
+    subnormals, overflow, and inputs where the two-step rounding differs from one step):
+    tests/golden/bf16_rounding.txt."""
     f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
     b = f.view(np.uint32).astype(np.uint64)
     b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)

@@ -461,3 +461,39 @@ def test_run_step_stored_formats_reduce_to_plain_on_representable_rows():
                            main_kv_fp4=True, swa_fp8=True)
     plain2, _ = Lr.run_step(kv_src, idx_src, ratio, layers, B, Tq, q_pos0, k=8)
     assert not np.array_equal(moved[0], plain2[0])
+
+
+# ---- bf16 store rounding ----------------------------------------------------------------
+def test_bf16_store_rounding_golden():
+    """f64_to_bf16_bits against hand-worked values (tests/golden/bf16_rounding.txt): ties
+    to even in both directions, signed zeros, subnormals (including a tie), overflow to
+    infinity at bf16 max + half an ulp, and two float64 inputs where rounding through
+    float32 (the GPU's path: a float32 result stored as bf16) differs from rounding float64
+    to bf16 in one step -- so truncation, a lost tie rule or one-step rounding each fail."""
+    g = read_golden("bf16_rounding.txt")
+    rows = g["round"]
+    assert len(rows) >= 18
+    xs = np.array([float.fromhex(r[1]) for r in rows])
+    want = np.array([int(r[2], 16) for r in rows], dtype=np.uint16)
+    got = R.f64_to_bf16_bits(xs)
+    bad = [(r[0], hex(int(a)), hex(int(b))) for r, a, b in zip(rows, got, want) if a != b]
+    assert not bad, bad
+    # elementwise on any shape, one value at a time the same
+    assert (R.f64_to_bf16_bits(xs.reshape(2, -1)).ravel() == want).all()
+    assert all(R.f64_to_bf16_bits(np.float64(x)) == w for x, w in zip(xs, want))
+
+
+def test_bf16_widening_golden_and_round_trip():
+    g = read_golden("bf16_rounding.txt")
+    for bits, val in g["widen"]:
+        v = R.bf16_to_f64(np.uint16(int(bits, 16)))
+        want = float("inf") if val == "inf" else float.fromhex(val)
+        assert v == want and np.signbit(v) == np.signbit(want), (bits, v, want)
+    # every finite bf16 widens exactly and rounds back to itself
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = R.bf16_to_f64(allb)
+    fin = np.isfinite(v)
+    assert (R.f64_to_bf16_bits(v[fin]) == allb[fin]).all()
+    # widening is monotone over the positive finite patterns
+    pos = v[: 0x7F80]
+    assert (np.diff(pos) > 0).all()
