@@ -9,6 +9,8 @@
 // loaded on a device and stays until the process exits.
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace {
@@ -19,25 +21,58 @@ static __device__ __align__(256) unsigned char g_indexer_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// A __device__ array's address belongs to the CUDA context that loaded the module, not to
+// the device: after cudaDeviceReset the primary context (and the array) is created anew,
+// and a context made current through the driver API holds a copy of its own.  So each
+// device slot remembers the context its address was looked up in, and a call made under
+// another context looks the address up again.
+struct ScratchSlot {
+  CUcontext ctx;
+  void* ptr;
+};
+ScratchSlot g_slot[kMaxDevices] = {};
 
-// Device address of g_indexer_scratch on the current device (looked up once per device).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CtxGetCurrentFn ctx_get_current_fn() {   // driver entry point, looked up once
+  static const CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return CtxGetCurrentFn(nullptr);
+  }();
+  return fn;
+}
+
+// Device address of g_indexer_scratch in the current context of the current device.
+// With no context current yet (a thread's first runtime call), the symbol lookup itself
+// makes the device's primary context current, so the context is read again after it.
 int scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return csa2::cuda_fail(e, "indexer_noalloc: cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices)
     return csa2::fail(CSA2_ERR_UNSUPPORTED, "indexer_noalloc: device ordinal %d not supported", dev);
+  CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx)
+    return csa2::fail(CSA2_ERR_CUDA, "indexer_noalloc: driver entry point cuCtxGetCurrent not found");
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  ScratchSlot& slot = g_slot[dev];
+  if (ctx == nullptr || slot.ptr == nullptr || slot.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_indexer_scratch);
     if (e != cudaSuccess || !p)
       return csa2::cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
                              "indexer_noalloc: cudaGetSymbolAddress of the scratch array");
-    g_scratch_ptr[dev] = p;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+      return csa2::fail(CSA2_ERR_CUDA, "indexer_noalloc: no current CUDA context");
+    slot.ctx = ctx;
+    slot.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return CSA2_OK;
 }
 

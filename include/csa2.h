@@ -196,15 +196,21 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
  * convenience.  Same computation, arguments and results as csa2_indexer_score_topk
  * (no scores_out, no workspace), for callers that cannot allocate device memory --
  * e.g. code running inside an allocator hook or under a framework that has reserved
- * all device memory, or a plain C host with no GPU allocator of its own.  The score
- * scratch lives in a fixed 16 MiB array inside the library (so B * Tq * row_len <=
- * 4 Mi scores, row_len = n_entries, or nb * blk with cand); every GPU that loads the
- * library holds that array until the process exits.  Larger calls return
- * CSA2_ERR_UNSUPPORTED.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress); make that first call before any stream capture.
- * All calls share the one array: calls that overlap on the GPU (other streams,
- * other host threads) race and must be serialised by the caller.  Nothing in the
- * array needs to start at zero: each call writes every score it reads.
+ * all device memory, or a plain C host with no GPU allocator of its own.  The scratch
+ * that csa2_indexer_score_topk takes as its workspace lives here in a fixed 16 MiB
+ * array inside the library; every GPU that loads the library holds that array until
+ * the process exits.  A call is accepted exactly when
+ *   csa2_indexer_workspace_size(B, Tq, n_entries, nb, blk, cand != NULL)
+ *       <= csa2_indexer_noalloc_max_scratch_bytes()
+ * (scores of every row plus, for rows longer than 32768 entries, the chunked
+ * selection's candidate lists, and 2176 bytes of FP4 query image per query row);
+ * larger calls return CSA2_ERR_UNSUPPORTED before any launch.  The array's device
+ * address is looked up (cudaGetSymbolAddress) on the first call in each CUDA context
+ * of a device -- again after cudaDeviceReset or under another context; make that
+ * first call before any stream capture.  All calls share the one array: calls that
+ * overlap on the GPU (other streams, other host threads) race and must be serialised
+ * by the caller.  Nothing in the array needs to start at zero: each call writes
+ * every score it reads.
  * ------------------------------------------------------------------------------- */
 size_t csa2_indexer_noalloc_max_scratch_bytes(void);
 int csa2_indexer_score_topk_noalloc(const void* q_idx, const float* w, int B, int Tq,

@@ -297,3 +297,38 @@ int main(void) {
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stderr)
+
+
+def _noalloc_limit_entries(lib, B, blk=64):
+    """Largest decode row length (Tq = 1, Full) whose workspace fits the built-in array."""
+    cap = lib.csa2_indexer_noalloc_max_scratch_bytes()
+    ws = lambda n: lib.csa2_indexer_workspace_size(B, 1, n, 0, blk, 0)
+    lo, hi = 1, 1 << 26
+    assert ws(lo) <= cap < ws(hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if ws(mid) <= cap:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def test_noalloc_refuses_one_entry_past_its_limit(lib):
+    # The limit is the workspace size of the call, not a count of scores: one entry more
+    # than the largest accepted row length is refused on the host, before any launch.
+    f = lib.csa2_indexer_score_topk_noalloc
+    cap = lib.csa2_indexer_noalloc_max_scratch_bytes()
+    for B in (1, 4):
+        n = _noalloc_limit_entries(lib, B)
+        assert lib.csa2_indexer_workspace_size(B, 1, n, 0, 64, 0) <= cap
+        assert lib.csa2_indexer_workspace_size(B, 1, n + 1, 0, 64, 0) > cap
+        st = f(_vp(FAKE), _vp(FAKE), B, 1, n, _vp(FAKE), _vp(FAKE), n + 1, n + 1, 1, None, 0, 64,
+               512, _vp(FAKE), None, _vp(0))
+        assert st == L.ERR_UNSUPPORTED
+        assert str(cap).encode() in lib.csa2_last_error_message()
+    # a prefill call with short rows is counted with its FP4 query images (2176 B per row)
+    Tq = cap // 2176 + 1
+    st = f(_vp(FAKE), _vp(FAKE), 1, Tq, 0, _vp(FAKE), _vp(FAKE), 64, 64, 1, None, 0, 64, 16,
+           _vp(FAKE), None, _vp(0))
+    assert st == L.ERR_UNSUPPORTED

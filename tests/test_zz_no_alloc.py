@@ -83,3 +83,110 @@ def test_noalloc_pool_mode_and_size_limit(lib):
         _p(qi), _p(w), 1, 1, big - 1, _p(codes), _p(scales), big, big, 1, None, 0, blk, k,
         _p(got), None, stream)
     assert st == 2 and b"16777216" in lib.csa2_last_error_message()
+
+
+def test_noalloc_at_its_exact_limit(lib):
+    # The largest call the array admits (its workspace size equals the array's size
+    # exactly) runs and matches the workspace entry point.
+    from compressed_sparse_attention_04_gb300 import ops
+    B, k, blk = 4, 512, 64
+    cap = lib.csa2_indexer_noalloc_max_scratch_bytes()
+    n_entries = 826080
+    assert lib.csa2_indexer_workspace_size(B, 1, n_entries, 0, blk, 0) == cap
+    qi, w, codes, scales = _inputs(33, B, n_entries)
+    ref = ops.indexer_score_topk(qi, w, n_entries - 1, codes, scales, n_entries, 1, k, blk=blk)
+    got = torch.full((B, 1, k), -7, dtype=torch.int32, device="cuda")
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.csa2_indexer_score_topk_noalloc(
+        _p(qi), _p(w), B, 1, n_entries - 1, _p(codes), _p(scales), n_entries, n_entries, 1,
+        None, 0, blk, k, _p(got), None, stream)
+    assert st == 0, lib.csa2_last_error_message()
+    torch.cuda.synchronize()
+    assert ops.last_device_status() == 0
+    np.testing.assert_array_equal(got.cpu().numpy(), ref.cpu().numpy())
+
+
+_CONTEXT_SCRIPT = r'''
+import ctypes as C, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from compressed_sparse_attention_04_gb300 import _lib
+lib = _lib.load()
+cu = C.CDLL("libcuda.so.1")
+def ok(r, what):
+    assert r == 0, f"{what}: CUresult {r}"
+ok(cu.cuInit(0), "cuInit")
+dev = C.c_int()
+ok(cu.cuDeviceGet(C.byref(dev), 0), "cuDeviceGet")
+
+def alloc(nbytes):
+    p = C.c_uint64()
+    ok(cu.cuMemAlloc_v2(C.byref(p), C.c_size_t(nbytes)), "cuMemAlloc")
+    return p.value
+
+def upload(a):
+    a = np.ascontiguousarray(a)
+    p = alloc(a.nbytes)
+    ok(cu.cuMemcpyHtoD_v2(C.c_uint64(p), a.ctypes.data_as(C.c_void_p), C.c_size_t(a.nbytes)), "HtoD")
+    return p
+
+def download(p, shape, dtype):
+    a = np.empty(shape, dtype)
+    ok(cu.cuMemcpyDtoH_v2(a.ctypes.data_as(C.c_void_p), C.c_uint64(p), C.c_size_t(a.nbytes)), "DtoH")
+    return a
+
+def one_context_case(seed):
+    # inputs allocated in the current context; workspace entry point vs no-alloc, twice
+    B, n, k, blk = 2, 5000, 64, 64
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((B, 1, 32, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w = rng.standard_normal((B, 1, 32)).astype(np.float32)
+    codes = rng.integers(0, 256, (B, n, 64), dtype=np.uint8)
+    scales = rng.integers(0x18, 0x58, (B, n, 4), dtype=np.uint8)
+    dq, dw, dc, ds = upload(q), upload(w), upload(codes), upload(scales)
+    ws_bytes = lib.csa2_indexer_workspace_size(B, 1, n, 0, blk, 0)
+    ws = alloc(ws_bytes + 256)
+    ref_p, got_p = alloc(B * k * 4), alloc(B * k * 4)
+    vp = C.c_void_p
+    st = lib.csa2_indexer_score_topk(vp(dq), vp(dw), B, 1, n - 1, vp(dc), vp(ds), n, n, 1, None, 0,
+                                     blk, k, vp(ref_p), None, None, vp(ws), ws_bytes + 256, None)
+    assert st == 0, lib.csa2_last_error_message()
+    ref = None
+    for call in range(2):
+        ok(cu.cuMemsetD8_v2(C.c_uint64(got_p), C.c_ubyte(0xA5), C.c_size_t(B * k * 4)), "memset")
+        st = lib.csa2_indexer_score_topk_noalloc(vp(dq), vp(dw), B, 1, n - 1, vp(dc), vp(ds), n, n,
+                                                 1, None, 0, blk, k, vp(got_p), None, None)
+        assert st == 0, lib.csa2_last_error_message()
+        assert lib.csa2_last_device_status(None) == 0
+        ref = download(ref_p, (B, k), np.int32)
+        got = download(got_p, (B, k), np.int32)
+        assert (got == ref).all(), f"call {call}"
+    assert (ref >= 0).all()
+    for p in (dq, dw, dc, ds, ws, ref_p, got_p):
+        ok(cu.cuMemFree_v2(C.c_uint64(p)), "cuMemFree")
+
+# first the device's primary context, then a second context made current through the
+# driver API: the array has another address there, which the entry point must look up
+prim = C.c_void_p()
+ok(cu.cuDevicePrimaryCtxRetain(C.byref(prim), dev), "cuDevicePrimaryCtxRetain")
+ok(cu.cuCtxSetCurrent(prim), "cuCtxSetCurrent")
+one_context_case(1)
+ctx2 = C.c_void_p()
+ok(cu.cuCtxCreate_v2(C.byref(ctx2), 0, dev), "cuCtxCreate")
+one_context_case(2)
+ok(cu.cuCtxDestroy_v2(ctx2), "cuCtxDestroy")
+ok(cu.cuCtxSetCurrent(prim), "cuCtxSetCurrent")
+one_context_case(3)
+print("contexts ok")
+'''
+
+
+def test_noalloc_in_a_second_cuda_context(lib):
+    # A caller that makes its own context current through the driver API gets that
+    # context's copy of the array, not the one the primary context saw first.
+    import subprocess
+    import sys
+    from conftest import ROOT
+    r = subprocess.run([sys.executable, "-c", _CONTEXT_SCRIPT, ROOT], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and "contexts ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
