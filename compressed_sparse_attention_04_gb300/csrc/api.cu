@@ -22,6 +22,17 @@ RopeTurns rope_turns(float rope_base) {
   }
   return t;
 }
+EncodeTiledFn tensor_map_encoder() {   // thread-safe static initialisation
+  static const EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return EncodeTiledFn(nullptr);
+  }();
+  return fn;
+}
 bool pdl_enabled() {
   static const bool on = [] {
     const char* v = std::getenv("CSA2_NO_PDL");

@@ -8,15 +8,16 @@
 // [P3] "DeepSeek-V4.1-Flash：把百万 Token 的记忆，压缩成一套分级缓存" (junki.cn), §四:
 //      p_j = softmax_j(c_j . q / sqrt d), o = sum_j p_j c_j.
 //
-// attn_flash_kernel (64 heads): a cluster of 1-4 CTAs per query row shares the row's
-// attended list (each CTA an equal part of the window rows and of the top-k slots); each CTA
-// streams its rows in chunks of 48 through a three-slot ring (16-byte asynchronous gathers
-// into a K-major 128-byte-swizzled tile), tcgen05
-// computes S = Q C^T (64 heads x 48 rows, K = 512) so that one thread owns one head's
-// scores, an online softmax writes P (bf16, a head per row), and tcgen05 accumulates O^T = C^T P^T
-// (512 dims x 64 heads) in TMEM, reading the SAME shared tile as the MN-major operand
-// (K = V).  The CTAs of a cluster combine their (max, sum, O) through distributed shared
-// memory; nothing intermediate goes to global memory.
+// attn_decode_kernel (64 heads): a cluster of 1-4 CTAs per query row shares the row's
+// attended list (each CTA an equal part of the window rows and of the top-k slots).  The
+// queries and the bf16 window rows arrive by TMA tile loads; the selected entries are
+// gathered by 16-byte asynchronous copies into a two-slot ring of 64-row chunks (K-major,
+// 128-byte swizzle).  tcgen05 computes S = Q C^T (64 heads x 64 rows, K = 512) so that one
+// thread owns one head's scores, an online softmax writes P (bf16, a head per row), and
+// tcgen05 accumulates O^T = C^T P^T (512 dims x 64 heads) in TMEM, reading the SAME shared
+// tile as the MN-major operand (K = V).  The CTAs of a cluster combine their (max, sum)
+// through distributed shared memory and send each other's O^T tiles by bulk copies between
+// their shared memories; nothing intermediate goes to global memory.
 // Its second instantiation serves stored formats ([P3] §六, §七): FP4 entries (E2M1 with one
 // E4M3 scale per 16 channels) and / or FP8 window rows (E4M3 with one power-of-two scale per
 // 64 channels) are loaded into registers as 16-byte pieces before the ring slot is free and
@@ -189,41 +190,56 @@ __global__ void __launch_bounds__(AT_T) attn_simt_kernel(AttnArgs a) {
 
 // ---------------------------------------------------------------- pipelined tensor-core
 // attention (64 heads).  The CTAs of one cluster share a row's attended list: CTA r takes
-// its part of the window rows followed by its part of the top-k slots (window rows first:
-// the first chunk's copies need no top-k index), cut into chunks of 48 rows, and the CTAs
-// merge their partial results through distributed shared memory.  Per chunk:
-//   S   = Q C^T     (M = 64 heads, N = 48 rows, K = 512)   -> TMEM, one head per lane,
-//                    so each head's softmax runs inside one thread;
-//   O^T += C^T P^T  (M = 4 x 128 dims, N = 64 heads, K = 48 rows) -> TMEM,
+// its part of the window rows, then its part of the top-k slots, in chunks of 64 rows.
+// Shared memory holds the 64 queries (64 KB) and two 64-row chunk slots (64 KB each); a
+// slot is eight 8 KB planes, plane j holding dims 64 j .. 64 j + 63 of the slot's rows in
+// 8-row atoms of 1 KB (K-major, 128-byte swizzle); the queries use the same layout.
+// Where the rows come from:
+//   queries and bf16 window rows: TMA tile loads (one 64-row x 64-dim box per plane),
+//     issued at the start for the first two chunks by the MMA warp;
+//   top-k entries (and later window chunks): 16-byte cp.async gathers by two copy groups
+//     of 64 threads, group g owning slot g; thread t copies 16-byte piece t of every row;
+//   FP4 entries / FP8 window rows: the same groups load the quantised pieces into
+//     registers before the slot is free and dequantise them exactly into the tile.
+// Per chunk:
+//   S   = Q C^T     (M = 64 heads, N = 64 rows, K = 512)   -> TMEM, one head per lane,
+//                    so each head's softmax runs inside one thread (two lanes split its rows);
+//   O^T += C^T P^T  (M = 4 x 128 dims, N = 64 heads, K = 64 rows) -> TMEM,
 // reading the SAME shared tile of C (K = V) as a K-major and an MN-major operand.
-// The running maximum is only moved when a chunk exceeds it by more than 2^8 (probabilities
-// then stay below 256, exact in float32 sums); moving it rescales that head's columns of
-// O^T in TMEM after the previous chunk's products have landed.
-constexpr int AF_CH = 48;                              // rows per chunk
-constexpr int AF_SLOTS = 3;                            // KV ring depth (chunks)
-constexpr int AF_T = 288;                              // 4 copy + 4 softmax + 1 MMA warp
-constexpr uint32_t AF_KV_BYTES = AF_CH * 1024;         // 48 KB per ring slot
-constexpr uint32_t AF_ATOM = AF_CH * 128;              // one 64-dim atom column of a slot
-constexpr uint32_t AF_Q_BYTES = 64 * 1024;
-// P: 64 heads x 48 rows, K-major without swizzle: 8-head x 8-row core matrices of 128 B,
-// K (rows) direction 128 B apart, 8-head groups AF_P_SBO apart
-constexpr uint32_t AF_P_SBO = (AF_CH / 8) * 128;
-constexpr uint32_t AF_P_BYTES = 8 * AF_P_SBO;          // 6 KB per P buffer
-constexpr uint32_t AF_SMEM = AF_SLOTS * AF_KV_BYTES + AF_Q_BYTES + 2 * AF_P_BYTES + 1024;
-// Quantised rows (FP4 entries, FP8 window rows) are loaded into registers as 16-byte pieces,
-// at most AF_PC per copy thread and round (one round per chunk of FP4 entries, two for a
-// chunk of FP8 window rows), then dequantised into the tile.
-constexpr int AF_PC = 12;
-constexpr int AF_HALF = AF_CH / 2;                     // rows per lane (two lanes per head)
-// S: 2 buffers x 2 K-halves x 64 columns (the two halves are independent accumulators so
-// that consecutive MMAs do not wait on each other); O^T: 4 x 64 columns
-constexpr uint32_t AF_S_COL = 0, AF_O_COL = 256;
-constexpr float AF_LAZY = 8.f;                         // log2 slack before the max moves
-constexpr int AF_MAX_SPLIT = 4;
+// The running maximum is only moved when a chunk exceeds it by more than 2^4 (probabilities
+// then stay below 16; a larger slack costs accuracy where one row dominates, since the
+// dominant probability is then rounded to bf16 instead of being exactly 1); moving it
+// rescales that head's columns of O^T in TMEM after the previous chunk's products have
+// landed.  The softmax sum adds the bf16-rounded probabilities the products use.
+// Merge: the CTAs exchange their (max, sum) per head through distributed shared memory;
+// each scales the O^T tiles that another CTA owns into its own shared memory and sends
+// each to its owner with one bulk copy; the owner adds them to its own tiles.
+constexpr int AD_CH = 64;                              // rows per chunk
+constexpr int AD_SLOTS = 2;                            // chunk slots (one per copy group)
+constexpr int AD_T = 288;                              // 4 copy + 4 softmax + 1 MMA warp
+constexpr uint32_t AD_PLANE = AD_CH * 128;             // 64 rows x 64 dims: 8 KB
+constexpr uint32_t AD_SLOT_BYTES = 8 * AD_PLANE;       // 64 KB per slot
+constexpr uint32_t AD_Q_BYTES = 64 * 1024;             // 64 heads, same plane layout
+// P: 64 heads x 64 rows, K-major without swizzle: 8-head x 8-row core matrices of 128 B,
+// K (rows) direction 128 B apart, 8-head groups AD_P_SBO apart
+constexpr uint32_t AD_P_SBO = (AD_CH / 8) * 128;
+constexpr uint32_t AD_P_BYTES = 8 * AD_P_SBO;          // 8 KB per P buffer
+constexpr uint32_t AD_SMEM = AD_SLOTS * AD_SLOT_BYTES + AD_Q_BYTES + 2 * AD_P_BYTES + 1024;
+constexpr uint32_t AD_TILE_BYTES = 64 * 128 * 4;       // one O^T tile: 64 heads x 128 dims f32
+// Quantised rows are loaded as 16-byte pieces, AD_PC per copy thread and round: one round
+// per chunk of FP4 entries (16 pieces a row), two for a chunk of FP8 window rows (32).
+constexpr int AD_PC = 16;
+constexpr int AD_HALF = AD_CH / 2;                     // rows per lane (two lanes per head)
+constexpr uint32_t AD_S_COL = 0, AD_O_COL = 256;       // S: 2 x 64 columns; O^T: 4 x 64
+constexpr float AD_LAZY = 4.f;                         // log2 slack before the max moves
+constexpr int AD_MAX_SPLIT = 4;
+// named barriers (0 is __syncthreads): copy threads 1, copy groups 2 and 3, softmax 4
+constexpr int BAR_COPY = 1, BAR_GROUP = 2, BAR_SOFTMAX = 4;
 
-struct AttnFlashArgs {
+struct AttnDecodeArgs {
   AttnArgs a;
   int n_split;        // CTAs per row (cluster size)
+  int win_tma;        // bf16 window rows through the tensor map
 };
 
 // Shared-memory descriptor without swizzle: 8-row x 16-byte core matrices, LBO = stride
@@ -235,6 +251,12 @@ __device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr, uint32_t lbo, uin
   d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
   d |= uint64_t(1) << 46;
   return d;
+}
+// Byte offset of channels ch .. ch + 7 (ch a multiple of 8) of row r inside a slot (or the
+// query block): plane ch / 64, 8-row atom r / 8, 16-byte chunk swizzled by r % 8.
+__device__ __forceinline__ uint32_t plane_off(int r, int ch) {
+  return uint32_t((ch >> 6) * AD_PLANE + (r >> 3) * 1024 + (r & 7) * 128 +
+                  ((((ch & 63) >> 3) ^ (r & 7)) << 4));
 }
 // 2^x by the MUFU approximation (relative error about 2^-22; the probabilities are rounded
 // to bf16 for the products, and the sums use the same values).
@@ -303,10 +325,6 @@ __device__ __forceinline__ uint4 fp4_piece_bf16(uint32_t codes, uint32_t scale_b
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
-// Bring `bytes` (a multiple of 16) at p into L2 without waiting for them.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
-}
 
 // Named barrier over n threads that also reduces a predicate (and / or) across them.
 __device__ __forceinline__ bool bar_and(int id, int n, bool v) {
@@ -324,51 +342,86 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool v) {
   return r != 0;
 }
 
-// Marks a quantised row among the bf16 row sources.
-#define kQuantRow (reinterpret_cast<const uint16_t*>(uintptr_t(16)))
+// ---- TMA tile loads, bulk shared-memory copies between the CTAs of a cluster
+__device__ __forceinline__ void mbar_expect_tx(void* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(umma::smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, void* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];"
+      :: "r"(umma::smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(umma::smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            void* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(umma::smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(z), "r"(umma::smem_u32(bar))
+      : "memory");
+}
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(const void* p, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(umma::smem_u32(p)), "r"(rank));
+  return r;
+}
+// `bytes` from this CTA's shared memory to another CTA's, completing on its mbarrier.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, const void* src, uint32_t bytes,
+                                             uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst_cluster), "r"(umma::smem_u32(src)), "r"(bytes), "r"(bar_cluster) : "memory");
+}
+// O^T tiles (4 of 128 dims) owned by CTA r of n: dt = r, r + n, ...
+__device__ __forceinline__ int tiles_owned(int r, int n) { return (4 - r + n - 1) / n; }
 
 template <bool QNT>   // QNT: FP4 entries and / or FP8 window rows
-__global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
-  constexpr int NS = AF_SLOTS;
+__global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
+                                                              const __grid_constant__ CUtensorMap q_map,
+                                                              const __grid_constant__ CUtensorMap swa_map) {
   pdl_wait();
   namespace cg = cooperative_groups;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* KV = base;                                   // NS x 48 rows (K-major SW128)
-  uint8_t* Qs = base + NS * AF_KV_BYTES;                // 64 heads (K-major SW128)
-  uint8_t* Ps = Qs + AF_Q_BYTES;                        // 2 x P (64 heads x 64 rows, K-major)
-  // after the last chunk: partial O^T tiles pushed by the cluster's CTAs to the tile's owner,
-  // [slot = source rank][owned tile][head][dim] (KV ring and Q, 192 KB)
-  float* Obuf = reinterpret_cast<float*>(KV);
-  __shared__ const uint16_t* row_src[NS][AF_CH];   // bf16 row sources (NULL: none)
-  __shared__ int row_e[2][AF_CH];                  // (QNT) per copy group: quantised rows, -1 none
-  __shared__ unsigned long long row_mask[NS];
-  __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
-  __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready;
+  uint8_t* KV = base;                                   // 2 slots x 64 rows
+  uint8_t* Qs = base + AD_SLOTS * AD_SLOT_BYTES;        // 64 heads
+  uint8_t* Ps = Qs + AD_Q_BYTES;                        // 2 x P (64 heads x 64 rows)
+  // after the last chunk the slots and the queries (192 KB) hold the merge tiles: first the
+  // tiles this CTA sends, then the ones it receives, [source][owned tile][head][dim]
+  uint8_t* Mg = base;
+  __shared__ int sidx[CSA2_MAX_TOPK];                   // this CTA's top-k slots
+  __shared__ const uint16_t* row_src[AD_SLOTS][AD_CH];  // bf16 row sources (NULL: none)
+  __shared__ int row_q[AD_SLOTS][AD_CH];                // (QNT) quantised rows, -1 none
+  __shared__ unsigned long long row_mask[AD_SLOTS];
+  __shared__ __align__(8) uint64_t kv_full[AD_SLOTS], kv_empty[AD_SLOTS];
+  __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready, q_full, recv_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ float fac[64];                              // per-head factor (rescale / final)
-  __shared__ __align__(8) float ml_all[AF_MAX_SPLIT][64][2];   // every CTA's (max, sum), log2 units
+  // every CTA's (max, sum of the bf16-rounded probabilities, exact sum) per head, log2 units
+  __shared__ __align__(16) float ml_all[AD_MAX_SPLIT][64][4];
 
   const AttnArgs& a = u.a;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = int(cluster.block_rank());
+  const int ns = u.n_split;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = blockIdx.x / u.n_split;
+  const int row = blockIdx.x / ns;
   const int b = row / a.Tq, i = row % a.Tq;
   const long long t = (long long)a.q_pos0 + i;
   const long long lo = t - a.window + 1 > 0 ? t - a.window + 1 : 0;
-  // this CTA's rows: window rows w0 .. w1 - 1, then top-k slots k0 .. k1 - 1 (the window
-  // first, so that the first chunk's copies need no top-k index)
+  // this CTA's rows: window rows w0 .. w0 + nw - 1, then top-k slots k0 .. k0 + nk - 1
   const int n_win = int(t - lo + 1);
-  const int w0 = int((long long)n_win * rank / u.n_split), nw = int((long long)n_win * (rank + 1) / u.n_split) - w0;
-  const int k0 = int((long long)a.k * rank / u.n_split), nk_mine = int((long long)a.k * (rank + 1) / u.n_split) - k0;
-  const int n_mine = nw + nk_mine;
-  const int n_ch = (n_mine + AF_CH - 1) / AF_CH;
+  const int w0 = int((long long)n_win * rank / ns), nw = int((long long)n_win * (rank + 1) / ns) - w0;
+  const int k0 = int((long long)a.k * rank / ns), nk = int((long long)a.k * (rank + 1) / ns) - k0;
+  const int n_wch = (nw + AD_CH - 1) / AD_CH, n_ch = n_wch + (nk + AD_CH - 1) / AD_CH;
+  const int n_tma = u.win_tma ? min(n_wch, AD_SLOTS) : 0;   // window chunks loaded by the TMA
   const float scale_log2 = a.scale * 1.4426950408889634f;
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      umma::mbar_init(&kv_full[s], 64);   // the 64 threads of the group that fills it
+    for (int s = 0; s < AD_SLOTS; ++s) {
+      umma::mbar_init(&kv_full[s], 1);    // the TMA issuer's or a copy group's elected arrive
       umma::mbar_init(&kv_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -377,6 +430,8 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       umma::mbar_init(&p_full[s], 4);
     }
     umma::mbar_init(&o_ready, 1);
+    umma::mbar_init(&q_full, 1);
+    umma::mbar_init(&recv_bar, 1);
     umma::mbar_fence_init();
   }
   if (warp == 0) umma::tmem_alloc(&tmem_slot, 512);
@@ -385,40 +440,38 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
   bool ok = true;
-  float m_fin = -INFINITY, l_fin = 0.f;   // softmax lanes: this CTA's (max, sum) of their head
+  // softmax lanes: this CTA's (max, rounded sum, exact sum) of their head
+  float m_fin = -INFINITY, l_fin = 0.f, e_fin = 0.f;
   // announce that this CTA runs; the matching wait precedes the first remote access
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   if (warp < 4) {
-    // ---------------- copy warps, two groups of two warps: group g fills chunks g, g + 2,
-    // g + 4, ... (slot c % 3; group 0 also the queries with chunk 0), waits for its own copies
-    // and announces the chunk, so one group waiting for a free slot never holds back the
-    // other's announcement.  Thread t < 48 of a group holds the selected entry of row t of
-    // the group's next chunk, loaded one chunk ahead.
+    // ---------------- copy warps.  Group g (warps 2g, 2g + 1) fills the chunks of slot g
+    // that the TMA does not: it waits for the slot, gathers the chunk (thread gt copies
+    // piece gt of each of its 64 rows), waits for its own copies and announces the chunk.
+    for (int j = tid; j < nk; j += 128) sidx[j] = a.topk[size_t(row) * a.k + k0 + j];
+    named_bar(BAR_COPY, 128);
     const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
     const bool fp4 = QNT && a.kv_codes != nullptr, fp8w = QNT && a.swa_codes != nullptr;
-    auto topk_at = [&](int c) -> int {
-      const int j = c * AF_CH + gt;
-      return (gt < AF_CH && c < n_ch && j >= nw && j < n_mine) ? a.topk[size_t(row) * a.k + k0 + (j - nw)] : -1;
-    };
-    int e_next = topk_at(grp);
-    for (int c = grp; c < n_ch && ok; c += 2) {
-      const int s = c % AF_SLOTS;
-      const int e = e_next;
-      e_next = topk_at(c + 2);
-      // row gt of the chunk: a bf16 source, or the row of a quantised one (qrow), or none
-      const int j = c * AF_CH + gt;
-      int okr = 0;
+    uint8_t* dst = KV + grp * AD_SLOT_BYTES;
+    for (int c = grp; c < n_ch && ok; c += AD_SLOTS) {
+      if (c < n_tma) continue;
+      const int s = grp;
+      const bool win = c < n_wch;
+      const bool qchunk = QNT && (win ? fp8w : fp4);
+      // row gt of the chunk: a bf16 source, a quantised row, or none (zero-filled)
+      const int j = win ? c * AD_CH + gt : (c - n_wch) * AD_CH + gt;
+      int okr = 0, qrow = -1;
       const uint16_t* src = nullptr;
-      int qrow = -1;
-      if (gt >= AF_CH) {
-        // (lanes past the chunk only complete the ballot)
-      } else if (j < nw) {
-        okr = 1;
-        const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
-        if (fp8w) qrow = int(wr);
-        else src = a.swa + wr * 512;
-      } else if (j < n_mine) {
+      if (win) {
+        if (j < nw) {
+          okr = 1;
+          const size_t wr = size_t(b) * a.S + size_t(lo + w0 + j - a.swa_pos0);
+          if (fp8w) qrow = int(wr);
+          else src = a.swa + wr * 512;
+        }
+      } else if (j < nk) {
+        const int e = sidx[j];
         if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
         if (e >= 0 && e < a.n_entries) {
           okr = 1;
@@ -426,187 +479,133 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
           else src = a.kv + (size_t(b) * a.n_cap + e) * 512;
         }
       }
-      const int r_w = max(0, min(AF_CH, nw - c * AF_CH));   // the chunk's window rows come first
-      // (QNT) the chunk's quantised rows as 16-byte pieces, 32 per FP8 window row and 16 per
-      // FP4 entry, window rows first; piece idx of the chunk goes to thread idx % 64, at most
-      // AF_PC per thread and round, held in registers from before the slot is free
-      const int pw = fp8w ? 32 : 0, pm = fp4 ? 16 : 0;
-      const int n_pc = r_w * pw + (AF_CH - r_w) * pm;
-      uint4 pc[AF_PC];
-      uint32_t psc[AF_PC];
-      auto piece_at = [&](int idx, int& r, int& p) {
-        if (idx < r_w * pw) {
-          r = idx >> 5;
-          p = idx & 31;
-        } else {
-          const int i2 = idx - r_w * pw;
-          r = r_w + (i2 >> 4);
-          p = i2 & 15;
-        }
-      };
-      auto load_round = [&](int base) {   // codes and the scales they need, all in flight
+      // (QNT) the chunk's quantised rows as 16-byte pieces: piece idx of the chunk (row
+      // idx / ppr) goes to thread idx % 64, AD_PC per thread and round, held in registers
+      // from before the slot is free
+      const int ppr = win ? 32 : 16;
+      uint4 pc[AD_PC];
+      uint32_t psc[AD_PC];
+      auto load_round = [&](int base_idx) {
 #pragma unroll
-        for (int i = 0; i < AF_PC; ++i) {
-          const int idx = base + gt + 64 * i;
-          if (idx >= n_pc) break;
-          int r, p;
-          piece_at(idx, r, p);
-          const int qr = row_e[grp][r];
+        for (int x = 0; x < AD_PC; ++x) {
+          const int idx = base_idx + gt + 64 * x;
+          const int r = idx / ppr, p = idx % ppr;
+          const int qr = row_q[s][r];
           if (qr < 0) continue;
-          if (r < r_w) {
-            pc[i] = ld_v4_early(a.swa_codes + size_t(qr) * 512 + 16 * p);
-            psc[i] = ld_u8_early(a.swa_scales + size_t(qr) * 8 + (p >> 2));
+          if (win) {
+            pc[x] = ld_v4_early(a.swa_codes + size_t(qr) * 512 + 16 * p);
+            psc[x] = ld_u8_early(a.swa_scales + size_t(qr) * 8 + (p >> 2));
           } else {
-            pc[i] = ld_v4_early(a.kv_codes + size_t(qr) * 256 + 16 * p);
-            psc[i] = ld_u16_early(a.kv_scales + size_t(qr) * 32 + 2 * p);
+            pc[x] = ld_v4_early(a.kv_codes + size_t(qr) * 256 + 16 * p);
+            psc[x] = ld_u16_early(a.kv_scales + size_t(qr) * 32 + 2 * p);
           }
         }
       };
-      uint8_t* dst = KV + s * AF_KV_BYTES;
-      auto store_round = [&](int base) {  // dequantised into the tile (exact in bf16)
+      auto store_round = [&](int base_idx) {   // dequantised into the tile (exact in bf16)
 #pragma unroll
-        for (int i = 0; i < AF_PC; ++i) {
-          const int idx = base + gt + 64 * i;
-          if (idx >= n_pc) break;
-          int r, p;
-          piece_at(idx, r, p);
-          if (row_e[grp][r] < 0) continue;
-          if (r < r_w) {   // channels 16 p .. 16 p + 15, scale group p / 4
-            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 16 * p, AF_CH)) =
-                fp8_piece_bf16(make_uint2(pc[i].x, pc[i].y), psc[i]);
-            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 16 * p + 8, AF_CH)) =
-                fp8_piece_bf16(make_uint2(pc[i].z, pc[i].w), psc[i]);
-          } else {         // channels 32 p .. 32 p + 31, scale groups 2 p and 2 p + 1
-            const uint32_t s0 = psc[i] & 0xFFu, s1 = (psc[i] >> 8) & 0xFFu;
-            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p, AF_CH)) = fp4_piece_bf16(pc[i].x, s0);
-            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p + 8, AF_CH)) = fp4_piece_bf16(pc[i].y, s0);
-            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p + 16, AF_CH)) = fp4_piece_bf16(pc[i].z, s1);
-            *reinterpret_cast<uint4*>(dst + umma::kmajor_sw128_offset(r, 32 * p + 24, AF_CH)) = fp4_piece_bf16(pc[i].w, s1);
+        for (int x = 0; x < AD_PC; ++x) {
+          const int idx = base_idx + gt + 64 * x;
+          const int r = idx / ppr, p = idx % ppr;
+          const bool have = row_q[s][r] >= 0;
+          if (win) {   // channels 16 p .. 16 p + 15, scale group p / 4
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dst + plane_off(r, 16 * p)) =
+                have ? fp8_piece_bf16(make_uint2(pc[x].x, pc[x].y), psc[x]) : z;
+            *reinterpret_cast<uint4*>(dst + plane_off(r, 16 * p + 8)) =
+                have ? fp8_piece_bf16(make_uint2(pc[x].z, pc[x].w), psc[x]) : z;
+          } else {     // channels 32 p .. 32 p + 31, scale groups 2 p and 2 p + 1
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            const uint32_t s0 = psc[x] & 0xFFu, s1 = (psc[x] >> 8) & 0xFFu;
+            *reinterpret_cast<uint4*>(dst + plane_off(r, 32 * p)) = have ? fp4_piece_bf16(pc[x].x, s0) : z;
+            *reinterpret_cast<uint4*>(dst + plane_off(r, 32 * p + 8)) = have ? fp4_piece_bf16(pc[x].y, s0) : z;
+            *reinterpret_cast<uint4*>(dst + plane_off(r, 32 * p + 16)) = have ? fp4_piece_bf16(pc[x].z, s1) : z;
+            *reinterpret_cast<uint4*>(dst + plane_off(r, 32 * p + 24)) = have ? fp4_piece_bf16(pc[x].w, s1) : z;
           }
         }
       };
-      if constexpr (QNT) {
-        named_bar(2 + grp, 64);   // the group's previous chunk no longer reads row_e[grp]
-        if (gt < AF_CH) row_e[grp][gt] = qrow;
-        named_bar(2 + grp, 64);
+      if (qchunk) {
+        row_q[s][gt] = qrow;
+        named_bar(BAR_GROUP + grp, 64);
         load_round(0);
       }
-      bool okw = c < AF_SLOTS || umma::mbar_wait(&kv_empty[s], ((c / AF_SLOTS) - 1) & 1, &d_err_attn);
-      {   // row sources (both warps of the group, whole warps for the ballot)
+      const bool okw = c < AD_SLOTS || umma::mbar_wait(&kv_empty[s], ((c / AD_SLOTS) - 1) & 1, &d_err_attn);
+      {   // row sources and the chunk's row mask (whole warps for the ballot)
         const unsigned m0 = __ballot_sync(0xffffffffu, okr);
         if (okw) {
-          if (gt < AF_CH) row_src[s][gt] = qrow >= 0 ? kQuantRow : src;
+          row_src[s][gt] = src;
           if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[gw] = m0;
         }
       }
       // row sources ready; the group agrees on whether the slot wait succeeded
-      if (!bar_and(2 + grp, 64, okw)) { ok = false; break; }
-      // bf16 rows: 48 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are
-      // read eight at a time before their copies (an asynchronous copy orders the loads after
-      // it); a row with no source is zero-filled, a quantised row is written below
-#pragma unroll 1
-      for (int r0 = 0; r0 < AF_CH; r0 += 8) {
-        const uint16_t* sp[8];
-#pragma unroll
-        for (int u2 = 0; u2 < 8; ++u2) sp[u2] = row_src[s][r0 + u2];
-#pragma unroll
-        for (int u2 = 0; u2 < 8; ++u2) {
-          if (QNT && sp[u2] == kQuantRow) continue;
-          umma::cp_async16(dst + umma::kmajor_sw128_offset(r0 + u2, gt * 8, AF_CH),
-                           sp[u2] ? sp[u2] + gt * 8 : a.q, sp[u2] ? 16u : 0u);
-        }
-      }
-      if constexpr (QNT) {
+      if (!bar_and(BAR_GROUP + grp, 64, okw)) { ok = false; break; }
+      if (qchunk) {
         store_round(0);
-        for (int base = 64 * AF_PC; base < n_pc; base += 64 * AF_PC) {   // (FP8 window chunks)
-          load_round(base);
-          store_round(base);
+        for (int base_idx = 64 * AD_PC; base_idx < AD_CH * ppr; base_idx += 64 * AD_PC) {   // (FP8)
+          load_round(base_idx);
+          store_round(base_idx);
         }
-      }
-      {   // while this chunk is in flight: the rows of the group's next chunk into L2
-        const int jn = (c + 2) * AF_CH + gt;
-        if (gt < AF_CH && c + 2 < n_ch && jn < n_mine) {
-          if (jn < nw) {
-            const size_t wr = size_t(b) * a.S + size_t(lo + w0 + jn - a.swa_pos0);
-            if (fp8w) prefetch_l2(a.swa_codes + wr * 512, 512);   // (8 scale bytes: too short)
-            else prefetch_l2(a.swa + wr * 512, 1024);
-          } else if (e_next >= 0 && e_next < a.n_entries) {
-            const size_t er = size_t(b) * a.n_cap + e_next;
-            if (fp4) {
-              prefetch_l2(a.kv_codes + er * 256, 256);
-              prefetch_l2(a.kv_scales + er * 32, 32);
-            } else {
-              prefetch_l2(a.kv + er * 512, 1024);
-            }
-          }
+      } else {
+        // bf16 rows: 64 rows x 64 pieces of 16 bytes, piece gt of row r; the row sources are
+        // read eight at a time before their copies; a row with no source is zero-filled
+#pragma unroll 1
+        for (int r0 = 0; r0 < AD_CH; r0 += 8) {
+          const uint16_t* sp[8];
+#pragma unroll
+          for (int u2 = 0; u2 < 8; ++u2) sp[u2] = row_src[s][r0 + u2];
+#pragma unroll
+          for (int u2 = 0; u2 < 8; ++u2)
+            umma::cp_async16(dst + plane_off(r0 + u2, gt * 8), sp[u2] ? sp[u2] + gt * 8 : a.q,
+                             sp[u2] ? 16u : 0u);
         }
+        umma::cp_async_commit();
+        umma::cp_async_wait_all();        // this thread's copies of chunk c landed
       }
-      if (c <= 1) {
-        // the queries come with the first chunk of each group: heads 0..31 with chunk 0,
-        // heads 32..63 with chunk 1 (all 64 with chunk 0 when there is no chunk 1)
-        const uint16_t* qrow_p = a.q + size_t(row) * 64 * 512;
-        const int h0 = c == 0 ? 0 : 32, nh = (c == 0 && n_ch > 1) ? 32 : 64 - h0;
-#pragma unroll 4
-        for (int rep = 0; rep < nh; ++rep) {
-          const int uidx = rep * 64 + gt, h = h0 + (uidx >> 6), ch = uidx & 63;
-          umma::cp_async16(Qs + umma::kmajor_sw128_offset(h, ch * 8, 64), qrow_p + h * 512 + ch * 8, 16u);
-        }
-      }
-      umma::cp_async_commit();
-      umma::cp_async_wait_all();        // this thread's copies of chunk c landed
       umma::fence_proxy_async();
-      umma::mbar_arrive(&kv_full[s]);
+      named_bar(BAR_GROUP + grp, 64);     // every thread's part of the chunk is in place
+      if (gt == 0) umma::mbar_arrive(&kv_full[s]);
     }
   } else if (warp < 8) {
     // ---------------- softmax warps: warp q holds heads 16 q .. 16 q + 15 in TMEM lanes
-    // 0..15; lane l < 16 then takes rows 0..23 of head 16 q + l and lane l + 16 rows 24..47
+    // 0..15; lane l < 16 then takes rows 0..31 of head 16 q + l and lane l + 16 rows 32..63
     // (handed over by shuffles), so the whole warp shares the work.
     const int q = warp & 3, h = 16 * q + (lane & 15);
     const bool head_lane = lane < 16;
     const int half = lane >> 4;
     const uint32_t lane_addr = uint32_t(32 * q) << 16;
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f, le = 0.f;   // sums of the rounded / exact probabilities
     for (int c = 0; c < n_ch && ok; ++c) {
       const int s = c & 1;
-      bool okc = __all_sync(0xffffffffu, umma::mbar_wait(&s_full[s], (c >> 1) & 1, &d_err_attn));
-      if (!bar_and(1, 128, okc)) { ok = false; break; }
+      const bool okc = __all_sync(0xffffffffu, umma::mbar_wait(&s_full[s], (c >> 1) & 1, &d_err_attn));
+      if (!bar_and(BAR_SOFTMAX, 128, okc)) { ok = false; break; }
       umma::fence_after();
-      float sv[AF_HALF];   // this lane's 24 rows of its head (log2 units, masked)
+      float sv[AD_HALF];   // this lane's 32 rows of its head (log2 units, masked)
       {
-        uint32_t v0[32], v1[32], w0[32], w1[32];   // K halves, columns 0..31 | 32..63
-        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s, v0);
-        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 32, v1);
-        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 64, w0);
-        umma::tmem_ld32(tmem + lane_addr + AF_S_COL + 128 * s + 96, w1);
+        uint32_t v0[32], v1[32];   // rows 0..31 | 32..63 of the lane's head (lanes < 16)
+        umma::tmem_ld32(tmem + lane_addr + AD_S_COL + 64 * s, v0);
+        umma::tmem_ld32(tmem + lane_addr + AD_S_COL + 64 * s + 32, v1);
         umma::tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < AF_HALF; ++j) {
-          const float lo_rows = __uint_as_float(v0[j]) + __uint_as_float(w0[j]);
-          const int jh = AF_HALF + j;   // row of the upper half (24..47)
-          const float hi_rows = jh < 32 ? __uint_as_float(v0[jh < 32 ? jh : 0]) + __uint_as_float(w0[jh < 32 ? jh : 0])
-                                        : __uint_as_float(v1[jh >= 32 ? jh - 32 : 0]) +
-                                              __uint_as_float(w1[jh >= 32 ? jh - 32 : 0]);
-          const float moved = __shfl_sync(0xffffffffu, hi_rows, lane & 15);
-          sv[j] = half ? moved : lo_rows;
+        for (int j = 0; j < AD_HALF; ++j) {
+          const float moved = __shfl_sync(0xffffffffu, __uint_as_float(v1[j]), lane & 15);
+          sv[j] = half ? moved : __uint_as_float(v0[j]);
         }
       }
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&s_empty[s]);
-      constexpr unsigned half_bits = (1u << AF_HALF) - 1u;
-      const unsigned mask = unsigned(row_mask[c % NS] >> (half * AF_HALF)) & half_bits;
+      const unsigned mask = unsigned(row_mask[s] >> (half * AD_HALF));
       float cmx[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) cmx[u] = -INFINITY;
-      if (mask == half_bits) {
+      for (int x = 0; x < 8; ++x) cmx[x] = -INFINITY;
+      if (mask == 0xffffffffu) {
 #pragma unroll
-        for (int j = 0; j < AF_HALF; ++j) {
+        for (int j = 0; j < AD_HALF; ++j) {
           sv[j] *= scale_log2;
           cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < AF_HALF; ++j) {
+        for (int j = 0; j < AD_HALF; ++j) {
           sv[j] = ((mask >> j) & 1u) ? sv[j] * scale_log2 : -INFINITY;
           cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
         }
@@ -614,51 +613,54 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
       float cm = fmaxf(fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3])),
                        fmaxf(fmaxf(cmx[4], cmx[5]), fmaxf(cmx[6], cmx[7])));
       cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));   // the head's maximum
-      // move the running max only when this chunk exceeds it by more than AF_LAZY
+      // move the running max only when this chunk exceeds it by more than AD_LAZY
       float f = 1.f;
-      if (cm > m_used + AF_LAZY || (m_used == -INFINITY && cm != -INFINITY)) {
+      if (cm > m_used + AD_LAZY || (m_used == -INFINITY && cm != -INFINITY)) {
         f = m_used == -INFINITY ? 0.f : exp2f(m_used - cm);
         m_used = cm;
         l *= f;
+        le *= f;
       }
-      float psx[8];
+      // probabilities rounded to bf16 for the products; the output's normaliser adds the
+      // same rounded values (so each output is an exact convex combination of its rows),
+      // the log-sum-exp the exact ones
+      float psx[4], pex[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) psx[u] = 0.f;
-      float p[AF_HALF];
+      for (int x = 0; x < 4; ++x) psx[x] = pex[x] = 0.f;
+      uint32_t pk[AD_HALF / 2];
       const float msub = m_used == -INFINITY ? INFINITY : m_used;   // all p = 0 before a valid row
 #pragma unroll
-      for (int j = 0; j < AF_HALF; ++j) {
-        p[j] = fast_exp2(sv[j] - msub);
-        psx[j & 7] += p[j];
+      for (int j = 0; j < AD_HALF; j += 2) {
+        const float p0 = fast_exp2(sv[j] - msub), p1 = fast_exp2(sv[j + 1] - msub);
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+        pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+        const float2 r2 = __bfloat1622float2(v2);
+        psx[(j >> 1) & 3] += r2.x + r2.y;
+        pex[(j >> 1) & 3] += p0 + p1;
       }
-      l += ((psx[0] + psx[1]) + (psx[2] + psx[3])) + ((psx[4] + psx[5]) + (psx[6] + psx[7]));
+      l += (psx[0] + psx[1]) + (psx[2] + psx[3]);
+      le += (pex[0] + pex[1]) + (pex[2] + pex[3]);
       // P buffer s is free once the products of chunk c - 2 have completed
-      bool okp = c < 2 ||
-                 umma::mbar_wait(&kv_empty[(c - 2) % NS], ((c - 2) / NS) & 1, &d_err_attn);
-      if (!bar_and(1, 128, okp)) { ok = false; break; }
+      const bool okp = c < 2 || umma::mbar_wait(&kv_empty[s], ((c - 2) >> 1) & 1, &d_err_attn);
+      if (!bar_and(BAR_SOFTMAX, 128, okp)) { ok = false; break; }
       // P as the K-major B operand of O^T += C^T P^T (no swizzle): head h's 8-row runs are
-      // 16-byte core-matrix rows; this lane writes its 24 rows as three of them
-      uint8_t* pb = Ps + s * AF_P_BYTES + (h >> 3) * AF_P_SBO + (h & 7) * 16;
+      // 16-byte core-matrix rows; this lane writes its 32 rows as four of them
+      uint8_t* pb = Ps + s * AD_P_BYTES + (h >> 3) * AD_P_SBO + (h & 7) * 16;
 #pragma unroll
-      for (int c3 = 0; c3 < AF_HALF / 8; ++c3) {
-        uint32_t w[4];
-#pragma unroll
-        for (int u2 = 0; u2 < 4; ++u2) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(p[8 * c3 + 2 * u2], p[8 * c3 + 2 * u2 + 1]);
-          w[u2] = *reinterpret_cast<uint32_t*>(&v2);
-        }
-        const int kc = half * (AF_HALF / 8) + c3;   // 8-row group of the chunk
-        *reinterpret_cast<uint4*>(pb + kc * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int c4 = 0; c4 < AD_HALF / 8; ++c4) {
+        const int kc = half * (AD_HALF / 8) + c4;   // 8-row group of the chunk
+        *reinterpret_cast<uint4*>(pb + kc * 128) =
+            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
       }
       // heads whose max moved after products were accumulated: rescale their O^T columns
       const bool need = head_lane && f != 1.f && c > 0;
       if (head_lane) fac[h] = need ? f : 1.f;
-      if (bar_or(1, 128, need)) {
+      if (bar_or(BAR_SOFTMAX, 128, need)) {
         // the previous chunk's products must have landed in O^T first
         const bool okr = __all_sync(0xffffffffu,
-                                    umma::mbar_wait(&kv_empty[(c - 1) % NS], ((c - 1) / NS) & 1,
+                                    umma::mbar_wait(&kv_empty[(c - 1) & 1], ((c - 1) >> 1) & 1,
                                                     &d_err_attn));
-        if (!bar_and(1, 128, okr)) { ok = false; break; }
+        if (!bar_and(BAR_SOFTMAX, 128, okr)) { ok = false; break; }
         umma::fence_after();
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -668,7 +670,7 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
 #pragma unroll 1
           for (int dt = 0; dt < 4; ++dt) {
             uint32_t o[32];
-            const uint32_t addr = tmem + lane_addr + AF_O_COL + 64 * dt + 32 * hf;
+            const uint32_t addr = tmem + lane_addr + AD_O_COL + 64 * dt + 32 * hf;
             umma::tmem_ld32(addr, o);
             umma::tmem_ld_wait();
 #pragma unroll
@@ -685,42 +687,60 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
     }
     m_fin = m_used;
     l_fin = l + __shfl_xor_sync(0xffffffffu, l, 16);   // both halves of the head's rows
+    e_fin = le + __shfl_xor_sync(0xffffffffu, le, 16);
   } else if (warp == 8 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc_s = umma::idesc_f16(64, AF_CH, 1, 0, 0);
+    // ---------------- TMA and MMA issuer.  First the queries and the window chunks the
+    // TMA loads (their row masks are written here, before their slot is announced).
+    mbar_expect_tx(&q_full, AD_Q_BYTES);
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) tma_load_2d(Qs + j * AD_PLANE, &q_map, 64 * j, row * 64, &q_full);
+#pragma unroll 1
+    for (int c = 0; c < n_tma; ++c) {
+      const int valid = min(AD_CH, nw - AD_CH * c);
+      row_mask[c] = valid >= 64 ? ~0ull : ((1ull << valid) - 1ull);
+      mbar_expect_tx(&kv_full[c], AD_SLOT_BYTES);
+      const int y = int(lo + w0 + AD_CH * c - a.swa_pos0);
+#pragma unroll 1
+      for (int j = 0; j < 8; ++j)
+        tma_load_3d(KV + c * AD_SLOT_BYTES + j * AD_PLANE, &swa_map, 64 * j, y, b, &kv_full[c]);
+    }
+    constexpr uint32_t idesc_s = umma::idesc_f16(64, AD_CH, 1, 0, 0);
     constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 0);   // A = C^T (MN-major), B = P (K-major)
     const uint32_t kv0 = umma::smem_u32(KV), q0 = umma::smem_u32(Qs), p0 = umma::smem_u32(Ps);
     auto issue_s = [&](int c) {
-      const int s = c & 1, ks_ = c % NS;
-      if (!umma::mbar_wait(&kv_full[ks_], (c / NS) & 1, &d_err_attn)) return false;
-      // the first S also needs the queries' second half, which comes with chunk 1
-      if (c == 0 && n_ch > 1 && !umma::mbar_wait(&kv_full[1], 0, &d_err_attn)) return false;
-      if (c >= 2 && !umma::mbar_wait(&s_empty[s], ((c >> 1) - 1) & 1, &d_err_attn)) return false;
+      const int s = c & 1;
       umma::fence_after();
-      // K steps alternate between the two half accumulators (dims 0-255, 256-511)
       const uint64_t da0 = umma::desc_sw128(q0, 16, 1024);
-      const uint64_t db0 = umma::desc_sw128(kv0 + ks_ * AF_KV_BYTES, 16, 1024);
+      const uint64_t db0 = umma::desc_sw128(kv0 + s * AD_SLOT_BYTES, 16, 1024);
 #pragma unroll
-      for (int st = 0; st < 16; ++st)
-#pragma unroll
-        for (int hk = 0; hk < 2; ++hk) {
-          const int ks = hk * 16 + st;
-          const uint32_t offa = uint32_t(((ks >> 2) * 8192 + (ks & 3) * 32) >> 4);
-          const uint32_t offb = uint32_t(((ks >> 2) * AF_ATOM + (ks & 3) * 32) >> 4);
-          umma::mma_f16(tmem + AF_S_COL + 128 * s + 64 * hk, da0 + offa, db0 + offb, idesc_s, st > 0);
-        }
+      for (int ks = 0; ks < 32; ++ks) {
+        const uint32_t off = uint32_t(((ks >> 2) * AD_PLANE + (ks & 3) * 32) >> 4);
+        umma::mma_f16(tmem + AD_S_COL + 64 * s, da0 + off, db0 + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
       umma::commit(&s_full[s]);
-      return true;
+    };
+    auto issue_pv = [&](int c) {
+      const int s = c & 1;
+      umma::fence_after();
+      // the four dims tiles are independent accumulators: interleave them
+      const uint64_t pa0 = umma::desc_sw128(kv0 + s * AD_SLOT_BYTES, AD_PLANE, 1024);
+      const uint64_t pb0 = desc_noswz(p0 + s * AD_P_BYTES, 128, AD_P_SBO);
+#pragma unroll
+      for (int kk = 0; kk < AD_CH / 16; ++kk)
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt)
+          umma::mma_f16(tmem + AD_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * AD_PLANE + kk * 2048) >> 4),
+                        pb0 + uint32_t((kk * 256) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
+      umma::commit(&kv_empty[s]);   // slot s and P buffer s free again
     };
     // issue whichever is ready: the next chunk's S (its rows landed, its TMEM buffer read
-    // out) or the oldest pending P V (its probabilities written)
+    // out, the queries there) or the oldest pending P V (its probabilities written)
     int next_s = 0, next_pv = 0;
     uint32_t idle = 0;
     while (next_pv < n_ch) {
       if (next_s < n_ch && next_s <= next_pv + 1) {
         const int c = next_s, s = c & 1;
-        if (umma::mbar_test(&kv_full[c % NS], (c / NS) & 1) &&
-            (c != 0 || n_ch == 1 || umma::mbar_test(&kv_full[1], 0)) &&
+        if (umma::mbar_test(&kv_full[s], (c >> 1) & 1) && (c != 0 || umma::mbar_test(&q_full, 0)) &&
             (c < 2 || umma::mbar_test(&s_empty[s], ((c >> 1) - 1) & 1))) {
           issue_s(c);
           ++next_s;
@@ -728,122 +748,132 @@ __global__ void __launch_bounds__(AF_T, 1) attn_flash_kernel(AttnFlashArgs u) {
           continue;
         }
       }
-      const int c = next_pv, s = c & 1;
-      if (next_pv >= next_s || !umma::mbar_test(&p_full[s], (c >> 1) & 1)) {
-        if (++idle > (1u << 26)) { atomicOr(&d_err_attn, ERR_TIMEOUT); break; }
+      const int c = next_pv;
+      if (next_pv < next_s && umma::mbar_test(&p_full[c & 1], (c >> 1) & 1)) {
+        issue_pv(c);
+        ++next_pv;
+        idle = 0;
         continue;
       }
-      idle = 0;
-      ++next_pv;
-      umma::fence_after();
-      // the four dims tiles are independent accumulators: interleave them
-      const int ks_ = c % NS;
-      const uint64_t pa0 = umma::desc_sw128(kv0 + ks_ * AF_KV_BYTES, AF_ATOM, 1024);
-      const uint64_t pb0 = desc_noswz(p0 + s * AF_P_BYTES, 128, AF_P_SBO);
-#pragma unroll
-      for (int kk = 0; kk < AF_CH / 16; ++kk)
-#pragma unroll
-        for (int dt = 0; dt < 4; ++dt)
-          umma::mma_f16(tmem + AF_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * AF_ATOM + kk * 2048) >> 4),
-                        pb0 + uint32_t((kk * 256) >> 4), idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
-      umma::commit(&kv_empty[ks_]);
+      if (++idle > (1u << 26)) { atomicOr(&d_err_attn, ERR_TIMEOUT); break; }
     }
     umma::commit(&o_ready);
   }
 
-  // ---------------- merge.  Every CTA pushes its (max, sum) per head to all CTAs of the
-  // row and its scaled O^T tiles to each tile's owner (CTA dt % n_split); remote stores
-  // only, so no CTA waits on a remote load.  The owner then sums the slots it received.
+  // ---------------- merge
   __syncthreads();
-  if (n_ch > 0 && warp >= 4 && warp < 8) {
+  const bool o_warp = warp >= 4 && warp < 8;
+  if (n_ch > 0 && o_warp) {
     ok = ok && umma::mbar_wait(&o_ready, 0, &d_err_attn);
     umma::fence_after();
   }
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // every peer has started
-  if (warp >= 4 && warp < 8 && lane < 16) {
+  const int n_own = tiles_owned(rank, ns), n_out = 4 - n_own;
+  if (ns > 1 && tid == 0) mbar_expect_tx(&recv_bar, uint32_t(n_own * (ns - 1)) * AD_TILE_BYTES);
+  if (o_warp && lane < 16) {
     const int h = 16 * (warp & 3) + lane;
-    const float2 mine = make_float2(m_fin, l_fin);
-    for (int r = 0; r < u.n_split; ++r)
-      *reinterpret_cast<float2*>(cluster.map_shared_rank(&ml_all[rank][h][0], r)) = mine;
+    const float4 mine = make_float4(m_fin, l_fin, e_fin, 0.f);
+    for (int r = 0; r < ns; ++r)
+      *reinterpret_cast<float4*>(cluster.map_shared_rank(&ml_all[rank][h][0], r)) = mine;
   }
   cluster.sync();
   if (tid < 64) {
     const int h = tid;
     const float sk = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
     float M = sk;
-    for (int r = 0; r < u.n_split; ++r) M = fmaxf(M, ml_all[r][h][0]);
-    float L = a.sink ? exp2f(sk - M) : 0.f;
-    for (int r = 0; r < u.n_split; ++r)
-      if (ml_all[r][h][1] > 0.f) L += ml_all[r][h][1] * exp2f(ml_all[r][h][0] - M);
+    for (int r = 0; r < ns; ++r) M = fmaxf(M, ml_all[r][h][0]);
+    float L = a.sink ? exp2f(sk - M) : 0.f, Le = L;
+    for (int r = 0; r < ns; ++r)
+      if (ml_all[r][h][1] > 0.f) {
+        const float g = exp2f(ml_all[r][h][0] - M);
+        L += ml_all[r][h][1] * g;
+        Le += ml_all[r][h][2] * g;
+      }
     fac[h] = ml_all[rank][h][1] > 0.f ? exp2f(ml_all[rank][h][0] - M) / L : 0.f;
-    if (rank == 0 && a.lse) a.lse[size_t(row) * 64 + h] = (M + log2f(L)) * 0.6931471805599453f;
+    if (rank == 0 && a.lse) a.lse[size_t(row) * 64 + h] = (M + log2f(Le)) * 0.6931471805599453f;
   }
   __syncthreads();
-  const int n_lt = (4 + u.n_split - 1) / u.n_split;   // tile slots per source rank
   // softmax warps: lane = dim 32 q + lane of each 128-dim tile; the factors go to registers
   // first (the compiler cannot tell the stores below from fac[] and would reload it)
-  const bool o_warp = warp >= 4 && warp < 8;
   const int q = warp & 3;
   const uint32_t lane_addr = uint32_t(32 * q) << 16;
   float fr[64];
   if (o_warp) {
 #pragma unroll
     for (int x = 0; x < 64; ++x) fr[x] = n_ch > 0 ? fac[x] : 0.f;
-    // tiles owned by another CTA: scaled O^T to the owner's slot for this rank
-    for (int dt = 0; dt < 4; ++dt) {
-      if (dt % u.n_split == rank) continue;
-      float* dst = cluster.map_shared_rank(Obuf, dt % u.n_split) +
-                   size_t((rank * n_lt + dt / u.n_split) * 64) * 128 + 32 * q + lane;
+    // tiles owned by another CTA: scaled O^T, [head][dim], into this CTA's outgoing slots
+    int o = 0;
+    for (int dt = 0; dt < 4 && ns > 1; ++dt) {
+      if (dt % ns == rank) continue;
+      float* stg = reinterpret_cast<float*>(Mg + o * AD_TILE_BYTES) + 32 * q + lane;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t o[32];
+        uint32_t v[32];
         if (n_ch > 0) {
-          umma::tmem_ld32(tmem + lane_addr + AF_O_COL + 64 * dt + 32 * hf, o);
+          umma::tmem_ld32(tmem + lane_addr + AD_O_COL + 64 * dt + 32 * hf, v);
           umma::tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = 0u;
+          for (int x = 0; x < 32; ++x) v[x] = 0u;
         }
 #pragma unroll
-        for (int x = 0; x < 32; ++x) dst[(32 * hf + x) * 128] = __uint_as_float(o[x]) * fr[32 * hf + x];
+        for (int x = 0; x < 32; ++x) stg[(32 * hf + x) * 128] = __uint_as_float(v[x]) * fr[32 * hf + x];
       }
+      ++o;
     }
   }
-  umma::fence_before();
-  cluster.sync();
-  // owned tiles: own O^T (TMEM) plus the other CTAs' slots (local shared memory), bf16 out
+  umma::fence_proxy_async();   // the outgoing tiles are read by the bulk copies below
+  __syncthreads();
+  if (ns > 1 && tid == 0) {
+    int o = 0;
+    for (int dt = 0; dt < 4; ++dt) {
+      const int owner = dt % ns;
+      if (owner == rank) continue;
+      // in the owner's incoming slots: [index of this CTA among its sources][owned tile]
+      const int src_idx = rank < owner ? rank : rank - 1;
+      const int own_o = tiles_owned(owner, ns);
+      const uint32_t off = uint32_t(4 - own_o + src_idx * own_o + dt / ns) * AD_TILE_BYTES;
+      bulk_to_peer(map_rank(Mg + off, owner), Mg + o * AD_TILE_BYTES, AD_TILE_BYTES,
+                   map_rank(&recv_bar, owner));
+      ++o;
+    }
+  }
+  // owned tiles: own O^T (TMEM) plus the other CTAs' tiles (received), bf16 out
   if (o_warp) {
-    for (int lt = 0; rank + lt * u.n_split < 4; ++lt) {
-      const int dt = rank + lt * u.n_split;
+    const bool okr = ns == 1 || umma::mbar_wait(&recv_bar, 0, &d_err_attn);
+    for (int lt = 0; rank + lt * ns < 4 && okr; ++lt) {
+      const int dt = rank + lt * ns;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + size_t(row) * 64 * 512 +
                             dt * 128 + 32 * q + lane;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t o[32];
+        uint32_t v[32];
         if (n_ch > 0) {
-          umma::tmem_ld32(tmem + lane_addr + AF_O_COL + 64 * dt + 32 * hf, o);
+          umma::tmem_ld32(tmem + lane_addr + AD_O_COL + 64 * dt + 32 * hf, v);
           umma::tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int x = 0; x < 32; ++x) o[x] = 0u;
+          for (int x = 0; x < 32; ++x) v[x] = 0u;
         }
         float acc[32];
 #pragma unroll
-        for (int x = 0; x < 32; ++x) acc[x] = __uint_as_float(o[x]) * fr[32 * hf + x];
-        for (int r = 0; r < u.n_split; ++r) {
-          if (r == rank) continue;
-          const float* src = Obuf + size_t((r * n_lt + lt) * 64 + 32 * hf) * 128 + 32 * q + lane;
-          float v[32];
+        for (int x = 0; x < 32; ++x) acc[x] = __uint_as_float(v[x]) * fr[32 * hf + x];
+        for (int si = 0; si < ns - 1; ++si) {
+          const float* in = reinterpret_cast<const float*>(Mg + (n_out + si * n_own + lt) * AD_TILE_BYTES) +
+                            (32 * hf) * 128 + 32 * q + lane;
+          float w[32];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] = src[x * 128];
+          for (int x = 0; x < 32; ++x) w[x] = in[x * 128];
 #pragma unroll
-          for (int x = 0; x < 32; ++x) acc[x] += v[x];
+          for (int x = 0; x < 32; ++x) acc[x] += w[x];
         }
 #pragma unroll
         for (int x = 0; x < 32; ++x) orow[(32 * hf + x) * 512] = __float2bfloat16_rn(acc[x]);
       }
     }
   }
+  umma::fence_before();
+  cluster.sync();   // no CTA leaves while a peer may still read or write its shared memory
   umma::fence_after();
   if (warp == 0) umma::tmem_free(tmem, 512);
 }
@@ -915,8 +945,8 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
               scale, (uint16_t*)out, lse_out, kv_codes, kv_scales, swa_codes, swa_scales};
   cudaStream_t st = (cudaStream_t)stream;
   if (H == 64) {
-    // tensor-core path: a cluster of n_split CTAs per row (enough CTAs to cover the SMs),
-    // partial results merged through distributed shared memory
+    // tensor-core path: a cluster of n_split CTAs per row, partial results merged through
+    // distributed shared memory; queries (and bf16 window rows) through tensor maps
     (void)workspace; (void)ws_bytes;
     // per device, once: the kernels' shared-memory attribute and the SM count (cached only
     // after both succeeded; concurrent first calls repeat the same settings)
@@ -927,29 +957,60 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     if (dev < 0 || dev >= 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: device id");
     int sms = sms_cache[dev].load(std::memory_order_acquire);
     if (sms == 0) {
-      e0 = cudaFuncSetAttribute(attn_flash_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
+      e0 = cudaFuncSetAttribute(attn_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
       if (e0 == cudaSuccess)
-        e0 = cudaFuncSetAttribute(attn_flash_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AF_SMEM));
+        e0 = cudaFuncSetAttribute(attn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
       if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
       sms_cache[dev].store(sms, std::memory_order_release);
     }
-    // CTAs per row: all CTAs in one wave, and the estimated time of a row's chunks (about
-    // 1.5 us each, per CTA) plus the cluster merge (about 4 us) the smallest
-    const int n_ch_max = ceil_div(k + window, AF_CH);
-    const int n_fit = std::max(1, std::min(int(sms / rows), AF_MAX_SPLIT));
+    if (rows * 64 > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many query rows");
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return fail(CSA2_ERR_CUDA, "sparse_attn: cuTensorMapEncodeTiled not available");
+    // queries: [rows * 64 heads][512 dims] bf16, one box = 64 heads x 64 dims (one plane)
+    CUtensorMap q_map, swa_map;
+    {
+      const cuuint64_t dims[2] = {512, cuuint64_t(rows * 64)};
+      const cuuint64_t strides[1] = {1024};
+      const cuuint32_t box[2] = {64, 64};
+      const cuuint32_t estr[2] = {1, 1};
+      if (enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return fail(CSA2_ERR_CUDA, "sparse_attn: query tensor map");
+    }
+    // bf16 window rows: [B][rows up to the last query's position][512 dims]; rows past the
+    // last query are outside the map and read as zeros
+    int win_tma = 0;
+    swa_map = q_map;   // (unused unless the window rows are bf16)
+    if (swa_kv) {
+      const long long valid = std::min<long long>(S, (long long)q_pos0 + Tq - swa_pos0);
+      const cuuint64_t dims[3] = {512, cuuint64_t(valid), cuuint64_t(B)};
+      const cuuint64_t strides[2] = {1024, cuuint64_t(S) * 1024};
+      const cuuint32_t box[3] = {64, 64, 1};
+      const cuuint32_t estr[3] = {1, 1, 1};
+      if (enc(&swa_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(swa_kv), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return fail(CSA2_ERR_CUDA, "sparse_attn: window tensor map");
+      win_tma = 1;
+    }
+    // CTAs per row: all CTAs in one wave, and the estimated time of a CTA's chunks (about
+    // 1.4 us each) plus the cluster merge (about 2 us) the smallest
+    const int n_ch_max = ceil_div(k, AD_CH) + ceil_div(window, AD_CH);
+    const int n_fit = std::max(1, std::min(int(sms / rows), AD_MAX_SPLIT));
     int n_split = 1;
     for (int n = 2; n <= n_fit; ++n) {
-      const int t_n = 3 * ceil_div(n_ch_max, n) + 8, t_best = 3 * ceil_div(n_ch_max, n_split) + (n_split > 1 ? 8 : 0);
+      const int t_n = 7 * ceil_div(n_ch_max, n) + 10, t_best = 7 * ceil_div(n_ch_max, n_split) + (n_split > 1 ? 10 : 0);
       if (t_n < t_best) n_split = n;
     }
     if (rows * n_split > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
-    AttnFlashArgs fa{aa, n_split};
+    AttnDecodeArgs da{aa, n_split, win_tma};
     e0 = (fp4 || fp8w)
-             ? launch_k(attn_flash_kernel<true>, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1),
-                        AF_SMEM, st, unsigned(n_split), fa)
-             : launch_k(attn_flash_kernel<false>, dim3(unsigned(rows * n_split), 1, 1), dim3(AF_T, 1, 1),
-                        AF_SMEM, st, unsigned(n_split), fa);
+             ? launch_k(attn_decode_kernel<true>, dim3(unsigned(rows * n_split), 1, 1), dim3(AD_T, 1, 1),
+                        AD_SMEM, st, unsigned(n_split), da, q_map, swa_map)
+             : launch_k(attn_decode_kernel<false>, dim3(unsigned(rows * n_split), 1, 1), dim3(AD_T, 1, 1),
+                        AD_SMEM, st, unsigned(n_split), da, q_map, swa_map);
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: launch");
     note_launch();
   } else {

@@ -1026,23 +1026,8 @@ namespace {
 // (2 halves) x (64-key blocks over all sequences).  A box of {64, 32, 1, nblk} lands one
 // half of nblk consecutive blocks as 32 nblk rows of 64 bytes with the 64-byte swizzle:
 // with nblk = 4 that is one whole MMA tile of a 256-key step.
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiledFn encode_fn() {   // looked up once (thread-safe static initialisation)
-  static const EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess && q == cudaDriverEntryPointSuccess)
-      return reinterpret_cast<EncodeTiledFn>(p);
-    return EncodeTiledFn(nullptr);
-  }();
-  return fn;
-}
 bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys, int nblk) {
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (!enc || total_keys % 64 != 0 || total_keys / 64 > (1ll << 31) - 1) return false;
   const cuuint64_t dims[4] = {64, 32, 2, cuuint64_t(total_keys / 64)};
   const cuuint64_t strides[3] = {64, 64 * 32, 64 * 64};
