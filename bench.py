@@ -73,18 +73,18 @@ def attention_kernel_hash(text):
     return hashlib.sha256("\n".join(code).encode()).hexdigest()[:16]
 
 
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "attn_traffic.json")
+
+
 def attention_traffic(modes):
-    """DRAM bytes per attention launch, averaged over one step's layers, from the ncu record in
-    profiles/attn_flash_b64_ctx8k.md (layers with a global branch read the headline shape,
-    window-only layers 128 rows).  None when the kernel code no longer matches the record or
-    the record is missing."""
+    """DRAM bytes per attention launch, averaged over one step's layers, from the ncu traffic
+    record (a JSON data file next to the profile summaries: bytes of a launch for a layer with
+    a global branch at the headline shape, and of a window-only launch, plus the hash of the
+    kernel code they were captured on).  None when the kernel code no longer matches the
+    record or the record is missing."""
     try:
-        rec = {}
-        with open(os.path.join(ROOT, "profiles", "attn_flash_b64_ctx8k.md"), encoding="utf-8") as f:
-            for line in f:
-                parts = line.strip().split(":")
-                if len(parts) == 2 and parts[0].startswith(("traffic_", "attention_kernel")):
-                    rec[parts[0].strip()] = parts[1].strip()
+        with open(TRAFFIC_RECORD, encoding="utf-8") as f:
+            rec = json.load(f)
         with open(os.path.join(ROOT, "compressed_sparse_attention_04_gb300", "csrc", "attention.cu"),
                   encoding="utf-8") as f:
             h = attention_kernel_hash(f.read())
