@@ -1,4 +1,5 @@
-"""Compile libcsa2.so (and the input generator's libcsa2_synth.so) for sm_103a.
+"""Compile libcsa2.so (and the input generator's libcsa2_synth.so, and the tensor-rate
+probe libcsa2_peak.so that bench.py uses for the FP4 roofline denominator) for sm_103a.
 
 Each .cu is compiled to an object in parallel with nvcc, then linked into a shared
 library next to its sources' package.  Run ``python -m
@@ -68,6 +69,7 @@ def build_all(force=False):
                     extra_deps=[os.path.join(ROOT, "include", "csa2.h")], force=force)
     syn = build_lib(os.path.join(ROOT, "synth", "csrc"), os.path.join(ROOT, "synth", "libcsa2_synth.so"),
                     force=force)
+    build_lib(os.path.join(PKG_DIR, "peak"), os.path.join(PKG_DIR, "peak", "libcsa2_peak.so"), force=force)
     return lib, syn
 
 
