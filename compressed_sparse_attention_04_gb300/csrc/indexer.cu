@@ -196,11 +196,11 @@ __device__ __forceinline__ uint64_t desc_noswz(uint32_t saddr) {
   return d;
 }
 __device__ __forceinline__ void mma_fp4(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t sfa,
-                                        uint32_t sfb, uint32_t accumulate) {
+                                        uint32_t sfb, uint32_t accumulate, uint32_t idesc = SU_IDESC) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-      :: "r"(tmem_d), "l"(da), "l"(db), "r"(SU_IDESC), "r"(sfa), "r"(sfb), "r"(accumulate));
+      :: "r"(tmem_d), "l"(da), "l"(db), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate));
 }
 // per-16 scale words for the two K = 64 halves from four per-32 E4M3 bytes: (s0 s0 s1 s1),
 // (s2 s2 s3 s3)
@@ -285,12 +285,38 @@ struct StepCursor {
   __device__ int row(const ScoreArgs& a) const { return b * a.Tq + i; }
 };
 
+// ---- prefill scoring (score_prefill_kernel below): PF_QG consecutive queries of a
+// sequence share each 128-key tile, their 32 heads each side by side on the MMA's N.
+constexpr int PF_QG = 4;                        // queries per group (N = 128)
+constexpr int PF_TILE = 128;                    // keys per step (M)
+constexpr int PF_STAGES = 8;                    // key ring
+constexpr int PF_ND = 3;                        // TMEM accumulators (steps)
+constexpr int PF_T = 448;                       // copy, MMA, 4 scale-factor and 8 epilogue warps
+constexpr uint32_t PF_A_BYTES = PF_TILE * 64;   // 8 KB of codes per step
+constexpr uint32_t PF_Q_IMG = PF_QG * SU_Q_BYTES;            // 8 KB of query codes per group
+constexpr uint32_t PF_Q_SC = PF_QG * 128;                    // their scale words
+constexpr uint32_t PF_SMEM = PF_STAGES * (PF_A_BYTES + PF_TILE * 4) + 2 * (PF_Q_IMG + PF_Q_SC) + 1024;
+constexpr uint32_t PF_SFA_COL = 384, PF_SFB_COL = 448;       // D: 3 x 128 columns
+constexpr uint32_t PF_IDESC = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr int PF_MIN_TQ = 64;                   // calls with fewer queries keep the decode scorer
+
 // One warp per (query row, head), grid-stride: the FP4 query as the MMA's B operand image
 // (32 heads x 64 bytes, K-major, no swizzle) followed by its E4M3 block scales (4 bytes per
 // head).  Lane l holds dims 4 l .. 4 l + 3, so lanes 8 b .. 8 b + 7 form 32-dim block b; the
 // block's scale and codes follow the same rules as fp4_quant_lane.  CTA 0 also writes the
 // step prefix table.
-__global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep, int* prefix,
+// Where q_prep writes a row's FP4 image and scale words (decode: image and scales of a row
+// together, SU_QROW_BYTES apart; prefill: images 2 KB apart, scale words 128 B apart, so that
+// the images of consecutive queries form one operand), and which step table it builds.
+struct QPrepOut {
+  uint8_t* img;
+  uint32_t img_stride;
+  uint8_t* sc;
+  uint32_t sc_stride;
+  int groups;   // prefill scorer: steps per group of PF_QG queries instead of per query
+};
+
+__global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, QPrepOut qo, int* prefix,
                                                      long long n_items) {
   pdl_wait();
   __shared__ int scan[32];
@@ -322,13 +348,31 @@ __global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, uint8_t* qprep
     const uint32_t w1 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 2);
     const uint32_t w2 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 4);
     const uint32_t w3 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 6);
-    uint8_t* out = qprep + size_t(row) * SU_QROW_BYTES;
     if (l8 == 0) {
-      *reinterpret_cast<uint4*>(out + fp4_chunk_off(h, blk)) = make_uint4(word, w1, w2, w3);
-      out[SU_Q_BYTES + h * 4 + blk] = uint8_t(sb);
+      *reinterpret_cast<uint4*>(qo.img + size_t(row) * qo.img_stride + fp4_chunk_off(h, blk)) =
+          make_uint4(word, w1, w2, w3);
+      qo.sc[size_t(row) * qo.sc_stride + h * 4 + blk] = uint8_t(sb);
     }
   }
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == 0 && qo.groups) {
+    // prefill: the 128-key steps of each group of PF_QG queries (the group's last query
+    // sees the most entries)
+    const int G = (a.Tq + PF_QG - 1) / PF_QG;
+    const int per = (G + 127) / 128, g0 = tid * per, g1 = min(G, g0 + per);
+    auto steps = [&](int g) {
+      const int last = min(a.Tq - 1, PF_QG * g + PF_QG - 1);
+      return (n_visible((long long)a.q_pos0 + last, a.m, a.n_entries) + PF_TILE - 1) / PF_TILE;
+    };
+    int mine = 0;
+    for (int g = g0; g < g1; ++g) mine += steps(g);
+    int tot;
+    int run = block_excl_scan<128>(mine, scan, tot);
+    for (int g = g0; g < g1; ++g) {
+      prefix[g] = run;
+      run += steps(g);
+    }
+    if (tid == 0) prefix[G] = tot;
+  } else if (blockIdx.x == 0) {
     // thread t sums the steps of rows [t per, (t + 1) per), one block scan of the 128 sums,
     // then each thread writes its rows' offsets (one scan instead of Tq / 128 of them)
     const bool pool = a.cand != nullptr, bm = a.blockmax != nullptr;
@@ -643,6 +687,239 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
   umma::fence_before();
   __syncthreads();
   if (warp == 0) umma::tmem_free(tmem, SU_TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- prefill scoring
+// Work: the (sequence, group of PF_QG queries, 128-key step) triples in order, split evenly
+// over persistent CTAs (one per SM).  A step's keys (128 keys x 64 code bytes: one TMA box
+// of two 64-key blocks, plus 512 scale bytes) are the MMA's A operand (M = 128); the group's
+// four query images (32 heads each, consecutive in the workspace) are B (N = 128); two
+// K = 64 block-scaled FP4 MMAs per step into one of three TMEM accumulators.  Eight epilogue
+// warps (two per TMEM lane quadrant, two queries each) apply ReLU and the head weights
+// (packed float pairs) and store the scores of the keys each query sees.
+struct GroupCursor {
+  int b, g, st, n;   // sequence, group, step within the group, steps in the group
+  int k;             // groups entered by this CTA so far, minus one
+  __device__ void init(const ScoreArgs& a, int G, long long s) {
+    const int T = a.prefix[G];
+    b = int(s / T);
+    const int r = int(s % T);
+    int lo = 0, hi = G - 1;   // largest group with prefix <= r (that group has steps)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.prefix[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    st = r - a.prefix[g];
+    n = a.prefix[g + 1] - a.prefix[g];
+    k = 0;
+  }
+  __device__ bool next(const ScoreArgs& a, int G) {   // only called while steps remain
+    if (++st < n) return false;
+    do {
+      if (++g == G) { g = 0; ++b; }
+      n = a.prefix[g + 1] - a.prefix[g];
+    } while (n == 0);
+    st = 0;
+    ++k;
+    return true;
+  }
+};
+
+__device__ __forceinline__ float relu_dot32(const uint32_t (&v)[32], const float (&w)[32]) {
+  // sum_h w_h max(s_h, 0) with packed pair FMAs (even heads in .x, odd in .y)
+  uint64_t acc;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(acc) : "f"(0.f));
+#pragma unroll
+  for (int h = 0; h < 32; h += 2) {
+    uint64_t ww, rr;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ww) : "f"(w[h]), "f"(w[h + 1]));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rr) : "f"(fmaxf(__uint_as_float(v[h]), 0.f)),
+                                             "f"(fmaxf(__uint_as_float(v[h + 1]), 0.f)));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(ww), "l"(rr));
+  }
+  float x, y;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(acc));
+  return x + y;
+}
+
+__global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, const uint8_t* qimg,
+                                                                const uint8_t* qsc, int G,
+                                                                const __grid_constant__ CUtensorMap codes_map2) {
+  pdl_wait();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* As = base;                                                        // PF_STAGES x 8 KB
+  uint32_t* Ss = reinterpret_cast<uint32_t*>(base + PF_STAGES * PF_A_BYTES); // PF_STAGES x 128 words
+  uint8_t* Qb = base + PF_STAGES * (PF_A_BYTES + PF_TILE * 4);               // 2 x (image + scales)
+  __shared__ __align__(8) uint64_t a_empty[PF_STAGES], land[PF_STAGES], sf_ready[PF_STAGES];
+  __shared__ __align__(8) uint64_t d_full[PF_ND], d_empty[PF_ND], q_empty[2];
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long S = a.total_steps;
+  const long long s_begin = S * blockIdx.x / gridDim.x, s_end = S * (blockIdx.x + 1) / gridDim.x;
+  const int L = int(s_end - s_begin);
+  if (L <= 0) return;   // uniform
+  constexpr uint32_t QBUF = PF_Q_IMG + PF_Q_SC;
+
+  if (tid == 0) {
+    for (int s2 = 0; s2 < PF_STAGES; ++s2) {
+      umma::mbar_init(&a_empty[s2], 1);
+      umma::mbar_init(&land[s2], 1);
+      umma::mbar_init(&sf_ready[s2], 4);
+    }
+    for (int d = 0; d < PF_ND; ++d) {
+      umma::mbar_init(&d_full[d], 1);
+      umma::mbar_init(&d_empty[d], 8);
+    }
+    umma::mbar_init(&q_empty[0], 1);
+    umma::mbar_init(&q_empty[1], 1);
+    umma::mbar_fence_init();
+  }
+  if (warp == 0) umma::tmem_alloc(&tmem_slot, 512);
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- copy thread: per step one TMA box of codes and the scale bytes; at a
+    // new group the group's query images and scale words
+    if (lane == 0) {
+      const long long total_keys = (long long)(a.rows / a.Tq) * a.n_cap;   // B * n_cap
+      GroupCursor cc;
+      cc.init(a, G, s_begin);
+      for (int g = 0; g < L; ++g) {
+        const bool new_grp = g > 0 && cc.next(a, G);
+        const int s2 = g % PF_STAGES;
+        if (g >= PF_STAGES &&
+            !umma::mbar_wait(&a_empty[s2], ((g / PF_STAGES) - 1) & 1, &d_err_indexer)) break;
+        const int qb = cc.k & 1;
+        if ((g == 0 || new_grp) && cc.k >= 2 &&
+            !umma::mbar_wait(&q_empty[qb], ((cc.k >> 1) - 1) & 1, &d_err_indexer)) break;
+        const long long key0 = (long long)cc.b * a.n_cap + (long long)cc.st * PF_TILE;
+        const uint32_t sbytes = uint32_t(min((long long)PF_TILE, total_keys - key0)) * 4u;
+        const bool load_q = g == 0 || new_grp;
+        mbar_arrive_expect_tx(&land[s2], PF_A_BYTES + sbytes + (load_q ? QBUF : 0u));
+        if (load_q) {
+          const size_t r0 = size_t(cc.b) * a.Tq + size_t(cc.g) * PF_QG;   // the group's first row
+          bulk_load(Qb + qb * QBUF, qimg + r0 * SU_Q_BYTES, PF_Q_IMG, &land[s2]);
+          bulk_load(Qb + qb * QBUF + PF_Q_IMG, qsc + r0 * 128, PF_Q_SC, &land[s2]);
+        }
+        tma_load_4d(As + s2 * PF_A_BYTES, &codes_map2, 0, 0, 0, int(key0 >> 6), &land[s2]);
+        bulk_load(Ss + s2 * PF_TILE, a.scales + key0 * 4, sbytes, &land[s2]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: two K = 64 MMAs per step
+    if (lane == 0) {
+      const uint32_t a0 = umma::smem_u32(As), q0 = umma::smem_u32(Qb);
+      GroupCursor cm;
+      cm.init(a, G, s_begin);
+      for (int g = 0; g < L; ++g) {
+        // entering a new group: the MMAs so far are the last that read the other query
+        // buffer's predecessor, which may be refilled once they complete
+        if (g > 0 && cm.next(a, G)) umma::commit(&q_empty[(cm.k - 1) & 1]);
+        const int s2 = g % PF_STAGES, d = g % PF_ND, qb = cm.k & 1;
+        if (!umma::mbar_wait(&sf_ready[s2], (g / PF_STAGES) & 1, &d_err_indexer)) break;
+        if (!umma::mbar_wait(&d_empty[d], ((g / PF_ND) & 1) ^ 1, &d_err_indexer)) break;
+        umma::fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma_fp4(tmem + 128 * d, desc_sw64(a0 + s2 * PF_A_BYTES + ks * 32),
+                  desc_noswz(q0 + qb * QBUF + ks * 256), tmem + PF_SFA_COL + 8 * s2 + 4 * ks,
+                  tmem + PF_SFB_COL + 8 * qb + 4 * ks, ks, PF_IDESC);
+        umma::commit(&a_empty[s2]);
+        umma::commit(&d_full[d]);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ---------------- scale factors into TMEM (this warp's lane quadrant): the step's keys
+    // (key 32 c + lane in column c of each K half) and, at a new group, its queries (head
+    // lane of query c in column c)
+    const uint32_t lane_addr = uint32_t((warp & 3) * 32) << 16;
+    GroupCursor cs;
+    cs.init(a, G, s_begin);
+    for (int g = 0; g < L; ++g) {
+      const bool new_grp = g > 0 && cs.next(a, G);
+      const int s2 = g % PF_STAGES, qb = cs.k & 1;
+      if (!umma::mbar_wait(&land[s2], (g / PF_STAGES) & 1, &d_err_indexer)) break;
+      if (g == 0 || new_grp) {
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(Qb + qb * QBUF + PF_Q_IMG);
+        uint32_t v[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t w4 = qw[32 * c + lane];
+          v[c] = sf_lo(w4);
+          v[4 + c] = sf_hi(w4);
+        }
+        umma::tmem_st8(tmem + lane_addr + PF_SFB_COL + 8 * qb, v);
+      }
+      uint32_t v[8];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t s4 = Ss[s2 * PF_TILE + 32 * c + lane];
+        v[c] = sf_lo(s4);
+        v[4 + c] = sf_hi(s4);
+      }
+      umma::tmem_st8(tmem + lane_addr + PF_SFA_COL + 8 * s2, v);
+      umma::tmem_st_wait();
+      umma::fence_before();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&sf_ready[s2]);
+    }
+  } else {
+    // ---------------- epilogue: lane quadrant warp % 4 (keys 32 q .. 32 q + 31 of the step),
+    // queries 2 hq and 2 hq + 1 of the group
+    const int q = warp & 3, hq = (warp - 6) >> 2;
+    const uint32_t lane_addr = uint32_t(q * 32) << 16;
+    GroupCursor ce;
+    ce.init(a, G, s_begin);
+    float w0[32], w1[32];
+    for (int g = 0; g < L; ++g) {
+      const bool new_grp = g == 0 || (g > 0 && ce.next(a, G));
+      const int i0 = ce.g * PF_QG + 2 * hq;              // this warp's first query index
+      const size_t row0 = size_t(ce.b) * a.Tq + i0;
+      const bool ok0 = i0 < a.Tq, ok1 = i0 + 1 < a.Tq;
+      if (new_grp) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          w0[h] = ok0 ? a.w[row0 * 32 + h] : 0.f;
+          w1[h] = ok1 ? a.w[(row0 + 1) * 32 + h] : 0.f;
+        }
+      }
+      const int d = g % PF_ND;
+      if (!umma::mbar_wait(&d_full[d], (g / PF_ND) & 1, &d_err_indexer)) break;
+      umma::fence_after();
+      // one query's 32 head sums at a time (registers: both queries' weights + one slice)
+      const int key = ce.st * PF_TILE + 32 * q + lane;
+      float sc0, sc1;
+      {
+        uint32_t v[32];
+        umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * (2 * hq)), v);
+        umma::tmem_ld_wait();
+        sc0 = relu_dot32(v, w0);
+      }
+      {
+        uint32_t v[32];
+        umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * (2 * hq + 1)), v);
+        umma::tmem_ld_wait();
+        sc1 = relu_dot32(v, w1);
+      }
+      umma::fence_before();
+      __syncwarp();
+      if (lane == 0) umma::mbar_arrive(&d_empty[d]);      // accumulators copied out
+      if (ok0 && key < n_visible((long long)a.q_pos0 + i0, a.m, a.n_entries))
+        a.scores[row0 * a.row_len + key] = sc0;
+      if (ok1 && key < n_visible((long long)a.q_pos0 + i0 + 1, a.m, a.n_entries))
+        a.scores[(row0 + 1) * a.row_len + key] = sc1;
+    }
+  }
+  umma::fence_before();
+  __syncthreads();
+  if (warp == 0) umma::tmem_free(tmem, 512);
 }
 
 constexpr int TK_T = 512;
@@ -1005,7 +1282,7 @@ size_t csa2_indexer_workspace_size(int B, int Tq, int n_entries, int nb, int blk
              align_up(size_t(B) * Tq * size_t((row_len + FT_SEG - 1) / FT_SEG) * 4, 256);   // counts
   }
   // FP4 query images and the step prefix table of the tensor-core scorer
-  bytes += align_up(size_t(B) * Tq * SU_QROW_BYTES, 256) + align_up(size_t(Tq + 1) * 4, 256);
+  bytes += align_up(size_t(size_t(B) * Tq + PF_QG) * SU_QROW_BYTES, 256) + align_up(size_t(Tq + 1) * 4, 256);
   return bytes;
 }
 
@@ -1026,12 +1303,13 @@ namespace {
 // (2 halves) x (64-key blocks over all sequences).  A box of {64, 32, 1, nblk} lands one
 // half of nblk consecutive blocks as 32 nblk rows of 64 bytes with the 64-byte swizzle:
 // with nblk = 4 that is one whole MMA tile of a 256-key step.
-bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys, int nblk) {
+// halves = 2: a box of whole blocks, nblk x 64 keys in key order (the prefill scorer's tiles)
+bool make_codes_map(CUtensorMap* map, const uint8_t* codes, long long total_keys, int nblk, int halves = 1) {
   EncodeTiledFn enc = tensor_map_encoder();
   if (!enc || total_keys % 64 != 0 || total_keys / 64 > (1ll << 31) - 1) return false;
   const cuuint64_t dims[4] = {64, 32, 2, cuuint64_t(total_keys / 64)};
   const cuuint64_t strides[3] = {64, 64 * 32, 64 * 64};
-  const cuuint32_t box[4] = {64, 32, 1, cuuint32_t(nblk)};
+  const cuuint32_t box[4] = {64, 32, cuuint32_t(halves), cuuint32_t(nblk)};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(codes), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -1071,7 +1349,8 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   const bool chunked = row_len > TK_SMEM_KEYS;
   const size_t n_chunks_tk = chunked ? size_t((row_len + TK_CHUNK - 1) / TK_CHUNK) : 0;
   const size_t cand_bytes = chunked ? align_up(size_t(rows) * n_chunks_tk * CSA2_MAX_TOPK * 4, 256) : 0;
-  const size_t qprep_bytes = align_up(size_t(rows) * SU_QROW_BYTES, 256);
+  // FP4 query images (+ PF_QG rows of padding: a prefill group may run past the last row)
+  const size_t qprep_bytes = align_up(size_t(rows + PF_QG) * SU_QROW_BYTES, 256);
   const size_t prefix_bytes = align_up(size_t(Tq + 1) * 4, 256);
   const int nb64 = int((row_len + 63) / 64);
   const size_t bm64_bytes = chunked ? align_up(size_t(rows) * nb64 * 4, 256) : 0;
@@ -1107,7 +1386,48 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
         bm64_src = bm64_ws;
       }
     }
-    if (umma_ok) {
+    // prefill rows (many queries per sequence, Full mode, rows short enough for the staged
+    // top-k): groups of PF_QG queries share each key tile
+    const bool prefill = !cand && !blockmax_out && !chunked && Tq >= PF_MIN_TQ && n_cap % 64 == 0;
+    if (prefill) {
+      const int G = ceil_div(Tq, PF_QG);
+      long long per_seq = 0;
+      for (int g = 0; g < G; ++g) {
+        const int last = std::min(Tq - 1, PF_QG * g + PF_QG - 1);
+        per_seq += ceil_div(n_visible((long long)q_pos0 + last, m, n_entries), PF_TILE);
+      }
+      sa.total_steps = per_seq * B;
+      if (per_seq > (1ll << 31) - 1 || sa.total_steps > (1ll << 40))
+        return fail(CSA2_ERR_UNSUPPORTED, "indexer: problem too large for one call");
+      static std::atomic<int> pf_sms[64];   // SMs per device once the attribute is set
+      int dev = 0;
+      cudaError_t e0 = cudaGetDevice(&dev);
+      if (e0 == cudaSuccess && (dev < 0 || dev >= 64)) return fail(CSA2_ERR_UNSUPPORTED, "indexer: device id");
+      int sms = e0 == cudaSuccess ? pf_sms[dev].load(std::memory_order_acquire) : 0;
+      if (e0 == cudaSuccess && sms == 0) {
+        e0 = cudaFuncSetAttribute(score_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PF_SMEM));
+        if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e0 == cudaSuccess) pf_sms[dev].store(sms, std::memory_order_release);
+      }
+      if (e0 != cudaSuccess) return cuda_fail(e0, "indexer: prefill scorer attributes");
+      CUtensorMap map2;
+      memset(&map2, 0, sizeof(map2));
+      if (!make_codes_map(&map2, codes, (long long)B * n_cap, 2, 2))
+        return fail(CSA2_ERR_CUDA, "indexer: code tensor map");
+      uint8_t* qimg = qprep;
+      uint8_t* qsc = qprep + size_t(rows + PF_QG) * SU_Q_BYTES;
+      if (sa.total_steps > 0) {
+        const long long n_items = (long long)rows * 32, q_ctas = (n_items + 3) / 4;
+        QPrepOut qo{qimg, SU_Q_BYTES, qsc, 128u, 1};
+        CSA2_LAUNCH("q_prep launch", q_prep_kernel, unsigned(q_ctas < 4096 ? q_ctas : 4096), 128, 0, st, sa,
+                    qo, prefix, n_items);
+        note_launch();
+        const long long grid = sa.total_steps < sms ? sa.total_steps : sms;
+        CSA2_LAUNCH("score_prefill launch", score_prefill_kernel, unsigned(grid), PF_T, PF_SMEM, st, sa,
+                    (const uint8_t*)qimg, (const uint8_t*)qsc, G, map2);
+        note_launch();
+      }
+    } else if (umma_ok) {
       long long per_seq = 0;   // steps of one sequence's Tq rows (same formula as the device)
       for (int i = 0; i < Tq; ++i)
         per_seq += row_steps(i, q_pos0, m, n_entries, int(row_len), cand != nullptr, blockmax_out != nullptr);
@@ -1146,8 +1466,9 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                    make_codes_map(&map4, codes, (long long)B * n_cap, 4);
       if (sa.total_steps > 0) {
         const long long n_items = (long long)rows * 32, q_ctas = (n_items + 3) / 4;
+        QPrepOut qo{qprep, SU_QROW_BYTES, qprep + SU_Q_BYTES, SU_QROW_BYTES, 0};
         CSA2_LAUNCH("q_prep launch", q_prep_kernel, unsigned(q_ctas < 4096 ? q_ctas : 4096), 128, 0, st, sa,
-                    qprep, prefix, n_items);
+                    qo, prefix, n_items);
         note_launch();
         const long long grid = sa.total_steps < n_slots ? sa.total_steps : n_slots;
         CSA2_LAUNCH("score_fp4 launch", score_fp4_kernel, unsigned(grid), SU_T, SU_SMEM, st, sa, map1, map4);

@@ -287,6 +287,37 @@ def test_indexer_full_parity(B, Tq, q_pos0, n_entries, m, k):
     assert swaps <= max(1, B * Tq // 50)
 
 
+@pytest.mark.parametrize("B,Tq,q_pos0,n_entries,m,k", [
+    (2, 301, 0, 150, 2, 64),        # causal prefill, two sequences, last group of 4 ragged
+    (1, 1030, 0, 515, 2, 128),      # several 128-key tiles, ragged tile and group
+    (2, 77, 1000, 538, 2, 256),     # a later prefill chunk (q_pos0 > 0), k above the early rows
+    (1, 200, 0, 200, 1, 64),        # m = 1
+])
+def test_indexer_prefill_groups_parity(B, Tq, q_pos0, n_entries, m, k):
+    # Prefill calls without block maxima take the grouped scorer (four queries per key
+    # tile); every visible score and every top-k row is checked against the oracle.
+    ops = _ops()
+    seed = 90 + n_entries + Tq
+    n_cap = -(-n_entries // 64) * 64 + 64        # a multiple of 64: the tensor-map path
+    qi, qi64, w, w64, codes, scales = _indexer_inputs(seed, B, Tq, n_cap)
+    scores = torch.full((B, Tq, n_entries), np.nan, dtype=torch.float32, device="cuda")
+    topk = ops.indexer_score_topk(qi, w, q_pos0, Hp.to_dev(codes, torch.uint8),
+                                  Hp.to_dev(scales, torch.uint8), n_entries, m, k, scores_out=scores)
+    torch.cuda.synchronize()
+    _ok()
+    topk, scores = topk.cpu().numpy(), scores.cpu().numpy()
+    swaps = 0
+    for b in range(B):
+        for i in range(Tq):
+            nv = R.n_visible(q_pos0 + i, m, n_entries)
+            so = _oracle_scores(qi64[b, i], w64[b, i], codes[b], scales[b], nv)
+            if nv:
+                scale_row = np.max(np.abs(so))
+                assert np.max(np.abs(scores[b, i, :nv] - so)) <= 1e-5 * max(scale_row, 1e-3), f"scores {b},{i}"
+            swaps += Hp.check_topk_row(topk[b, i], so, np.ones(nv, bool), k, f"row {b},{i}")
+    assert swaps <= max(1, B * Tq // 50)
+
+
 def test_indexer_non_staged_no_scores_out_uses_workspace():
     ops = _ops()
     B, n_entries, k = 2, 40000, 512

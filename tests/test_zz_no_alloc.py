@@ -85,14 +85,16 @@ def test_noalloc_pool_mode_and_size_limit(lib):
     assert st == 2 and b"16777216" in lib.csa2_last_error_message()
 
 
-def test_noalloc_at_its_exact_limit(lib):
-    # The largest call the array admits (its workspace size equals the array's size
-    # exactly) runs and matches the workspace entry point.
+def test_noalloc_at_its_limit(lib):
+    # The largest call the array admits (one entry more would be refused) runs and
+    # matches the workspace entry point.
     from compressed_sparse_attention_04_gb300 import ops
+    from test_abi_host import _noalloc_limit_entries
     B, k, blk = 4, 512, 64
     cap = lib.csa2_indexer_noalloc_max_scratch_bytes()
-    n_entries = 826080
-    assert lib.csa2_indexer_workspace_size(B, 1, n_entries, 0, blk, 0) == cap
+    n_entries = _noalloc_limit_entries(lib, B, blk)   # the longest rows the array admits
+    assert lib.csa2_indexer_workspace_size(B, 1, n_entries, 0, blk, 0) <= cap
+    assert lib.csa2_indexer_workspace_size(B, 1, n_entries + 1, 0, blk, 0) > cap
     qi, w, codes, scales = _inputs(33, B, n_entries)
     ref = ops.indexer_score_topk(qi, w, n_entries - 1, codes, scales, n_entries, 1, k, blk=blk)
     got = torch.full((B, 1, k), -7, dtype=torch.int32, device="cuda")
