@@ -399,6 +399,205 @@ def run_indexer_prefill(args):
     return 0
 
 
+PREFILL = {
+    # the 16384-token encoder macro-group: 1 Full (m = 2) + 5 Reuse layers, 64 heads, top-512
+    "prefill16k": dict(B=1, T=16384, hidden=4096, m=2, k=512, H=64, window=128, n_reuse=5),
+    # one Full layer over 1024 tokens, 16 heads, top-128
+    "prefill1k": dict(B=1, T=1024, hidden=4096, m=2, k=128, H=16, window=128, n_reuse=0),
+}
+
+
+def prefill_flops(wl):
+    """Algorithmic work of one prefill pass: the compressor's projections (bf16), the
+    indexer's causal FP4 products, every layer's attention (S and P V, bf16)."""
+    T, m, k, W, H, hid = wl["T"], wl["m"], wl["k"], wl["window"], wl["H"], wl["hidden"]
+    N = T // m
+    comp = 2.0 * wl["B"] * T * hid * 512 * (2 if m == 2 else 1)
+    pairs = sum(min((t + 1) // m, N) for t in range(T)) * wl["B"]
+    idx = pairs * 32 * 128 * 2.0
+    rows = sum(min(k, min((t + 1) // m, N)) + min(W, t + 1) for t in range(T)) * wl["B"]
+    attn = (1 + wl["n_reuse"]) * rows * 4.0 * H * 512
+    return {"compress": comp, "indexer_scores": idx, "sparse_attn": attn, "causal_pairs": pairs}
+
+
+def fp4_peak_tflops():
+    """Dense FP4 rate of this GPU from the library's tensor-rate probe (M 128 x N 256)."""
+    import ctypes as C
+    from compressed_sparse_attention_04_gb300 import build
+    lib = C.CDLL(os.path.join(os.path.dirname(build.__file__), "peak", "libcsa2_peak.so"))
+    f = lib.csa2peak_mxf4
+    f.argtypes = [C.c_int, C.c_int, C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_double)]
+    tf, ms = C.c_double(), C.c_double()
+    rc = f(128, 256, 8192, C.byref(tf), C.byref(ms))
+    return tf.value if rc == 0 else None
+
+
+def time_oracle_prefill(wl, n_sample=32, seed=78):
+    """The float64 oracle on the same prefill, timed on a bounded sample: the Full layer's
+    compressor and index keys over every token, then the indexer + top-k + attention of
+    n_sample queries spread over the sequence, and one Reuse layer's attention for the same
+    queries; per-query costs are scaled to all queries and all Reuse layers."""
+    import numpy as np
+    from oracle import csa2_ref as R
+    rng = np.random.default_rng(seed)
+    T, m, k, W, H, hid = wl["T"], wl["m"], wl["k"], wl["window"], wl["H"], wl["hidden"]
+    x = rng.standard_normal((1, T, hid))
+    w_kv, w_gate = rng.standard_normal((512, hid)) * 0.02, rng.standard_normal((512, hid)) * 0.02
+    w_ik = rng.standard_normal((128, 512)) * 0.02
+    t0 = time.perf_counter()
+    kv, pre = R.compress(x, w_kv, w_gate if m == 2 else None, np.ones(512), m, 0)
+    N = kv.shape[1]
+    kq = R.index_k(pre, w_ik, np.broadcast_to(m * np.arange(N), (1, N)))
+    codes, scales = R.index_k_quant(kq)
+    k_hat = R.fp4.dequantize_rows(codes, scales)[0]
+    kv_b = R.bf16_to_f64(R.f64_to_bf16_bits(kv))[0]
+    t_build = time.perf_counter() - t0
+    swa = rng.standard_normal((T, 512))
+    qs = [int(v) for v in np.linspace(T // 8, T - 1, n_sample)]
+    t_full = t_reuse = 0.0
+    for t in qs:
+        q_idx = rng.standard_normal((32, 128)) * 1.28
+        w = rng.standard_normal(32) * 1.28
+        q = rng.standard_normal((H, 512)) * 1.28
+        t1 = time.perf_counter()
+        nv = R.n_visible(t, m, N)
+        sc = R.indexer_scores(R.quant_query(q_idx), w, k_hat[:nv])
+        sel = R.topk(sc, np.ones(nv, dtype=bool), k)
+        R.sparse_attention(q, R.attention_rows(kv_b, sel, swa, 0, t, W))
+        t2 = time.perf_counter()
+        R.sparse_attention(q, R.attention_rows(kv_b, sel, swa, 0, t, W))
+        t3 = time.perf_counter()
+        t_full += t2 - t1
+        t_reuse += t3 - t2
+    total = t_build + T / n_sample * (t_full + wl["n_reuse"] * t_reuse)
+    return total, (f"Full layer compressor + index keys over all {T} tokens timed in full "
+                   f"({t_build:.2f} s); indexer + top-k + attention of {n_sample} queries spread "
+                   f"over the sequence and one Reuse layer's attention for them, scaled to {T} "
+                   f"queries and {wl['n_reuse']} Reuse layers (extrapolated)")
+
+
+def run_prefill(args):
+    """One prefill pass through the runner (a Full layer and its Reuse layers): tokens/s,
+    the per-stage times, and each contraction's rate against its tensor peak.  One JSON
+    line; the decode step stays the bench line."""
+    import numpy as np
+    import torch
+    import ctypes as C
+    from compressed_sparse_attention_04_gb300 import build, ops
+    from synth import gpu as sg
+    build.build_all()
+    wl = PREFILL[args.workload]
+    B, T, hid, m, k, H, W, n_re = (wl[x] for x in ("B", "T", "hidden", "m", "k", "H", "window", "n_reuse"))
+    n_layers = 1 + n_re
+    dev = torch.device("cuda", 0)
+    kv_src, idx_src, ratio = [0] * n_layers, [0] * n_layers, [m] + [0] * n_re
+    runner = ops.Runner(kv_src, idx_src, ratio, 64, 64)
+    params = ops.Runner.params(B, T, 0, H, hid, k, W)
+    N = T // m
+    gs = []
+    for l in range(n_layers):
+        s = 7000 + l
+        g = dict(q=sg.fill_normal(torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=dev), s, 5, 0, 1.28),
+                 swa_kv=sg.fill_normal(torch.empty(B, T, 512, dtype=torch.bfloat16, device=dev), s, 8),
+                 swa_len=T, swa_pos0=0, out=torch.empty(B, T, H, 512, dtype=torch.bfloat16, device=dev))
+        if l == 0:
+            g.update(x=sg.fill_normal(torch.empty(B, T, hid, dtype=torch.bfloat16, device=dev), s, 1),
+                     w_kv=sg.fill_normal(torch.empty(512, hid, dtype=torch.bfloat16, device=dev), s, 2, 0, 0.02),
+                     w_gate=sg.fill_normal(torch.empty(512, hid, dtype=torch.bfloat16, device=dev), s, 3, 0, 0.02)
+                     if m == 2 else None,
+                     w_ik=sg.fill_normal(torch.empty(128, 512, dtype=torch.bfloat16, device=dev), s, 4, 0, 0.02),
+                     norm_w=torch.ones(512, dtype=torch.float32, device=dev),
+                     kv_cache=torch.empty(B, N, 512, dtype=torch.bfloat16, device=dev),
+                     idx_codes=torch.empty(B, N, 64, dtype=torch.uint8, device=dev),
+                     idx_scales=torch.empty(B, N, 4, dtype=torch.uint8, device=dev),
+                     n_cap=N, x_tokens=T, x_pos0=0,
+                     q_idx=sg.fill_normal(torch.empty(B, T, 32, 128, dtype=torch.bfloat16, device=dev), s, 6, 0, 1.28),
+                     w_idx=sg.fill_normal(torch.empty(B, T, 32, dtype=torch.float32, device=dev), s, 7, 0, 1.28))
+        gs.append(g)
+    ios = [ops.layer_io(**g) for g in gs]
+    ws = torch.empty(runner.workspace_size(params, T, N) + 256, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        runner.step(params, ios, ws)
+    torch.cuda.synchronize()
+    assert ops.last_device_status() == 0
+    lib = ops.L.load()
+    n_ev = n_layers * 6 * 2
+    K = max(args.steps, 3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K)]
+    for es in evs:
+        for e in es:
+            e.record(stream)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    n0 = lib.csa2_kernel_launches()
+    t0.record(stream)
+    for _ in range(K):
+        runner.step(params, ios, ws)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    launches = lib.csa2_kernel_launches() - n0
+    ms = t0.elapsed_time(t1) / K
+    stage_ms = [0.0] * 6
+    for i in range(K):
+        h = (C.c_void_p * n_ev)(*[e.cuda_event for e in evs[i]])
+        ops.L.check(lib.csa2_runner_set_timing(runner._h, h, n_ev), "set_timing")
+        runner.step(params, ios, ws)
+    lib.csa2_runner_set_timing(runner._h, None, 0)
+    torch.cuda.synchronize()
+    assert ops.last_device_status() == 0
+    for i in range(K):
+        for l in range(n_layers):
+            for st_ in range(6):
+                a, b = evs[i][(l * 6 + st_) * 2], evs[i][(l * 6 + st_) * 2 + 1]
+                if (l > 0 and st_ < 5):
+                    continue
+                stage_ms[st_] += a.elapsed_time(b) / K
+    fl = prefill_flops(wl)
+    bf16_peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        bf16_peak = 1900.0
+    fp4_meas = fp4_peak_tflops()
+    fp4_recipe = bf16_peak * 6.0
+
+    def rate(name, flops, peak):
+        t = stage_ms[STAGE_NAMES.index(name)]
+        tf = flops / (t * 1e-3) / 1e12 if t > 0 else None
+        return {"tflops": tf, "peak_tflops": peak, "frac": (tf / peak) if (tf and peak) else None,
+                "ms": t, "gflop": flops / 1e9}
+
+    tensor = {"compress": rate("compress", fl["compress"], bf16_peak),
+              "indexer_scores": rate("indexer_scores", fl["indexer_scores"], fp4_meas),
+              "sparse_attn": rate("sparse_attn", fl["sparse_attn"], bf16_peak)}
+    tensor["indexer_scores"]["frac_of_recipe_peak"] = (
+        tensor["indexer_scores"]["tflops"] / fp4_recipe if tensor["indexer_scores"]["tflops"] else None)
+    cpu = None
+    if not args.no_cpu_baseline:
+        tot, desc = time_oracle_prefill(wl)
+        cpu = {"value": B * T / tot, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": desc}
+    line = {"metric": f"CSA2 prefill tokens/s ({T}-token group, 1 Full + {n_re} Reuse layers)",
+            "value": B * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"csa2_prefill_{n_layers}layer_T{T}", "batch": B, "tokens": T,
+                       "hidden": hid, "m": m, "topk": k, "heads": H, "window": W,
+                       "l2": f"no flush: a pass reads {6 * T * H * 512 * 2 / 1e9:.1f} GB of queries alone"},
+            "stage_ms_per_step": {STAGE_NAMES[i]: stage_ms[i] for i in range(6)},
+            "tensor": tensor, "fp4_peak_tflops": {"measured": fp4_meas, "recipe_bf16x6": fp4_recipe},
+            "causal_pairs": fl["causal_pairs"], "gpu_launches": launches // K, "clocks": ck,
+            "cpu_baseline": cpu}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_attention_formats(args):
     """The decode attention launch at the headline shape (64 rows x (512 entries + 128 window
     rows) x 64 heads, 64K-entry caches) with each stored format: bf16, FP8 window rows, FP4
@@ -745,7 +944,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode40")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(PREFILL), default="decode40")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--indexer-prefill", action="store_true",
@@ -763,6 +962,10 @@ def main():
         return run_indexer_prefill(args)
     if args.attention_formats:
         return run_attention_formats(args)
+    if args.workload in PREFILL:
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0   # one GPU: a prefill pass is not split over ranks
+        return run_prefill(args)
     wl = WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
