@@ -45,7 +45,18 @@ WORKLOADS = {
     # (64 rows x (512 + 128) rows x 64 heads) with a few GB of caches, small enough for a
     # full profiler capture (not a bench line)
     "b64_ctx8k": dict(B=64, C=8192, H=64, hidden=4096, k=512, window=128, blk=64, nb=64),
+    # the decoder group alone: a Full layer (m = 1) building the HSI pool, one Reindex layer
+    # rescoring it, two Reuse layers; 32 sequences at 65536 entries
+    "decoder_group": dict(B=32, C=65536, H=64, hidden=4096, k=512, window=128, blk=64, nb=64,
+                          pattern="decoder_group"),
+    # one encoder Full layer (m = 2) at 1 048 576 tokens of context: 524 288 entries, 4 sequences
+    "long1m": dict(B=4, C=1048576, H=64, hidden=4096, k=512, window=128, blk=64, nb=64,
+                   pattern="encoder_full"),
 }
+
+# Layer patterns: (kv_source_layer_ids, index_source_layer_ids, m per layer, 0 for a layer
+# that compresses nothing).
+PATTERN_NAMES = {"stack40": "40layer", "decoder_group": "decoder_group", "encoder_full": "full_layer"}
 
 
 def peaks():
@@ -143,8 +154,15 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- GPU setup
-def layer_tables():
-    """The 40-layer Full/Reindex/Reuse pattern (kv_source_layer_ids, index_source_layer_ids, m)."""
+def layer_tables(pattern="stack40"):
+    """A workload's Full/Reindex/Reuse pattern (kv_source_layer_ids, index_source_layer_ids, m):
+    the 40-layer stack, the decoder group (Full m = 1, Reindex, 2 Reuse) or one encoder Full
+    layer (m = 2)."""
+    if pattern == "decoder_group":
+        return [0, 0, 0, 0], [0, 1, 1, 1], [1, 0, 0, 0]
+    if pattern == "encoder_full":
+        return [0], [0], [2]
+    assert pattern == "stack40", pattern
     kv, idx, ratio = [], [], []
     cur_kv = cur_idx = -1
     for l in range(40):
@@ -172,9 +190,13 @@ class Stack:
         self.wl = wl
         B, C, H, hid, W = wl["B"], wl["C"], wl["H"], wl["hidden"], wl["window"]
         self.t = C - 1
-        self.kv_src, self.idx_src, self.ratio = layer_tables()
+        self.kv_src, self.idx_src, self.ratio = layer_tables(wl.get("pattern", "stack40"))
+        self.n_layers = len(self.kv_src)
         self.runner = ops.Runner(self.kv_src, self.idx_src, self.ratio, wl["blk"], wl["nb"])
-        self.modes = [self.runner.mode(l) for l in range(40)]
+        self.modes = [self.runner.mode(l) for l in range(self.n_layers)]
+        # Full layers whose block maxima feed a Reindex layer's candidate pool
+        self.builds_pool = [any(self.modes[j] == 2 and self.kv_src[j] == l for j in range(self.n_layers))
+                            for l in range(self.n_layers)]
         self.params = ops.Runner.params(B, 1, self.t, H, hid, wl["k"], W)
         self.layers = []
         dev = device
@@ -184,7 +206,7 @@ class Stack:
         gemm_ws = torch.empty(ops.L.load().csa2_compress_workspace_size(B, Tc, hid, 2) + 256,
                               dtype=torch.uint8, device=dev)
         pre_buf = torch.empty(B * Tc * 512, dtype=torch.float32, device=dev)
-        for l in range(40):
+        for l in range(self.n_layers):
             s = seed_base + l
             md = self.modes[l]
             g = {}
@@ -239,6 +261,18 @@ class Stack:
                     for l, g in enumerate(self.layers) if "x" in g)
         nbytes = self.runner.workspace_size(self.params, 2, max_n)
         self.ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=dev)
+        # a step that moves less than 4x the L2 (129 MB) could find the previous step's rows
+        # there: such workloads overwrite a 512 MB buffer before every timed step, outside
+        # the step's events
+        self.step_bytes = sum(self.stage_bytes(l, s) for l in range(self.n_layers) for s in range(6))
+        self.flush_buf = (torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+                          if self.step_bytes < 4 * 129e6 else None)
+
+    def flush_l2(self, stream=None):
+        if self.flush_buf is not None:
+            import torch
+            with torch.cuda.stream(stream or torch.cuda.current_stream()):
+                self.flush_buf.fill_(1)
 
     def step(self, stream=None):
         self.runner.step(self.params, self.ios, self.ws, stream)
@@ -267,7 +301,7 @@ class Stack:
             if stage == 3:
                 return B * N * 4 + B * k * 4
             if stage == 4:
-                return B * (N // wl["blk"]) * 4 + B * wl["nb"] * 4
+                return B * (N // wl["blk"]) * 4 + B * wl["nb"] * 4 if self.builds_pool[l] else 0
         if md == 2:
             pool = wl["nb"] * wl["blk"]
             if stage == 2:
@@ -283,11 +317,11 @@ def oracle_sample(wl, n_seq=1, seed=77):
     NumPy generator: this leg only times the oracle)."""
     import numpy as np
     rng = np.random.default_rng(seed)
-    kv_src, idx_src, ratio = layer_tables()
+    kv_src, idx_src, ratio = layer_tables(wl.get("pattern", "stack40"))
     C, H, hid, W = wl["C"], wl["H"], wl["hidden"], wl["window"]
     t = C - 1
     layers = []
-    for l in range(40):
+    for l in range(len(kv_src)):
         d = {"q": rng.standard_normal((n_seq, 1, H, 512)) * 1.28,
              "swa": rng.standard_normal((n_seq, W, 512)), "swa_pos0": t - W + 1}
         if idx_src[l] == l:
@@ -347,10 +381,11 @@ def job_throughput(batch, world, ms):
 # ----------------------------------------------------------------------------- main arms
 def workload_config(wl, world):
     """The `config` object both arms print: the workload's name and shape."""
-    return {"workload": f"csa2_decode_40layer_b{wl['B']}_ctx{wl['C']}" +
+    n_layers = len(layer_tables(wl.get("pattern", "stack40"))[0])
+    return {"workload": f"csa2_decode_{PATTERN_NAMES[wl.get('pattern', 'stack40')]}_b{wl['B']}_ctx{wl['C']}" +
                         (f"_hsi{wl['nb']}x{wl['blk']}" if wl["blk"] != 64 else "") +
                         ("_fp4kv_fp8swa" if wl.get("stored") else ""),
-            "batch": wl["B"], "context": wl["C"], "layers": 40, "heads": wl["H"], "topk": wl["k"],
+            "batch": wl["B"], "context": wl["C"], "layers": n_layers, "heads": wl["H"], "topk": wl["k"],
             "window": wl["window"], "hsi": f"{wl['nb']}x{wl['blk']}",
             "kv_format": "fp4 main kv, fp8 window rows" if wl.get("stored") else "bf16",
             "l2": "no flush: each step reads ~3.5 GB of caches (> 129 MB L2)",
@@ -578,6 +613,16 @@ def run_prefill(args):
               "sparse_attn": rate("sparse_attn", fl["sparse_attn"], bf16_peak)}
     tensor["indexer_scores"]["frac_of_recipe_peak"] = (
         tensor["indexer_scores"]["tflops"] / fp4_recipe if tensor["indexer_scores"]["tflops"] else None)
+    # dominant kernel against its tensor peak: FLOPs per launch / mean launch time
+    dom = max(tensor, key=lambda n: tensor[n]["ms"])
+    n_launch = n_layers if dom == "sparse_attn" else 1
+    roof = {"bound": "tensor", "kernel": dom, "achieved": tensor[dom]["tflops"],
+            "peak": tensor[dom]["peak_tflops"], "peak_kind": "measured", "unit": "TFLOP/s",
+            "frac": tensor[dom]["frac"], "traffic": None, "launches_per_step": n_launch,
+            "flops_per_launch": tensor[dom]["gflop"] * 1e9 / n_launch}
+    e2e = None
+    if not args.no_e2e:
+        e2e = prefill_e2e(runner, params, gs, ws, stream, args, B * T)
     cpu = None
     if not args.no_cpu_baseline:
         tot, desc = time_oracle_prefill(wl)
@@ -592,10 +637,55 @@ def run_prefill(args):
                        "l2": f"no flush: a pass reads {6 * T * H * 512 * 2 / 1e9:.1f} GB of queries alone"},
             "stage_ms_per_step": {STAGE_NAMES[i]: stage_ms[i] for i in range(6)},
             "tensor": tensor, "fp4_peak_tflops": {"measured": fp4_meas, "recipe_bf16x6": fp4_recipe},
-            "causal_pairs": fl["causal_pairs"], "gpu_launches": launches // K, "clocks": ck,
-            "cpu_baseline": cpu}
+            "roofline": roof, "causal_pairs": fl["causal_pairs"], "gpu_launches": launches // K,
+            "clocks": ck, "cpu_baseline": cpu, "e2e": e2e}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def prefill_e2e(runner, params, gs, ws, stream, args, tokens):
+    """The prefill pass through the C ABI with host buffers: each step copies every layer's
+    inputs (hidden states, queries, window rows, indexer queries and weights) from pinned host
+    memory, runs the pass and reads the last layer's output back; copies and pass in order on
+    one stream, all inside the timed region."""
+    import torch
+    from compressed_sparse_attention_04_gb300 import ops
+    keys = ("x", "q", "swa_kv", "q_idx", "w_idx")
+    pairs, h2d = [], 0
+    for g in gs:
+        for key in keys:
+            if key in g and g[key] is not None:
+                h = torch.empty_like(g[key], device="cpu").pin_memory()
+                h.copy_(g[key])
+                pairs.append((g[key], h))
+                h2d += g[key].numel() * g[key].element_size()
+    out_h = torch.empty_like(gs[-1]["out"], device="cpu").pin_memory()
+    d2h = out_h.numel() * out_h.element_size()
+    ios = [ops.layer_io(**g) for g in gs]
+
+    def one():
+        for d, h in pairs:
+            d.copy_(h, non_blocking=True)
+        runner.step(params, ios, ws, stream.cuda_stream)
+        out_h.copy_(gs[-1]["out"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    K = max(args.steps, 3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    assert ops.last_device_status() == 0
+    ms = max(e0.elapsed_time(e1), wall * 1e3) / K
+    return {"value": tokens / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelined": "no: uploads, pass and read-back in order on one stream"}
 
 
 def run_attention_formats(args):
@@ -695,7 +785,7 @@ def run_ours(args, wl, rank, world, local_rank):
     assert ops.last_device_status() == 0, "device-side check fired during warm-up"
 
     # per-stage timing events, one array per timed step
-    n_ev = 40 * 6 * 2
+    n_ev = st.n_layers * 6 * 2
     import ctypes as C
     lib = ops.L.load()
     ev_sets, handles = [], []
@@ -737,27 +827,36 @@ def run_ours(args, wl, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush = st.flush_buf is not None
+        # back to back: one event pair around the K steps; with an L2 flush before every
+        # step: one pair per step, the flush outside it
+        n_pairs = args.steps if flush else 1
+        t0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_pairs)]
+        t1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_pairs)]
         n_launch0 = lib.csa2_kernel_launches()
-        if graphs:
-            t0.record(stream)
-            for g in graphs[0]:
-                g.replay()
-            t1.record(stream)
-            launches = graphs[1] * args.steps
-        else:
-            t0.record(stream)
-            for i in range(args.steps):
+        if not flush:
+            t0[0].record(stream)
+        for i in range(args.steps):
+            if flush:
+                st.flush_l2(stream)
+                t0[i].record(stream)
+            if graphs:
+                graphs[0][i].replay()
+            else:
                 if with_events:
                     ops.L.check(lib.csa2_runner_set_timing(st.runner._h, handles[i], n_ev), "set_timing")
                 st.step()
-            t1.record(stream)
-            launches = lib.csa2_kernel_launches() - n_launch0
+            if flush:
+                t1[i].record(stream)
+        if not flush:
+            t1[0].record(stream)
+        launches = graphs[1] * args.steps if graphs else lib.csa2_kernel_launches() - n_launch0
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         lib.csa2_runner_set_timing(st.runner._h, None, 0)
-        ms_ = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+        total = sum(a.elapsed_time(b) for a, b in zip(t0, t1))
+        ms_ = max_over_ranks(total / args.steps, world, dev)
         assert ops.last_device_status() == 0, "device-side check fired during the timed steps"
         return ms_, launches
 
@@ -777,7 +876,7 @@ def run_ours(args, wl, rank, world, local_rank):
     stage_launches = [0] * 6
     for i in range(args.steps):
         evs = ev_sets[i]
-        for l in range(40):
+        for l in range(st.n_layers):
             for s in range(6):
                 a, b = evs[(l * 6 + s) * 2], evs[(l * 6 + s) * 2 + 1]
                 nb = st.stage_bytes(l, s)
@@ -802,7 +901,7 @@ def run_ours(args, wl, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline and not wl.get("stored"):
         reps, total = time_oracle(wl)
         cpu = {"value": reps / total, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{reps} x one sequence of the decode step (all 40 layers, full-size "
+               "sample": f"{reps} x one sequence of the decode step (all {st.n_layers} layers, full-size "
                          "caches, cache building excluded as on the GPU); NumPy float64, BLAS threads "
                          "= host cores"}
     if rank != 0:
@@ -812,6 +911,10 @@ def run_ours(args, wl, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(wl, world),
+                       l2=(f"no flush: each step moves {st.step_bytes / 1e9:.2f} GB (> 4 x the 129 MB L2)"
+                           if st.flush_buf is None else
+                           f"each step moves {st.step_bytes / 1e6:.0f} MB: a 512 MB buffer is written "
+                           "before every timed step, outside its events"),
                        launch="cuda_graph" if args.graph else "direct",
                        timing="headline pass without per-stage events; stage times from a second pass"),
         "roofline": {"bound": "hbm", "kernel": STAGE_NAMES[dom], "achieved": achieved, "peak": peak,

@@ -15,6 +15,7 @@ MODE_SWA, MODE_FULL, MODE_REINDEX, MODE_REUSE = range(4)
 STAGES = 6   # compress, index_k, scores, top-k, HSI, attention
 
 vp, i32, f32, sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+u32 = C.c_uint
 
 
 class LayerIO(C.Structure):
@@ -59,6 +60,8 @@ SIGNATURES = {
     "csa2_indexer_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
     "csa2_indexer_score_topk": (i32, [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, vp, i32,
                                       i32, i32, vp, vp, vp, vp, sz, vp]),
+    "csa2_indexer_score_topk_bounded": (i32, [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32,
+                                              vp, vp, sz, u32, i32, vp]),
     "csa2_indexer_noalloc_max_scratch_bytes": (sz, []),
     "csa2_indexer_score_topk_noalloc": (i32, [vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, vp,
                                               i32, i32, i32, vp, vp, vp]),

@@ -100,12 +100,14 @@ using err_reader = unsigned (*)();
 void register_err_reader(err_reader f);
 
 // csa2_indexer_score_topk with two optional events recorded between the scoring
-// launch and the top-k launch (used by the runner's per-stage timing).
+// launch and the top-k launch (used by the runner's per-stage timing), and the
+// tensor-core decode scorer's wait bound and stall switch (csa2_indexer_score_topk_bounded).
 int indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
                  const uint8_t* codes, const uint8_t* scales, int n_cap, int n_entries, int m,
                  const int32_t* cand, int nb, int blk, int k, int32_t* topk_out,
                  float* blockmax_out, float* scores_out, void* workspace, size_t ws_bytes,
-                 void* stream, cudaEvent_t ev_score_end, cudaEvent_t ev_topk_begin);
+                 void* stream, cudaEvent_t ev_score_end, cudaEvent_t ev_topk_begin,
+                 unsigned wait_limit = 0, int stall = 0, int* used_bounded = nullptr);
 
 // Entry positions visible to query position t (entry s covers tokens s*m..s*m+m-1).
 __host__ __device__ inline int n_visible(long long t, int m, int n_entries) {

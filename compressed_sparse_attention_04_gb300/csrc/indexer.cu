@@ -59,6 +59,9 @@ struct ScoreArgs {
   long long total_steps;   // B * prefix[Tq]
   float* bm64;             // [rows][nb64] maxima of 64-key blocks for the top-k threshold, or null
   int nb64;
+  uint32_t wait_limit;     // (tensor-core decode scorer) polls per device wait
+  int stall;               // (tensor-core decode scorer) the copy thread first waits on a
+                           // barrier that nothing completes, so that every wait runs out
 };
 
 __global__ void __launch_bounds__(SC_T) score_kernel(ScoreArgs a) {
@@ -398,9 +401,10 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
   uint32_t* Ss = reinterpret_cast<uint32_t*>(base + SU_STAGES * SU_STAGE_BYTES);   // SU_STAGES x 256
   uint8_t* Qb = base + SU_STAGES * (SU_STAGE_BYTES + SU_STEP * 4);  // 2 x query image + scales
   __shared__ __align__(8) uint64_t a_empty[SU_STAGES], land[SU_STAGES], sf_ready[SU_STAGES];
-  __shared__ __align__(8) uint64_t d_full[SU_ND], d_empty[SU_ND], q_empty[2];
+  __shared__ __align__(8) uint64_t d_full[SU_ND], d_empty[SU_ND], q_empty[2], never;
   __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t polls = a.wait_limit;
   const long long S = a.total_steps;
   const long long s_begin = S * blockIdx.x / gridDim.x, s_end = S * (blockIdx.x + 1) / gridDim.x;
   const int L = int(s_end - s_begin);
@@ -420,6 +424,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
     }
     umma::mbar_init(&q_empty[0], 1);
     umma::mbar_init(&q_empty[1], 1);
+    umma::mbar_init(&never, 1);
     umma::mbar_fence_init();
   }
   if (warp == 0) umma::tmem_alloc(&tmem_slot, SU_TMEM_COLS);
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
         if (g > 0) ci.next(a);
         const int s2 = g % SU_STAGES;
         if (g >= SU_STAGES &&
-            !umma::mbar_wait(&a_empty[s2], ((g / SU_STAGES) - 1) & 1, &d_err_indexer)) return false;
+            !umma::mbar_wait(&a_empty[s2], ((g / SU_STAGES) - 1) & 1, &d_err_indexer, polls)) return false;
         const int row = ci.row(a);
         const int n_vis = n_visible((long long)a.q_pos0 + ci.i, a.m, a.n_entries);
         const int limit = pool ? a.row_len : n_vis;
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
         umma::fence_proxy_async();
         umma::mbar_arrive(&land[s2]);
       }
-      if (!umma::mbar_wait(&land[s2], (g / SU_STAGES) & 1, &d_err_indexer)) { ok = false; break; }
+      if (!umma::mbar_wait(&land[s2], (g / SU_STAGES) & 1, &d_err_indexer, polls)) { ok = false; break; }
       if (new_row) {   // query scale factors: heads 0..31 in word 0 of each 4-column group
         const uint32_t qs = reinterpret_cast<const uint32_t*>(Qb + (cs.k & 1) * SU_QROW_BYTES + SU_Q_BYTES)[lane];
         const uint32_t v[8] = {sf_lo(qs), 0u, 0u, 0u, sf_hi(qs), 0u, 0u, 0u};
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
       const int n_vis = n_visible((long long)a.q_pos0 + ce.i, a.m, a.n_entries);
       const int limit = pool ? a.row_len : n_vis;
       const int d = g % SU_ND;
-      if (!umma::mbar_wait(&d_full[d], (g / SU_ND) & 1, &d_err_indexer)) break;
+      if (!umma::mbar_wait(&d_full[d], (g / SU_ND) & 1, &d_err_indexer, polls)) break;
       umma::fence_after();
       uint32_t v0[32], v1[32];
       umma::tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(64 * d), v0);
@@ -602,8 +607,8 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
       // predecessor, so that buffer may be refilled once they complete
       if (g > 0 && cm.next(a)) umma::commit(&q_empty[(cm.k - 1) & 1]);
       const int s2 = g % SU_STAGES, d = g % SU_ND, qb = cm.k & 1;
-      if (!umma::mbar_wait(&sf_ready[s2], (g / SU_STAGES) & 1, &d_err_indexer)) break;
-      if (!umma::mbar_wait(&d_empty[d], ((g / SU_ND) & 1) ^ 1, &d_err_indexer)) break;
+      if (!umma::mbar_wait(&sf_ready[s2], (g / SU_STAGES) & 1, &d_err_indexer, polls)) break;
+      if (!umma::mbar_wait(&d_empty[d], ((g / SU_ND) & 1) ^ 1, &d_err_indexer, polls)) break;
       umma::fence_after();
 #pragma unroll
       for (int tile = 0; tile < 2; ++tile)
@@ -626,14 +631,17 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
     const long long total_keys = (long long)a.rows / a.Tq * a.n_cap;   // B * n_cap
     StepCursor cc;
     cc.init(a, s_begin);
-    for (int g = 0; g < L; ++g) {
+    // (stall) a wait that runs out: nothing is copied, so every other role's first wait
+    // runs out too and each role leaves its loop with no copy or MMA in flight
+    const bool go = !a.stall || umma::mbar_wait(&never, 0, &d_err_indexer, polls);
+    for (int g = 0; g < L && go; ++g) {
       const bool new_row = g == 0 || cc.next(a);
       const int s2 = g % SU_STAGES;
       if (g >= SU_STAGES &&
-          !umma::mbar_wait(&a_empty[s2], ((g / SU_STAGES) - 1) & 1, &d_err_indexer)) break;
+          !umma::mbar_wait(&a_empty[s2], ((g / SU_STAGES) - 1) & 1, &d_err_indexer, polls)) break;
       const int qb = cc.k & 1;
       if (new_row && cc.k >= 2 &&
-          !umma::mbar_wait(&q_empty[qb], ((cc.k >> 1) - 1) & 1, &d_err_indexer)) break;
+          !umma::mbar_wait(&q_empty[qb], ((cc.k >> 1) - 1) & 1, &d_err_indexer, polls)) break;
       const int row = cc.row(a);
       long long blk_key[4] = {-1, -1, -1, -1};   // pool steps: the four blocks' first keys
       long long dense_key = -1;                   // dense steps: the step's first key
@@ -1296,6 +1304,26 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
                             nullptr, nullptr);
 }
 
+int csa2_indexer_score_topk_bounded(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
+                                    const uint8_t* codes, const uint8_t* scales, int n_cap,
+                                    int n_entries, int m, int k, int32_t* topk_out, void* workspace,
+                                    size_t ws_bytes, unsigned wait_limit, int stall, void* stream) {
+  if (wait_limit == 0 && stall) return csa2::fail(CSA2_ERR_INVALID_ARG, "indexer_bounded: stall needs a wait_limit");
+  // the shapes that take the tensor-core decode scorer with at least one step
+  if (Tq < 1 || Tq >= csa2::PF_MIN_TQ || n_entries < 1 || m < 1 || q_pos0 + 1 < m)
+    return csa2::fail(CSA2_ERR_UNSUPPORTED,
+                      "indexer_bounded: needs 1 <= Tq < %d and entry 0 visible to the first query",
+                      csa2::PF_MIN_TQ);
+  int used = 0;
+  const int st = csa2::indexer_impl(q_idx, w, B, Tq, q_pos0, codes, scales, n_cap, n_entries, m, nullptr,
+                                    0, 64, k, topk_out, nullptr, nullptr, workspace, ws_bytes, stream,
+                                    nullptr, nullptr, wait_limit, stall, &used);
+  if (st == CSA2_OK && !used)
+    return csa2::fail(CSA2_ERR_UNSUPPORTED,
+                      "indexer_bounded: this call does not run the tensor-core decode scorer");
+  return st;
+}
+
 }  // extern "C"
 
 namespace {
@@ -1321,7 +1349,9 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                        const uint8_t* codes, const uint8_t* scales, int n_cap, int n_entries,
                        int m, const int32_t* cand, int nb, int blk, int k, int32_t* topk_out,
                        float* blockmax_out, float* scores_out, void* workspace, size_t ws_bytes,
-                       void* stream, cudaEvent_t ev_score_end, cudaEvent_t ev_topk_begin) {
+                       void* stream, cudaEvent_t ev_score_end, cudaEvent_t ev_topk_begin,
+                       unsigned wait_limit, int stall, int* used_bounded) {
+  if (used_bounded) *used_bounded = 0;
   if (!q_idx || !w || !codes || !scales || !topk_out)
     return fail(CSA2_ERR_INVALID_ARG, "indexer: null tensor pointer");
   if (B <= 0 || Tq <= 0 || q_pos0 < 0 || m < 1 || n_entries < 0 || n_cap < n_entries ||
@@ -1376,7 +1406,8 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
   if (row_len > 0) {
     ScoreArgs sa{(const uint16_t*)q_idx, w, int(rows), Tq, q_pos0, codes, scales, n_cap,
                  n_entries, m, cand, nb, blk, n_blocks, scores, int(row_len), blockmax_out,
-                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0, qprep, prefix, 0, nullptr, nb64};
+                 int((row_len + SC_CHUNK - 1) / SC_CHUNK), 0, qprep, prefix, 0, nullptr, nb64,
+                 umma::kWaitPolls, 0};
     const bool umma_ok = !(cand || blockmax_out) || blk <= 64;
     if (umma_ok && chunked && !cand) {
       if (blockmax_out && blk == 64) {
@@ -1471,8 +1502,12 @@ int csa2::indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_p
                     qo, prefix, n_items);
         note_launch();
         const long long grid = sa.total_steps < n_slots ? sa.total_steps : n_slots;
-        CSA2_LAUNCH("score_fp4 launch", score_fp4_kernel, unsigned(grid), SU_T, SU_SMEM, st, sa, map1, map4);
+        ScoreArgs sb = sa;
+        if (wait_limit) sb.wait_limit = wait_limit;
+        sb.stall = stall;
+        CSA2_LAUNCH("score_fp4 launch", score_fp4_kernel, unsigned(grid), SU_T, SU_SMEM, st, sb, map1, map4);
         note_launch();
+        if (used_bounded) *used_bounded = 1;
       }
     } else {
       CSA2_LAUNCH("score launch", score_kernel, unsigned(rows * sa.n_chunks), SC_T, 0, st, sa);

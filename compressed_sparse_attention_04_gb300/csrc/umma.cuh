@@ -149,10 +149,12 @@ __device__ __forceinline__ bool mbar_test(void* bar, uint32_t parity) {
   return done != 0;
 }
 // Bounded wait for phase `parity` to complete.  Returns false (and sets ERR_TIMEOUT in
-// *err) when the iteration limit is reached.
-__device__ __forceinline__ bool mbar_wait(void* bar, uint32_t parity, unsigned* err) {
+// *err) when `limit` polls (default 2^24) have not seen it.
+constexpr uint32_t kWaitPolls = 1u << 24;
+__device__ __forceinline__ bool mbar_wait(void* bar, uint32_t parity, unsigned* err,
+                                          uint32_t limit = kWaitPolls) {
   uint32_t done = 0;
-  for (uint32_t it = 0; it < (1u << 24); ++it) {
+  for (uint32_t it = 0; it < limit; ++it) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"

@@ -192,6 +192,26 @@ int csa2_indexer_score_topk(const void* q_idx, const float* w, int B, int Tq, in
                             void* stream);
 
 /* ---------------------------------------------------------------------------------
+ * Stage 3 with an explicit bound on the device waits -- a diagnostic of the library's
+ * error path; the pages have no counterpart.  The same computation as
+ * csa2_indexer_score_topk for a Full layer (cand, blockmax_out and scores_out NULL),
+ * restricted to the calls that run the tensor-core decode scorer: 1 <= Tq < 64, and
+ * entry 0 visible to the first query (n_entries >= 1, q_pos0 + 1 >= m); others return
+ * CSA2_ERR_UNSUPPORTED before any launch.  Every mbarrier wait of that kernel polls at most wait_limit times
+ * (0: the library's default, 2^24) before it gives up and sets CSA2_ERR_TIMEOUT in the
+ * device error word (csa2_last_device_status reads and clears it).  stall != 0 (needs
+ * wait_limit > 0) makes the kernel's copy thread first wait on a barrier that nothing
+ * completes: no copy is issued, every other role's first wait runs out, and each CTA
+ * leaves with no copy or MMA in flight; the top-k launch that follows then selects
+ * from whatever the workspace's score area held.  The context stays usable.
+ * ------------------------------------------------------------------------------- */
+int csa2_indexer_score_topk_bounded(const void* q_idx, const float* w, int B, int Tq,
+                                    int q_pos0, const uint8_t* codes, const uint8_t* scales,
+                                    int n_cap, int n_entries, int m, int k, int32_t* topk_out,
+                                    void* workspace, size_t ws_bytes, unsigned wait_limit,
+                                    int stall, void* stream);
+
+/* ---------------------------------------------------------------------------------
  * Stage 3 without allocation.  The pages have no counterpart: this is a library
  * convenience.  Same computation, arguments and results as csa2_indexer_score_topk
  * (no scores_out, no workspace), for callers that cannot allocate device memory --

@@ -93,6 +93,18 @@ def test_indexer_and_hsi_validation(lib):
     assert call(a10=_vp(FAKE), a11=0) == L.ERR_INVALID_ARG   # nb = 0
     assert call(a10=_vp(FAKE), a11=4, a15=_vp(FAKE)) == L.ERR_INVALID_ARG  # pool + blockmax
     assert call() == L.ERR_WORKSPACE
+    # the bounded-wait diagnostic: decode-scorer shapes only, stall needs a limit; both
+    # refused before any launch
+    g = lib.csa2_indexer_score_topk_bounded
+
+    def bounded(Tq=1, q_pos0=10, m=1, wait_limit=64, stall=1):
+        return g(_vp(FAKE), _vp(FAKE), 1, Tq, q_pos0, _vp(FAKE), _vp(FAKE), 64, 32, m, 16,
+                 _vp(FAKE), _vp(0), 0, wait_limit, stall, _vp(0))
+
+    assert bounded(wait_limit=0) == L.ERR_INVALID_ARG                 # stall needs a limit
+    assert bounded(Tq=64) == L.ERR_UNSUPPORTED                        # the prefill scorer's shape
+    assert bounded(q_pos0=0, m=2) == L.ERR_UNSUPPORTED                # no visible entry
+    assert bounded() == L.ERR_WORKSPACE
     h = lib.csa2_hsi_candidates
     assert h(_vp(0), 1, 1, 0, 10, 1, 64, 4, _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
     assert h(_vp(FAKE), 1, 1, 0, 10, 1, 64, 0, _vp(FAKE), _vp(0)) == L.ERR_INVALID_ARG
@@ -245,7 +257,8 @@ def _header_prototypes():
 
 
 def test_ctypes_signatures_match_header_prototypes():
-    kind_of = {C.c_void_p: "ptr", C.c_int: "int", C.c_float: "float", C.c_size_t: "size"}
+    kind_of = {C.c_void_p: "ptr", C.c_int: "int", C.c_uint: "int", C.c_float: "float",
+               C.c_size_t: "size"}
     protos = _header_prototypes()
     assert set(protos) == set(L.SIGNATURES)
     for name, (_, argtypes) in L.SIGNATURES.items():
