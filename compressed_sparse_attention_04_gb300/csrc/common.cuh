@@ -109,6 +109,16 @@ int indexer_impl(const void* q_idx, const float* w, int B, int Tq, int q_pos0,
                  void* stream, cudaEvent_t ev_score_end, cudaEvent_t ev_topk_begin,
                  unsigned wait_limit = 0, int stall = 0, int* used_bounded = nullptr);
 
+// The compressor (csa2_compress, or csa2_compress_chunk when state is given) whose epilogue
+// also writes the new entries' indexer keys (as csa2_index_k_quant would, bit for bit) when
+// the call has few entries; *fused tells whether it did -- if not, the caller runs
+// csa2_index_k_quant on kv_pre.
+int compress_index_k(const void* x, int B, int T, int hidden, int m, int pos0, const void* w_kv,
+                     const void* w_gate, const float* norm_w, float eps, float rope_base,
+                     float* state, void* kv_cache, int n_cap, float* kv_pre, void* workspace,
+                     size_t ws_bytes, const void* w_ik, uint8_t* idx_codes, uint8_t* idx_scales,
+                     void* stream, bool* fused);
+
 // Entry positions visible to query position t (entry s covers tokens s*m..s*m+m-1).
 __host__ __device__ inline int n_visible(long long t, int m, int n_entries) {
   long long v = (t + 1) / m;

@@ -209,6 +209,42 @@ int proj_splits(int M, int K, int Nout) {
   return s;
 }
 
+// Quarter qk of key dim j of one entry: sum over inputs 128 qk .. 128 qk + 127 of
+// w_ik[j][i] * y[i], in input order; quarters 1..3 go to ipart (after a barrier that the
+// caller's quarter 0 meets), quarter 0 is returned once they are there.
+__device__ __forceinline__ float idx_quarter(const float* ys, const uint4* wv, int qk, int j,
+                                             float (*ipart)[128]) {
+  float acc = 0.f;
+#pragma unroll
+  for (int u8 = 0; u8 < 16; ++u8) {
+    const uint16_t* pv = reinterpret_cast<const uint16_t*>(&wv[u8]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc = fmaf(bf16_to_f32(pv[u]), ys[128 * qk + 8 * u8 + u], acc);
+  }
+  if (qk > 0) ipart[qk - 1][j] = acc;
+  __syncthreads();
+  return acc;
+}
+// Key dim j (thread j of the first 128) of entry `ent`: RoPE on dims 64..127 at position
+// ent * m, FP4 codes (two per byte) and the E4M3 scale of each 32-dim block.
+__device__ __forceinline__ void idx_finish(float v, int j, long long ent, int m, const RopeTurns& rt,
+                                           uint8_t* codes, uint8_t* scales, size_t crow,
+                                           float* k_out, size_t k_row) {
+  const int lane = j & 31, w = j >> 5;
+  const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+  if (j >= 64) {
+    float c, s;
+    rope_cs(ent * m, (j - 64) >> 1, rt, c, s);
+    v = (j & 1) ? (partner * s + v * c) : (v * c - partner * s);
+  }
+  if (k_out) k_out[k_row * 128 + j] = v;
+  uint32_t sb;
+  const uint32_t code = fp4_quant_lane(v, sb);
+  const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+  if ((lane & 1) == 0) codes[crow * 64 + (j >> 1)] = uint8_t(code | (hi << 4));
+  if (lane == 0) scales[crow * 4 + w] = uint8_t(sb);
+}
+
 // One block of 512 threads per entry: thread t < 128 of split group sg = tid / 128 sums
 // channels 4t..4t+3 of splits [sg * n / 4, (sg + 1) * n / 4) of the n_split partial products
 // (split-K), all its loads in flight together; group 0 then adds the four group sums in group
@@ -219,16 +255,36 @@ int proj_splits(int M, int K, int Nout) {
 // chunk ends inside a group) the last token's kv and gate sums go to state: from block 0 when
 // head = 1 (which reads the old state first: one block per sequence touches it), else from an
 // extra block r = n_ent.
+// With IDX (few entries, as in decode) the block also computes the entry's indexer key from
+// the pre-RoPE entry it holds, exactly as index_k_kernel does (same products, same order):
+// the 512 threads split the 512 -> 128 projection into four quarters of the inputs, the
+// first 128 add them in quarter order, apply RoPE and quantise to FP4.
+struct IdxOut {
+  const uint16_t* w_ik;   // [128][512] bf16
+  uint8_t* codes;         // [B][n_cap][64]
+  uint8_t* scales;        // [B][n_cap][4]
+};
+template <bool IDX>
 __global__ void __launch_bounds__(512) compress_epilogue_kernel(
     const float* __restrict__ P, int n_split, size_t split_stride, int Nout, int T, int m,
     int pos0, int n_ent, int head, int tail,
     const float* __restrict__ norm_w, float eps, const RopeTurns rt, uint16_t* __restrict__ kv_cache,
-    int n_cap, float* __restrict__ kv_pre, float* __restrict__ state) {
+    int n_cap, float* __restrict__ kv_pre, float* __restrict__ state, IdxOut io) {
   pdl_wait();
   __shared__ float4 part[3][128][4];   // groups 1..3: their sums per thread
+  __shared__ float ys[IDX ? 512 : 1];           // (IDX) the entry before RoPE
+  __shared__ float ipart[IDX ? 3 : 1][128];     // (IDX) quarter sums of the key projection
   const int per = n_ent + (tail && !head ? 1 : 0);
   const int b = blockIdx.x / per, r = blockIdx.x % per, t = threadIdx.x & 127, sg = threadIdx.x >> 7;
   const bool from_state = head && r == 0, to_state = r == n_ent, stash_too = from_state && tail;
+  // (IDX) this thread's 128 key-projection weights: row t, inputs 128 sg .. 128 sg + 127, in
+  // flight while the entry is computed
+  uint4 wv[IDX ? 16 : 1];
+  if (IDX && !to_state) {
+    const uint4* wr = reinterpret_cast<const uint4*>(io.w_ik + size_t(t) * 512 + 128 * sg);
+#pragma unroll
+    for (int u8 = 0; u8 < (IDX ? 16 : 1); ++u8) wv[u8] = wr[u8];
+  }
   // first token of this block's group (row of P); for from_state, the group's second token
   const size_t row0 = to_state ? size_t(b) * T + T - 1
                                : size_t(b) * T + (from_state ? 0 : head + size_t(r - head) * m);
@@ -275,6 +331,11 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
     for (int v = 0; v < 4; ++v) part[sg - 1][t][v] = acc[v];
   }
   __syncthreads();
+  if (IDX && !to_state && sg > 0) {   // groups 1..3: the key projection once the entry is in ys
+    __syncthreads();
+    idx_quarter(ys, wv, sg, t, ipart);
+    return;
+  }
   if (sg > 0) return;   // the rest runs in group 0 (4 warps)
 #pragma unroll
   for (int q = 0; q < 3; ++q)
@@ -334,6 +395,7 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
     float4 v = make_float4(y[0], y[1], y[2], y[3]);
     *reinterpret_cast<float4*>(kv_pre + (size_t(b) * n_ent + r) * 512 + 4 * t) = v;
   }
+  if (IDX) *reinterpret_cast<float4*>(&ys[4 * t]) = make_float4(y[0], y[1], y[2], y[3]);
   if (4 * t >= 448) {
     const long long pos = (long long)(pos0 / m + r) * m;   // the group's first token
 #pragma unroll
@@ -353,6 +415,12 @@ __global__ void __launch_bounds__(512) compress_epilogue_kernel(
   st.y = *reinterpret_cast<uint32_t*>(&hi);
   const size_t crow = size_t(b) * n_cap + size_t(pos0 / m) + r;
   *reinterpret_cast<uint2*>(kv_cache + crow * 512 + 4 * t) = st;
+  if (IDX) {
+    __syncthreads();   // ys complete (groups 1..3 wait here too)
+    float acc_k = idx_quarter(ys, wv, 0, t, ipart);
+    acc_k = ((acc_k + ipart[0][t]) + ipart[1][t]) + ipart[2][t];
+    idx_finish(acc_k, t, (long long)(pos0 / m + r), m, rt, io.codes, io.scales, crow, nullptr, 0);
+  }
 }
 
 constexpr int IK_E = 8;  // entries per block (few entries, as in decode: 2)
@@ -371,7 +439,7 @@ __global__ void __launch_bounds__(512) index_k_kernel(const float* __restrict__ 
   pdl_wait();
   __shared__ float kv[E][512];
   __shared__ float part[3][E][128];
-  const int tid = threadIdx.x, j = tid & 127, qk = tid >> 7, lane = tid & 31, w = (tid >> 5) & 3;
+  const int tid = threadIdx.x, j = tid & 127, qk = tid >> 7;
   const int total = B * G;
   const int e0 = blockIdx.x * E;
   for (int idx = tid * 4; idx < E * 512; idx += 512 * 4) {
@@ -412,20 +480,7 @@ __global__ void __launch_bounds__(512) index_k_kernel(const float* __restrict__ 
     if (ei >= total) break;  // uniform across the block
     const int b = ei / G, g = ei % G;
     const long long ent = (long long)entry0 + g;
-    float v = acc[e];
-    const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-    if (j >= 64) {
-      float c, s;
-      rope_cs(ent * m, (j - 64) >> 1, rt, c, s);
-      v = (j & 1) ? (partner * s + v * c) : (v * c - partner * s);
-    }
-    if (k_out) k_out[size_t(ei) * 128 + j] = v;
-    uint32_t sb;
-    const uint32_t code = fp4_quant_lane(v, sb);
-    const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
-    const size_t crow = size_t(b) * n_cap + size_t(ent);
-    if ((lane & 1) == 0) codes[crow * 64 + (j >> 1)] = uint8_t(code | (hi << 4));
-    if (lane == 0) scales[crow * 4 + w] = uint8_t(sb);
+    idx_finish(acc[e], j, ent, m, rt, codes, scales, size_t(b) * n_cap + size_t(ent), k_out, size_t(ei));
   }
 }
 
@@ -516,10 +571,16 @@ namespace {
 
 // Shared body of the compressor entry points: tokens pos0 .. pos0+T-1 of B sequences, any
 // pos0 when `state` is given (m = 2), else pos0 % m == 0 and a trailing partial group ignored.
+// With idx (the runner's Full layers), a call of at most IDX_FUSE_ENTRIES entries also writes
+// their indexer keys from the epilogue (*fused = true); otherwise the caller runs the
+// indexer-key kernel on kv_pre.
+constexpr long long IDX_FUSE_ENTRIES = 4096;
 int compress_impl(const char* who, const void* x, int B, int T, int hidden, int m, int pos0,
                   const void* w_kv, const void* w_gate, const float* norm_w, float eps,
                   float rope_base, float* state, void* kv_cache, int n_cap, float* kv_pre,
-                  void* workspace, size_t ws_bytes, void* stream) {
+                  void* workspace, size_t ws_bytes, void* stream, const IdxOut* idx = nullptr,
+                  bool* fused = nullptr) {
+  if (fused) *fused = false;
   if (m != 1 && m != 2) return fail(CSA2_ERR_UNSUPPORTED, "%s: m must be 1 or 2 (got %d)", who, m);
   if (!x || !w_kv || !norm_w || !kv_cache)
     return fail(CSA2_ERR_INVALID_ARG, "%s: null tensor pointer", who);
@@ -545,6 +606,8 @@ int compress_impl(const char* who, const void* x, int B, int T, int hidden, int 
   const size_t need = csa2_compress_workspace_size(B, T, hidden, m);
   if (!workspace || ws_bytes < need || !aligned256(workspace))
     return fail(CSA2_ERR_WORKSPACE, "%s: workspace needs %zu bytes, 256-aligned", who, need);
+  if (idx && (!idx->w_ik || !idx->codes || !idx->scales || !aligned16(idx->w_ik)))
+    return fail(CSA2_ERR_INVALID_ARG, "%s: indexer-key weights and caches needed, 16-byte aligned", who);
   if (n_ent + tail == 0) return CSA2_OK;   // (n_ent == 0 implies head == 0)
   cudaStream_t st = (cudaStream_t)stream;
   const int M = B * T, nout = (m == 1) ? 512 : 1024;
@@ -562,14 +625,34 @@ int compress_impl(const char* who, const void* x, int B, int T, int hidden, int 
     CSA2_LAUNCH("proj_gemm launch", proj_gemm_kernel, grid, GT, 0, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, P);
   }
   note_launch();
-  CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel, B * (n_ent + (tail && !head ? 1 : 0)), 512, 0, st, P, splits, size_t(M) * nout, nout, T, m, pos0, n_ent, head, tail, norm_w, eps, rope_turns(rope_base), (uint16_t*)kv_cache, n_cap, kv_pre, state);
+  const bool use_idx = idx && (long long)B * n_ent <= IDX_FUSE_ENTRIES;
+  const unsigned n_blocks = unsigned(B * (n_ent + (tail && !head ? 1 : 0)));
+  if (use_idx) {
+    CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel<true>, n_blocks, 512, 0, st, P, splits, size_t(M) * nout, nout, T, m, pos0, n_ent, head, tail, norm_w, eps, rope_turns(rope_base), (uint16_t*)kv_cache, n_cap, kv_pre, state, *idx);
+  } else {
+    CSA2_LAUNCH("compress_epilogue launch", compress_epilogue_kernel<false>, n_blocks, 512, 0, st, P, splits, size_t(M) * nout, nout, T, m, pos0, n_ent, head, tail, norm_w, eps, rope_turns(rope_base), (uint16_t*)kv_cache, n_cap, kv_pre, state, IdxOut{nullptr, nullptr, nullptr});
+  }
   note_launch();
+  if (fused) *fused = use_idx;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return CSA2_OK;
 }
 
 }  // namespace
+
+int csa2::compress_index_k(const void* x, int B, int T, int hidden, int m, int pos0, const void* w_kv,
+                           const void* w_gate, const float* norm_w, float eps, float rope_base,
+                           float* state, void* kv_cache, int n_cap, float* kv_pre, void* workspace,
+                           size_t ws_bytes, const void* w_ik, uint8_t* idx_codes, uint8_t* idx_scales,
+                           void* stream, bool* fused) {
+  if (fused) *fused = false;
+  if (m == 1 && state) return fail(CSA2_ERR_INVALID_ARG, "compress_chunk: state must be NULL when m == 1");
+  const IdxOut io{static_cast<const uint16_t*>(w_ik), idx_codes, idx_scales};
+  return compress_impl(state ? "compress_chunk" : "compress", x, B, T, hidden, m, pos0, w_kv, w_gate,
+                       norm_w, eps, rope_base, state, kv_cache, n_cap, kv_pre, workspace, ws_bytes,
+                       stream, &io, fused);
+}
 
 extern "C" {
 

@@ -189,15 +189,14 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
         // step may start or end inside a group; without it, only whole groups count)
         const int e0 = L.x_pos0 / m;
         const int g_new = L.compress_state ? (L.x_pos0 + L.x_tokens) / m - e0 : L.x_tokens / m;
-        st = L.compress_state
-                 ? csa2_compress_chunk(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv,
-                                       L.w_gate, L.norm_w, p->eps, p->rope_base, L.compress_state,
-                                       L.kv_cache, L.n_cap, reinterpret_cast<float*>(ws + w.kv_pre),
-                                       ws + w.gemm, gemm_bytes, stream)
-                 : csa2_compress(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv, L.w_gate,
-                                 L.norm_w, p->eps, p->rope_base, L.kv_cache, L.n_cap,
-                                 reinterpret_cast<float*>(ws + w.kv_pre), ws + w.gemm, gemm_bytes,
-                                 stream);
+        // decode-sized calls write the indexer keys from the compressor's epilogue
+        if (!L.w_ik || !L.idx_codes || !L.idx_scales)
+          return fail(CSA2_ERR_INVALID_ARG, "layer %d: Full layer needs w_ik and the indexer-key caches", l);
+        bool idx_done = false;
+        st = compress_index_k(L.x, p->B, L.x_tokens, p->hidden, m, L.x_pos0, L.w_kv, L.w_gate,
+                              L.norm_w, p->eps, p->rope_base, L.compress_state, L.kv_cache, L.n_cap,
+                              reinterpret_cast<float*>(ws + w.kv_pre), ws + w.gemm, gemm_bytes,
+                              L.w_ik, L.idx_codes, L.idx_scales, stream, &idx_done);
         if (st != CSA2_OK) return st;
         if (L.kv_codes || L.kv_scales) {   // the new entries in the stored FP4 format too
           if (!L.kv_codes || !L.kv_scales)
@@ -208,9 +207,11 @@ int csa2_runner_step(csa2_runner* r, const csa2_step_params* p, const csa2_layer
         }
         mark(r, l, 0, 1, stream);
         mark(r, l, 1, 0, stream);
-        st = csa2_index_k_quant(reinterpret_cast<float*>(ws + w.kv_pre), p->B, g_new, e0, m, L.w_ik,
-                                p->rope_base, L.idx_codes, L.idx_scales, L.n_cap, nullptr, stream);
-        if (st != CSA2_OK) return st;
+        if (!idx_done) {
+          st = csa2_index_k_quant(reinterpret_cast<float*>(ws + w.kv_pre), p->B, g_new, e0, m, L.w_ik,
+                                  p->rope_base, L.idx_codes, L.idx_scales, L.n_cap, nullptr, stream);
+          if (st != CSA2_OK) return st;
+        }
         mark(r, l, 1, 1, stream);
       }
       n_entries[l] = (L.x_pos0 + L.x_tokens) / m;

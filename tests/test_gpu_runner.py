@@ -224,3 +224,68 @@ def test_runner_streaming_compressor_one_token_per_step():
             assert torch.equal(g[0]["kv_cache"][:, e_new], before)
         o1 = [dict(o[0], x=x2_64[:, : step + 1], x_pos0=P), o[1]]
         compare(kv_src, idx_src, ratio, g, o1, B, Tq, t, k, 64, 64, topks, cands)
+
+
+@pytest.mark.parametrize("m,B,x_tokens,pos0,use_state", [
+    (2, 8, 2, 1022, False),     # encoder decode step: one new entry per sequence
+    (1, 8, 1, 511, False),      # decoder decode step
+    (2, 4, 4, 1021, True),      # group state: completes an open group, leaves one open
+    (2, 3, 2732, 0, False),     # 4098 entries: above the fused limit, separate indexer-key kernel
+])
+def test_runner_index_keys_equal_the_separate_stage_calls(m, B, x_tokens, pos0, use_state):
+    # The runner writes decode-sized calls' indexer keys from the compressor's epilogue; the
+    # entries and keys it leaves in the caches equal, bit for bit, csa2_compress(_chunk)
+    # followed by csa2_index_k_quant on the same inputs.
+    from compressed_sparse_attention_04_gb300 import ops
+    hidden, H, k = 512, 64, 16
+    s = 870 + m + x_tokens
+    x, _ = Hp.bf16_input(s, 1, (B, x_tokens, hidden))
+    wkv, _ = Hp.bf16_input(s, 2, (512, hidden), 0.02)
+    wg = Hp.bf16_input(s, 3, (512, hidden), 0.02)[0] if m == 2 else None
+    wik, _ = Hp.bf16_input(s, 4, (128, 512), 0.02)
+    gam = torch.ones(512, dtype=torch.float32, device="cuda")
+    n_cap = (pos0 + x_tokens) // m + 2
+    st0 = None
+    if use_state:   # the open group's first token, as a previous call would leave it
+        st0 = Hp.f32_input(s, 9, (B, 1024))[0]
+    caches = []
+    for _ in range(2):
+        caches.append(dict(kv=torch.zeros(B, n_cap, 512, dtype=torch.bfloat16, device="cuda"),
+                           codes=torch.zeros(B, n_cap, 64, dtype=torch.uint8, device="cuda"),
+                           scales=torch.zeros(B, n_cap, 4, dtype=torch.uint8, device="cuda"),
+                           state=st0.clone() if use_state else None))
+    # separate stage calls
+    a = caches[0]
+    e0 = pos0 // m
+    if use_state:
+        pre = ops.compress_chunk(x, wkv, wg, gam, m, pos0, a["kv"], state=a["state"])
+    else:
+        pre = ops.compress(x, wkv, wg, gam, m, pos0, a["kv"])
+    ops.index_k_quant(pre, e0, m, wik, a["codes"], a["scales"])
+    # the runner (one Full layer; its attention output is not compared here)
+    b_ = caches[1]
+    Tq = 1
+    q = Hp.bf16_input(s, 5, (B, Tq, H, 512), 1.28)[0]
+    t_last = pos0 + x_tokens - 1
+    swa = Hp.bf16_input(s, 8, (B, 128, 512))[0]
+    runner = ops.Runner([0], [0], [m], 64, 64)
+    p = runner.params(B, Tq, t_last, H, hidden, k)
+    g = dict(q=q, swa_kv=swa, swa_len=128, swa_pos0=t_last - 127, out=torch.empty_like(q),
+             q_idx=Hp.bf16_input(s, 6, (B, Tq, 32, 128), 1.28)[0],
+             w_idx=Hp.f32_input(s, 7, (B, Tq, 32), 1.28)[0],
+             x=x, w_kv=wkv, w_gate=wg, norm_w=gam, w_ik=wik, kv_cache=b_["kv"],
+             idx_codes=b_["codes"], idx_scales=b_["scales"], n_cap=n_cap, x_tokens=x_tokens,
+             x_pos0=pos0, compress_state=b_["state"])
+    ws = torch.empty(runner.workspace_size(p, x_tokens, n_cap) + 256, dtype=torch.uint8, device="cuda")
+    runner.step(p, [ops.layer_io(**g)], ws)
+    torch.cuda.synchronize()
+    assert ops.last_device_status() == 0
+    n_new = (pos0 + x_tokens) // m - e0
+    sl = slice(e0, e0 + n_new)
+    assert n_new >= 1
+    for key in ("kv", "codes", "scales"):
+        np.testing.assert_array_equal(b_[key][:, sl].contiguous().view(torch.uint8).cpu().numpy(),
+                                      a[key][:, sl].contiguous().view(torch.uint8).cpu().numpy(),
+                                      err_msg=key)
+    if use_state:
+        np.testing.assert_array_equal(b_["state"].cpu().numpy(), a["state"].cpu().numpy())
