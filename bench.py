@@ -467,6 +467,29 @@ def fp4_peak_tflops():
     return tf.value if rc == 0 else None
 
 
+def run_gather_rate(args):
+    """DRAM read rate of row gathers through 16-byte cp.async on this GPU (the library's
+    gather probe: one CTA per SM, row indices staged in shared memory, 512 MB per launch after
+    an L2-evicting write), random and contiguous rows of 256 B .. 4 KB.  One JSON line."""
+    import ctypes as C
+    from compressed_sparse_attention_04_gb300 import build
+    build.build_all()
+    lib = C.CDLL(os.path.join(os.path.dirname(build.__file__), "peak", "libcsa2_peak.so"))
+    f = lib.csa2peak_gather
+    f.argtypes = [C.c_int, C.c_int, C.POINTER(C.c_double), C.POINTER(C.c_double)]
+    res = {}
+    for rb in (256, 512, 1024, 2048, 4096):
+        for rnd in (1, 0):
+            g, ms = C.c_double(), C.c_double()
+            rc = f(rb, rnd, C.byref(g), C.byref(ms))
+            if rc != 0:
+                raise RuntimeError(f"gather probe failed: CUDA error {rc}")
+            res[f"{rb}B_{'random' if rnd else 'contiguous'}"] = round(g.value, 1)
+    print(json.dumps({"metric": "row-gather DRAM read rate (cp.async, one CTA per SM, 192 KB in flight)",
+                      "unit": "GB/s", "rates": res}), flush=True)
+    return 0
+
+
 def time_oracle_prefill(wl, n_sample=32, seed=78):
     """The float64 oracle on the same prefill, timed on a bounded sample: the Full layer's
     compressor and index keys over every token, then the indexer + top-k + attention of
@@ -1052,6 +1075,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--indexer-prefill", action="store_true",
                     help="time the indexer of the 16384-token prefill alone (one JSON line, not the bench line)")
+    ap.add_argument("--gather-rate", action="store_true",
+                    help="measure the row-gather DRAM read rate of this GPU (one JSON line)")
     ap.add_argument("--attention-formats", action="store_true",
                     help="time the decode attention launch with each stored format (one JSON line)")
     ap.add_argument("--graph", action="store_true",
@@ -1065,6 +1090,8 @@ def main():
         return run_indexer_prefill(args)
     if args.attention_formats:
         return run_attention_formats(args)
+    if args.gather_rate:
+        return run_gather_rate(args)
     if args.workload in PREFILL:
         if int(os.environ.get("RANK", "0")) != 0:
             return 0   # one GPU: a prefill pass is not split over ranks

@@ -8,7 +8,8 @@
 // [P3] "DeepSeek-V4.1-Flash：把百万 Token 的记忆，压缩成一套分级缓存" (junki.cn), §四:
 //      p_j = softmax_j(c_j . q / sqrt d), o = sum_j p_j c_j.
 //
-// attn_decode_kernel (64 heads): a cluster of 1-4 CTAs per query row shares the row's
+// attn_decode_kernel (H a multiple of 8 up to 64; query rows past H are zero in its 64-row
+// query tile): a cluster of 1-4 CTAs per query row shares the row's
 // attended list (each CTA an equal part of the window rows and of the top-k slots).  The
 // queries and the bf16 window rows arrive by TMA tile loads; the selected entries are
 // gathered by 16-byte asynchronous copies into a two-slot ring of 64-row chunks (K-major,
@@ -377,7 +378,9 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t dst_cluster, const void* s
 // O^T tiles (4 of 128 dims) owned by CTA r of n: dt = r, r + n, ...
 __device__ __forceinline__ int tiles_owned(int r, int n) { return (4 - r + n - 1) / n; }
 
-template <bool QNT>   // QNT: FP4 entries and / or FP8 window rows
+// QNT: FP4 entries and / or FP8 window rows.  H64: exactly 64 heads (the head count is then a
+// compile-time constant and nothing is masked); otherwise a.H, a multiple of 8 below 64.
+template <bool QNT, bool H64>
 __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
                                                               const __grid_constant__ CUtensorMap q_map,
                                                               const __grid_constant__ CUtensorMap swa_map) {
@@ -403,6 +406,7 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
   __shared__ __align__(16) float ml_all[AD_MAX_SPLIT][64][4];
 
   const AttnArgs& a = u.a;
+  const int NH = H64 ? 64 : a.H;   // heads
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = int(cluster.block_rank());
   const int ns = u.n_split;
@@ -435,6 +439,12 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
     umma::mbar_fence_init();
   }
   if (warp == 0) umma::tmem_alloc(&tmem_slot, 512);
+  if (!H64) {   // query rows H..63 of every plane are zero (the TMA fills rows 0..H-1)
+    const int zb = (64 - NH) * 128 / 16;   // 16-byte units per plane
+    for (int u = tid; u < 8 * zb; u += AD_T)
+      *reinterpret_cast<uint4*>(Qs + (u / zb) * AD_PLANE + NH * 128 + (u % zb) * 16) = make_uint4(0, 0, 0, 0);
+    umma::fence_proxy_async();
+  }
   umma::fence_before();
   __syncthreads();
   umma::fence_after();
@@ -691,9 +701,9 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
   } else if (warp == 8 && lane == 0) {
     // ---------------- TMA and MMA issuer.  First the queries and the window chunks the
     // TMA loads (their row masks are written here, before their slot is announced).
-    mbar_expect_tx(&q_full, AD_Q_BYTES);
+    mbar_expect_tx(&q_full, uint32_t(NH) * 1024u);   // H heads x 512 dims x 2 bytes
 #pragma unroll 1
-    for (int j = 0; j < 8; ++j) tma_load_2d(Qs + j * AD_PLANE, &q_map, 64 * j, row * 64, &q_full);
+    for (int j = 0; j < 8; ++j) tma_load_2d(Qs + j * AD_PLANE, &q_map, 64 * j, row * NH, &q_full);
 #pragma unroll 1
     for (int c = 0; c < n_tma; ++c) {
       const int valid = min(AD_CH, nw - AD_CH * c);
@@ -779,7 +789,7 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
   cluster.sync();
   if (tid < 64) {
     const int h = tid;
-    const float sk = a.sink ? a.sink[h] * 1.4426950408889634f : -INFINITY;
+    const float sk = a.sink && h < NH ? a.sink[h] * 1.4426950408889634f : -INFINITY;
     float M = sk;
     for (int r = 0; r < ns; ++r) M = fmaxf(M, ml_all[r][h][0]);
     float L = a.sink ? exp2f(sk - M) : 0.f, Le = L;
@@ -790,7 +800,7 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
         Le += ml_all[r][h][2] * g;
       }
     fac[h] = ml_all[rank][h][1] > 0.f ? exp2f(ml_all[rank][h][0] - M) / L : 0.f;
-    if (rank == 0 && a.lse) a.lse[size_t(row) * 64 + h] = (M + log2f(Le)) * 0.6931471805599453f;
+    if (rank == 0 && a.lse && h < NH) a.lse[size_t(row) * NH + h] = (M + log2f(Le)) * 0.6931471805599453f;
   }
   __syncthreads();
   // softmax warps: lane = dim 32 q + lane of each 128-dim tile; the factors go to registers
@@ -843,7 +853,7 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
     const bool okr = ns == 1 || umma::mbar_wait(&recv_bar, 0, &d_err_attn);
     for (int lt = 0; rank + lt * ns < 4 && okr; ++lt) {
       const int dt = rank + lt * ns;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + size_t(row) * 64 * 512 +
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + size_t(row) * NH * 512 +
                             dt * 128 + 32 * q + lane;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -867,8 +877,14 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
 #pragma unroll
           for (int x = 0; x < 32; ++x) acc[x] += w[x];
         }
+        if (H64) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) orow[(32 * hf + x) * 512] = __float2bfloat16_rn(acc[x]);
+          for (int x = 0; x < 32; ++x) orow[(32 * hf + x) * 512] = __float2bfloat16_rn(acc[x]);
+        } else {   // heads past H are not written
+#pragma unroll
+          for (int x = 0; x < 32; ++x)
+            if (32 * hf + x < NH) orow[(32 * hf + x) * 512] = __float2bfloat16_rn(acc[x]);
+        }
       }
     }
   }
@@ -913,8 +929,11 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
   if (k < 0 || k > CSA2_MAX_TOPK) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k=%d out of [0, 2048]", k);
   if (k > 0 && (!topk || (fp4 ? (!kv_codes || !kv_scales) : !kv_cache)))
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: k > 0 needs topk and the cache entries");
-  if ((fp4 || fp8w) && H != 64)
-    return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: quantised entries or rows need H = 64 (got %d)", H);
+  // the tensor-core kernel takes up to 64 heads in multiples of 8 (its query tile has 64 rows,
+  // loaded by TMA 8-row atoms; rows past H are zero); other head counts take the SIMT kernel
+  const bool tc = H <= 64 && H % 8 == 0;
+  if ((fp4 || fp8w) && !tc)
+    return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: quantised entries or rows need H a multiple of 8 up to 64 (got %d)", H);
   if ((kv_codes && !aligned16(kv_codes)) || (kv_scales && !aligned16(kv_scales)) ||
       (swa_codes && !aligned16(swa_codes)) || (swa_scales && !aligned16(swa_scales)))
     return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: pointers must be 16-byte aligned");
@@ -944,7 +963,7 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
               n_cap, n_entries, topk, k, (const uint16_t*)swa_kv, S, swa_pos0, window, sink,
               scale, (uint16_t*)out, lse_out, kv_codes, kv_scales, swa_codes, swa_scales};
   cudaStream_t st = (cudaStream_t)stream;
-  if (H == 64) {
+  if (tc) {
     // tensor-core path: a cluster of n_split CTAs per row, partial results merged through
     // distributed shared memory; queries (and bf16 window rows) through tensor maps
     (void)workspace; (void)ws_bytes;
@@ -957,22 +976,27 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     if (dev < 0 || dev >= 64) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: device id");
     int sms = sms_cache[dev].load(std::memory_order_acquire);
     if (sms == 0) {
-      e0 = cudaFuncSetAttribute(attn_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
+      e0 = cudaFuncSetAttribute(attn_decode_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
       if (e0 == cudaSuccess)
-        e0 = cudaFuncSetAttribute(attn_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
+        e0 = cudaFuncSetAttribute(attn_decode_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(attn_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(attn_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
       if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
       sms_cache[dev].store(sms, std::memory_order_release);
     }
-    if (rows * 64 > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many query rows");
+    if (rows * H > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many query rows");
     EncodeTiledFn enc = tensor_map_encoder();
     if (!enc) return fail(CSA2_ERR_CUDA, "sparse_attn: cuTensorMapEncodeTiled not available");
-    // queries: [rows * 64 heads][512 dims] bf16, one box = 64 heads x 64 dims (one plane)
+    // queries: [rows * H heads][512 dims] bf16, one box = H heads x 64 dims (one plane's
+    // first H rows)
     CUtensorMap q_map, swa_map;
     {
-      const cuuint64_t dims[2] = {512, cuuint64_t(rows * 64)};
+      const cuuint64_t dims[2] = {512, cuuint64_t(rows * H)};
       const cuuint64_t strides[1] = {1024};
-      const cuuint32_t box[2] = {64, 64};
+      const cuuint32_t box[2] = {64, cuuint32_t(H)};
       const cuuint32_t estr[2] = {1, 1};
       if (enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1006,11 +1030,14 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     }
     if (rows * n_split > (1ll << 31) - 1) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: too many rows");
     AttnDecodeArgs da{aa, n_split, win_tma};
-    e0 = (fp4 || fp8w)
-             ? launch_k(attn_decode_kernel<true>, dim3(unsigned(rows * n_split), 1, 1), dim3(AD_T, 1, 1),
-                        AD_SMEM, st, unsigned(n_split), da, q_map, swa_map)
-             : launch_k(attn_decode_kernel<false>, dim3(unsigned(rows * n_split), 1, 1), dim3(AD_T, 1, 1),
-                        AD_SMEM, st, unsigned(n_split), da, q_map, swa_map);
+    const dim3 grid(unsigned(rows * n_split), 1, 1), block(AD_T, 1, 1);
+    const bool q8 = fp4 || fp8w;
+    if (H == 64)
+      e0 = q8 ? launch_k(attn_decode_kernel<true, true>, grid, block, AD_SMEM, st, unsigned(n_split), da, q_map, swa_map)
+              : launch_k(attn_decode_kernel<false, true>, grid, block, AD_SMEM, st, unsigned(n_split), da, q_map, swa_map);
+    else
+      e0 = q8 ? launch_k(attn_decode_kernel<true, false>, grid, block, AD_SMEM, st, unsigned(n_split), da, q_map, swa_map)
+              : launch_k(attn_decode_kernel<false, false>, grid, block, AD_SMEM, st, unsigned(n_split), da, q_map, swa_map);
     if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: launch");
     note_launch();
   } else {

@@ -290,7 +290,7 @@ int csa2_sparse_attn_fp4kv(const void* q, int B, int Tq, int H, int q_pos0,
  * u8 [B, n_cap, 32], kv_cache = NULL); the window rows as bf16 (swa_kv, swa_codes =
  * swa_scales = NULL) or FP8 (swa_codes u8 [B, S, 512] + swa_scales u8 [B, S, 8] from
  * csa2_swa_kv_quant_fp8, swa_kv = NULL).  Quantised rows are dequantised exactly into the
- * bf16 tile the attention reads.  Any quantised operand needs H == 64
+ * bf16 tile the attention reads.  Any quantised operand needs H a multiple of 8 up to 64
  * (CSA2_ERR_UNSUPPORTED otherwise); giving both forms, or neither, of an operand is
  * CSA2_ERR_INVALID_ARG.  Other arguments and errors as csa2_sparse_attn. */
 int csa2_sparse_attn_ex(const void* q, int B, int Tq, int H, int q_pos0, const void* kv_cache,
@@ -343,7 +343,8 @@ typedef struct {
    * also writes the layer's new entries there, and every layer reading this KV attends over
    * the FP4 entries (kv_cache still receives the bf16 entries).  Every layer: swa_codes /
    * swa_scales (u8 [B, swa_len, 512] / [B, swa_len, 8], FP8 as csa2_swa_kv_quant_fp8) in
-   * place of swa_kv (which is then NULL).  Quantised operands need H == 64. */
+   * place of swa_kv (which is then NULL).  Quantised operands need H a multiple of 8 up
+   * to 64. */
   uint8_t* kv_codes;
   uint8_t* kv_scales;
   const uint8_t* swa_codes;

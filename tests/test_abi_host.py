@@ -176,7 +176,8 @@ def test_sparse_attn_ex_validation(lib):
     assert call(a13=_vp(0), a14=_vp(0)) == L.ERR_INVALID_ARG       # ... and not at all
     assert call(a14=_vp(0)) == L.ERR_INVALID_ARG                   # codes without scales
     assert call(a5=_vp(FAKE)) == L.ERR_INVALID_ARG                 # entries given twice
-    assert call(a3=32) == L.ERR_UNSUPPORTED                        # quantised rows need 64 heads
+    assert call(a3=12) == L.ERR_UNSUPPORTED                        # quantised rows: H a multiple of 8
+    assert call(a3=72) == L.ERR_UNSUPPORTED                        # ... up to 64
     assert call(a14=_vp(FAKE + 8)) == L.ERR_INVALID_ARG            # misaligned scales
     assert call(a16=74) == L.ERR_INVALID_ARG                       # window row 73 missing
 

@@ -465,6 +465,10 @@ def _topk_input(seed, B, Tq, k, n_entries, holes=True):
     (1, 40, 64, 0, 20, 128, 40, 0, True),
     (2, 3, 64, 500, 700, 300, 200, 370, False),
     (2, 1, 64, 300, 0, 0, 128, 173, True),
+    # fewer heads on the tensor-core path (query rows past H are zero in its 64-row tile):
+    # 16 heads at the decode batch (two CTAs per row) with a sink, 32 heads over a prefill chunk
+    (64, 1, 16, 131071, 3000, 512, 128, 131071 - 127, True),
+    (3, 5, 32, 900, 800, 200, 256, 700, False),
     # enough rows for one CTA per row, and the decode batch (two CTAs per row)
     (80, 1, 64, 4095, 2000, 256, 128, 4095 - 127, False),
     (64, 1, 64, 131071, 3000, 512, 128, 131071 - 127, True),
@@ -673,12 +677,40 @@ def test_sparse_attn_ex_rejects_ambiguous_operands():
                                  p(None), p(None), p(None), 8, 0, 8, p(None), 0.05, p(out), p(None),
                                  p(None), 0, ops._stream(q.device))
     assert st == L.ERR_INVALID_ARG
-    # quantised rows need 64 heads
-    q32 = torch.zeros(1, 1, 32, 512, dtype=torch.bfloat16, device="cuda")
-    st = lib.csa2_sparse_attn_ex(p(q32), 1, 1, 32, 7, p(None), p(None), p(None), 0, 0, p(None), 0,
-                                 p(None), p(wc), p(ws), 8, 0, 8, p(None), 0.05, p(q32), p(None),
+    # quantised rows need the tensor-core kernel: H a multiple of 8 up to 64
+    q12 = torch.zeros(1, 1, 12, 512, dtype=torch.bfloat16, device="cuda")
+    st = lib.csa2_sparse_attn_ex(p(q12), 1, 1, 12, 7, p(None), p(None), p(None), 0, 0, p(None), 0,
+                                 p(None), p(wc), p(ws), 8, 0, 8, p(None), 0.05, p(q12), p(None),
                                  p(None), 0, ops._stream(q.device))
     assert st == L.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("H", [16, 32])
+def test_sparse_attn_fewer_heads_quantised_rows_equal_their_bf16_values(H):
+    # With fewer than 64 heads the stored formats run on the same tensor-core kernel: FP8
+    # window rows and FP4 entries dequantise exactly into the bf16 tile, so the output equals,
+    # bit for bit, the bf16 path over the dequantised values (computed by the oracle's
+    # decoders on the host).
+    ops = _ops()
+    B, Tq, q_pos0, n_entries, k, S = 64, 1, 131071, 1500, 512, 128
+    swa_pos0 = q_pos0 - 127
+    seed = 260 + H
+    q, _ = Hp.bf16_input(seed, 1, (B, Tq, H, 512), 1.28)
+    kv_b, kv64 = Hp.bf16_input(seed, 2, (B, n_entries, 512))
+    swa_b, swa64 = Hp.bf16_input(seed, 3, (B, S, 512))
+    kc, ks = R.main_kv_fp4(kv64)
+    wc, wsc = R.swa_kv_fp8(swa64)
+    kv_deq, _ = _bf16_dev(R.main_kv_dequant(kc, ks))
+    swa_deq, _ = _bf16_dev(R.swa_kv_dequant(wc, wsc))
+    topk = Hp.to_dev(_topk_input(seed, B, Tq, k, n_entries), torch.int32)
+    quant = ops.sparse_attn(q, q_pos0, None, n_entries, topk, None, swa_pos0, window=128,
+                            kv_fp4=(Hp.to_dev(kc, torch.uint8), Hp.to_dev(ks, torch.uint8)),
+                            swa_fp8=(Hp.to_dev(wc, torch.uint8), Hp.to_dev(wsc, torch.uint8)))
+    plain = ops.sparse_attn(q, q_pos0, kv_deq, n_entries, topk, swa_deq, swa_pos0, window=128)
+    torch.cuda.synchronize()
+    _ok()
+    np.testing.assert_array_equal(quant.view(torch.int16).cpu().numpy(),
+                                  plain.view(torch.int16).cpu().numpy())
 
 
 @pytest.mark.parametrize("B,Tq,q_pos0,n_entries,k,S,swa_pos0", [
