@@ -324,37 +324,49 @@ __global__ void __launch_bounds__(128) q_prep_kernel(ScoreArgs a, QPrepOut qo, i
   pdl_wait();
   __shared__ int scan[32];
   const int tid = threadIdx.x, lane = tid & 31, blk = lane >> 3, l8 = lane & 7;
-  for (long long item = (long long)blockIdx.x * 4 + (tid >> 5); item < n_items;
-       item += (long long)gridDim.x * 4) {
-    const long long row = item >> 5;
-    const int h = int(item & 31);
-    const uint2 raw = *reinterpret_cast<const uint2*>(a.q_idx + size_t(row) * 32 * 128 + h * 128 + 4 * lane);
-    const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
-                        __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
-    float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    const uint32_t sb = e4m3_rne_satfinite(__fdiv_rn(amax, 6.0f));
-    // this lane's four codes: elements 4 l8 .. 4 l8 + 3 of the block = nibbles 4 (l8 & 1) ..
-    // 4 (l8 & 1) + 3 of the block's word l8 / 2 (element 8 j + i in nibble i of word j)
-    uint32_t part = 0u;
-    if (sb != 0u) {
-      const float sc = e4m3_value(sb);
+  // four items per warp and round, their loads issued together
+  const long long stride = (long long)gridDim.x * 4;
+  for (long long item0 = (long long)blockIdx.x * 4 + (tid >> 5); item0 < n_items; item0 += 4 * stride) {
+    uint2 raws[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float u = __fdiv_rn(v[e], sc);
-        part |= (((__float_as_uint(u) >> 31) << 3) | e2m1_rne_mag(fabsf(u))) << (4 * e);
-      }
+    for (int r4 = 0; r4 < 4; ++r4) {
+      const long long it = min(item0 + r4 * stride, n_items - 1);
+      raws[r4] = *reinterpret_cast<const uint2*>(a.q_idx + size_t(it >> 5) * 32 * 128 + int(it & 31) * 128 + 4 * lane);
     }
-    const uint32_t word = (part << (16 * (l8 & 1))) | (__shfl_xor_sync(0xffffffffu, part, 1) << (16 * ((l8 & 1) ^ 1)));
-    const uint32_t w1 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 2);
-    const uint32_t w2 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 4);
-    const uint32_t w3 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 6);
-    if (l8 == 0) {
-      *reinterpret_cast<uint4*>(qo.img + size_t(row) * qo.img_stride + fp4_chunk_off(h, blk)) =
-          make_uint4(word, w1, w2, w3);
-      qo.sc[size_t(row) * qo.sc_stride + h * 4 + blk] = uint8_t(sb);
+#pragma unroll
+    for (int r4 = 0; r4 < 4; ++r4) {
+      const long long item = item0 + r4 * stride;
+      if (item >= n_items) break;   // uniform across the warp
+      const long long row = item >> 5;
+      const int h = int(item & 31);
+      const uint2 raw = raws[r4];
+      const float v[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      const uint32_t sb = e4m3_rne_satfinite(__fdiv_rn(amax, 6.0f));
+      // this lane's four codes: elements 4 l8 .. 4 l8 + 3 of the block = nibbles 4 (l8 & 1) ..
+      // 4 (l8 & 1) + 3 of the block's word l8 / 2 (element 8 j + i in nibble i of word j)
+      uint32_t part = 0u;
+      if (sb != 0u) {
+        const float sc = e4m3_value(sb);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float u = __fdiv_rn(v[e], sc);
+          part |= (((__float_as_uint(u) >> 31) << 3) | e2m1_rne_mag(fabsf(u))) << (4 * e);
+        }
+      }
+      const uint32_t word = (part << (16 * (l8 & 1))) | (__shfl_xor_sync(0xffffffffu, part, 1) << (16 * ((l8 & 1) ^ 1)));
+      const uint32_t w1 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 2);
+      const uint32_t w2 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 4);
+      const uint32_t w3 = __shfl_sync(0xffffffffu, word, (lane & ~7) + 6);
+      if (l8 == 0) {
+        *reinterpret_cast<uint4*>(qo.img + size_t(row) * qo.img_stride + fp4_chunk_off(h, blk)) =
+            make_uint4(word, w1, w2, w3);
+        qo.sc[size_t(row) * qo.sc_stride + h * 4 + blk] = uint8_t(sb);
+      }
     }
   }
   if (blockIdx.x == 0 && qo.groups) {
