@@ -440,9 +440,9 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
   }
   if (warp == 0) umma::tmem_alloc(&tmem_slot, 512);
   if (!H64) {   // query rows H..63 of every plane are zero (the TMA fills rows 0..H-1)
-    const int zb = (64 - NH) * 128 / 16;   // 16-byte units per plane
+    const int zb = (64 - a.H) * 128 / 16;   // 16-byte units per plane (a.H < 64 here)
     for (int u = tid; u < 8 * zb; u += AD_T)
-      *reinterpret_cast<uint4*>(Qs + (u / zb) * AD_PLANE + NH * 128 + (u % zb) * 16) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(Qs + (u / zb) * AD_PLANE + a.H * 128 + (u % zb) * 16) = make_uint4(0, 0, 0, 0);
     umma::fence_proxy_async();
   }
   umma::fence_before();
@@ -894,6 +894,377 @@ __global__ void __launch_bounds__(AD_T, 1) attn_decode_kernel(AttnDecodeArgs u,
   if (warp == 0) umma::tmem_free(tmem, 512);
 }
 
+// ---------------------------------------------------------------- persistent attention rows
+// For calls with one CTA per query row (many rows: prefill, large batches) and bf16 rows: one
+// CTA per SM walks rows blockIdx.x, blockIdx.x + gridDim.x, ... with the chunk pipeline of
+// attn_decode_kernel, its chunk counter running on across rows, so that the next row's gathers,
+// queries and score products proceed while the softmax warps write the current row's output.
+// Window rows are gathered by the copy warps like the selected entries.  The queries of row
+// j + 1 are loaded once the score products of row j have read its queries (q_free); the next
+// row's first P V overwrites O^T only after the softmax warps have read it out (its
+// probabilities are written after that row's output).
+struct RowShape {
+  int b, nw, n_wch, n_ch;
+  long long t, lo;
+};
+__device__ __forceinline__ RowShape row_shape(const AttnArgs& a, int row) {
+  RowShape r;
+  r.b = row / a.Tq;
+  r.t = (long long)a.q_pos0 + row % a.Tq;
+  r.lo = r.t - a.window + 1 > 0 ? r.t - a.window + 1 : 0;
+  r.nw = int(r.t - r.lo + 1);
+  r.n_wch = (r.nw + AD_CH - 1) / AD_CH;
+  r.n_ch = r.n_wch + (a.k + AD_CH - 1) / AD_CH;
+  return r;
+}
+
+template <bool H64>
+__global__ void __launch_bounds__(AD_T, 1) attn_rows_kernel(AttnArgs a, const __grid_constant__ CUtensorMap q_map) {
+  pdl_wait();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* KV = base;                                   // 2 slots x 64 rows
+  uint8_t* Qs = base + AD_SLOTS * AD_SLOT_BYTES;        // the row's queries
+  uint8_t* Ps = Qs + AD_Q_BYTES;                        // 2 x P
+  __shared__ int sidx[CSA2_MAX_TOPK];
+  __shared__ const uint16_t* row_src[AD_SLOTS][AD_CH];
+  __shared__ unsigned long long row_mask[AD_SLOTS];
+  __shared__ __align__(8) uint64_t kv_full[AD_SLOTS], kv_empty[AD_SLOTS];
+  __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full[2], o_ready, q_full, q_free;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float fac[64];
+  const int NH = H64 ? 64 : a.H;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float scale_log2 = a.scale * 1.4426950408889634f;
+  const int n_rows = a.rows > int(blockIdx.x) ? (a.rows - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x) : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < AD_SLOTS; ++s) {
+      umma::mbar_init(&kv_full[s], 1);
+      umma::mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      umma::mbar_init(&s_full[s], 1);
+      umma::mbar_init(&s_empty[s], 4);
+      umma::mbar_init(&p_full[s], 4);
+    }
+    umma::mbar_init(&o_ready, 1);
+    umma::mbar_init(&q_full, 1);
+    umma::mbar_init(&q_free, 1);
+    umma::mbar_fence_init();
+  }
+  if (warp == 0) umma::tmem_alloc(&tmem_slot, 512);
+  if (!H64) {   // query rows H..63 of every plane are zero (the TMA fills rows 0..H-1)
+    const int zb = (64 - a.H) * 128 / 16;   // (a.H < 64 here)
+    for (int u = tid; u < 8 * zb; u += AD_T)
+      *reinterpret_cast<uint4*>(Qs + (u / zb) * AD_PLANE + a.H * 128 + (u % zb) * 16) = make_uint4(0, 0, 0, 0);
+    umma::fence_proxy_async();
+  }
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool ok = true;
+
+  if (warp < 4) {
+    // ---------------- copy warps: group g fills the chunks of slot g, global chunk g, g + 2, ...
+    const int grp = warp >> 1, gt = tid & 63, gw = warp & 1;
+    uint8_t* dst = KV + grp * AD_SLOT_BYTES;
+    long long g_base = 0;   // global index of the row's first chunk
+    for (int jr = 0; jr < n_rows; ++jr) {
+      const int row = int(blockIdx.x) + jr * int(gridDim.x);
+      const RowShape rs = row_shape(a, row);
+      // both groups are past the previous row's chunks (and agree on going on)
+      if (!bar_and(BAR_COPY, 128, ok)) { ok = false; break; }
+      for (int j = tid; j < a.k; j += 128) sidx[j] = a.topk[size_t(row) * a.k + j];
+      named_bar(BAR_COPY, 128);
+      for (int c = int((grp ^ int(g_base & 1)) & 1); c < rs.n_ch && ok; c += AD_SLOTS) {
+        const long long g = g_base + c;
+        const int s = grp;
+        const bool win = c < rs.n_wch;
+        const int j = win ? c * AD_CH + gt : (c - rs.n_wch) * AD_CH + gt;
+        int okr = 0;
+        const uint16_t* src = nullptr;
+        if (win) {
+          if (j < rs.nw) {
+            okr = 1;
+            src = a.swa + (size_t(rs.b) * a.S + size_t(rs.lo + j - a.swa_pos0)) * 512;
+          }
+        } else if (j < a.k) {
+          const int e = sidx[j];
+          if (e >= a.n_entries) atomicOr(&d_err_attn, ERR_BOUNDS);
+          if (e >= 0 && e < a.n_entries) {
+            okr = 1;
+            src = a.kv + (size_t(rs.b) * a.n_cap + e) * 512;
+          }
+        }
+        const bool okw = g < AD_SLOTS || umma::mbar_wait(&kv_empty[s], ((g >> 1) - 1) & 1, &d_err_attn);
+        {
+          const unsigned m0 = __ballot_sync(0xffffffffu, okr);
+          if (okw) {
+            row_src[s][gt] = src;
+            if (lane == 0) reinterpret_cast<unsigned*>(&row_mask[s])[gw] = m0;
+          }
+        }
+        if (!bar_and(BAR_GROUP + grp, 64, okw)) { ok = false; break; }
+#pragma unroll 1
+        for (int r0 = 0; r0 < AD_CH; r0 += 8) {
+          const uint16_t* sp[8];
+#pragma unroll
+          for (int u2 = 0; u2 < 8; ++u2) sp[u2] = row_src[s][r0 + u2];
+#pragma unroll
+          for (int u2 = 0; u2 < 8; ++u2)
+            umma::cp_async16(dst + plane_off(r0 + u2, gt * 8), sp[u2] ? sp[u2] + gt * 8 : a.q,
+                             sp[u2] ? 16u : 0u);
+        }
+        umma::cp_async_commit();
+        umma::cp_async_wait_all();
+        umma::fence_proxy_async();
+        named_bar(BAR_GROUP + grp, 64);
+        if (gt == 0) umma::mbar_arrive(&kv_full[s]);
+      }
+      g_base += rs.n_ch;
+    }
+  } else if (warp < 8) {
+    // ---------------- softmax warps (as attn_decode_kernel), then each row's output
+    const int q = warp & 3, h = 16 * q + (lane & 15);
+    const bool head_lane = lane < 16;
+    const int half = lane >> 4;
+    const uint32_t lane_addr = uint32_t(32 * q) << 16;
+    long long g_base = 0;
+    for (int jr = 0; jr < n_rows && ok; ++jr) {
+      const int row = int(blockIdx.x) + jr * int(gridDim.x);
+      const RowShape rs = row_shape(a, row);
+      float m_used = -INFINITY, l = 0.f, le = 0.f;
+      for (int c = 0; c < rs.n_ch && ok; ++c) {
+        const long long g = g_base + c;
+        const int s = int(g & 1);
+        const bool okc = __all_sync(0xffffffffu, umma::mbar_wait(&s_full[s], (g >> 1) & 1, &d_err_attn));
+        if (!bar_and(BAR_SOFTMAX, 128, okc)) { ok = false; break; }
+        umma::fence_after();
+        float sv[AD_HALF];
+        {
+          uint32_t v0[32], v1[32];
+          umma::tmem_ld32(tmem + lane_addr + AD_S_COL + 64 * s, v0);
+          umma::tmem_ld32(tmem + lane_addr + AD_S_COL + 64 * s + 32, v1);
+          umma::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < AD_HALF; ++j) {
+            const float moved = __shfl_sync(0xffffffffu, __uint_as_float(v1[j]), lane & 15);
+            sv[j] = half ? moved : __uint_as_float(v0[j]);
+          }
+        }
+        umma::fence_before();
+        __syncwarp();
+        if (lane == 0) umma::mbar_arrive(&s_empty[s]);
+        const unsigned mask = unsigned(row_mask[s] >> (half * AD_HALF));
+        float cmx[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) cmx[x] = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < AD_HALF; ++j) {
+          sv[j] = ((mask >> j) & 1u) ? sv[j] * scale_log2 : -INFINITY;
+          cmx[j & 7] = fmaxf(cmx[j & 7], sv[j]);
+        }
+        float cm = fmaxf(fmaxf(fmaxf(cmx[0], cmx[1]), fmaxf(cmx[2], cmx[3])),
+                         fmaxf(fmaxf(cmx[4], cmx[5]), fmaxf(cmx[6], cmx[7])));
+        cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 16));
+        float f = 1.f;
+        if (cm > m_used + AD_LAZY || (m_used == -INFINITY && cm != -INFINITY)) {
+          f = m_used == -INFINITY ? 0.f : exp2f(m_used - cm);
+          m_used = cm;
+          l *= f;
+          le *= f;
+        }
+        float psx[4], pex[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) psx[x] = pex[x] = 0.f;
+        uint32_t pk[AD_HALF / 2];
+        const float msub = m_used == -INFINITY ? INFINITY : m_used;
+#pragma unroll
+        for (int j = 0; j < AD_HALF; j += 2) {
+          const float p0 = fast_exp2(sv[j] - msub), p1 = fast_exp2(sv[j + 1] - msub);
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(p0, p1);
+          pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&v2);
+          const float2 r2 = __bfloat1622float2(v2);
+          psx[(j >> 1) & 3] += r2.x + r2.y;
+          pex[(j >> 1) & 3] += p0 + p1;
+        }
+        l += (psx[0] + psx[1]) + (psx[2] + psx[3]);
+        le += (pex[0] + pex[1]) + (pex[2] + pex[3]);
+        const bool okp = g < 2 || umma::mbar_wait(&kv_empty[s], ((g - 2) >> 1) & 1, &d_err_attn);
+        if (!bar_and(BAR_SOFTMAX, 128, okp)) { ok = false; break; }
+        uint8_t* pb = Ps + s * AD_P_BYTES + (h >> 3) * AD_P_SBO + (h & 7) * 16;
+#pragma unroll
+        for (int c4 = 0; c4 < AD_HALF / 8; ++c4) {
+          const int kc = half * (AD_HALF / 8) + c4;
+          *reinterpret_cast<uint4*>(pb + kc * 128) =
+              make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+        }
+        const bool need = head_lane && f != 1.f && c > 0;
+        if (head_lane) fac[h] = need ? f : 1.f;
+        if (bar_or(BAR_SOFTMAX, 128, need)) {
+          const bool okr = __all_sync(0xffffffffu,
+                                      umma::mbar_wait(&kv_empty[(g - 1) & 1], ((g - 1) >> 1) & 1, &d_err_attn));
+          if (!bar_and(BAR_SOFTMAX, 128, okr)) { ok = false; break; }
+          umma::fence_after();
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            float fr[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x) fr[x] = fac[32 * hf + x];
+#pragma unroll 1
+            for (int dt = 0; dt < 4; ++dt) {
+              uint32_t o[32];
+              const uint32_t addr = tmem + lane_addr + AD_O_COL + 64 * dt + 32 * hf;
+              umma::tmem_ld32(addr, o);
+              umma::tmem_ld_wait();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * fr[x]);
+              umma::tmem_st32(addr, o);
+            }
+          }
+          umma::tmem_st_wait();
+        }
+        umma::fence_proxy_async();
+        umma::fence_before();
+        __syncwarp();
+        if (lane == 0) umma::mbar_arrive(&p_full[s]);
+      }
+      if (!ok) break;
+      // ---------------- the row's output: O^T (TMEM) / L per head, bf16
+      const float l_fin = l + __shfl_xor_sync(0xffffffffu, l, 16);
+      const float e_fin = le + __shfl_xor_sync(0xffffffffu, le, 16);
+      // the row's products are complete; every warp is past its rescales (fac reused)
+      ok = bar_and(BAR_SOFTMAX, 128, umma::mbar_wait(&o_ready, jr & 1, &d_err_attn));
+      if (!ok) break;
+      umma::fence_after();
+      if (head_lane) {
+        const float sk = a.sink && h < NH ? a.sink[h] * 1.4426950408889634f : -INFINITY;
+        const float M = fmaxf(sk, m_used);
+        float L = a.sink ? exp2f(sk - M) : 0.f, Le = L;
+        if (l_fin > 0.f) {
+          const float gm = exp2f(m_used - M);
+          L += l_fin * gm;
+          Le += e_fin * gm;
+        }
+        fac[h] = l_fin > 0.f ? exp2f(m_used - M) / L : 0.f;
+        if (a.lse && h < NH) a.lse[size_t(row) * NH + h] = (M + log2f(Le)) * 0.6931471805599453f;
+      }
+      named_bar(BAR_SOFTMAX, 128);
+      float fr[64];
+#pragma unroll
+      for (int x = 0; x < 64; ++x) fr[x] = fac[x];
+      named_bar(BAR_SOFTMAX, 128);   // fac is free for the next row's rescales
+#pragma unroll 1
+      for (int dt = 0; dt < 4; ++dt) {
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.out) + size_t(row) * NH * 512 +
+                              dt * 128 + 32 * q + lane;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[32];
+          umma::tmem_ld32(tmem + lane_addr + AD_O_COL + 64 * dt + 32 * hf, v);
+          umma::tmem_ld_wait();
+          if (H64) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              orow[(32 * hf + x) * 512] = __float2bfloat16_rn(__uint_as_float(v[x]) * fr[32 * hf + x]);
+          } else {
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+              if (32 * hf + x < NH)
+                orow[(32 * hf + x) * 512] = __float2bfloat16_rn(__uint_as_float(v[x]) * fr[32 * hf + x]);
+          }
+        }
+      }
+      g_base += rs.n_ch;
+    }
+  } else if (warp == 8 && lane == 0) {
+    // ---------------- TMA (queries) and MMA issuer over all rows' chunks
+    constexpr uint32_t idesc_s = umma::idesc_f16(64, AD_CH, 1, 0, 0);
+    constexpr uint32_t idesc_o = umma::idesc_f16(128, 64, 1, 1, 0);
+    const uint32_t kv0 = umma::smem_u32(KV), q0 = umma::smem_u32(Qs), p0 = umma::smem_u32(Ps);
+    auto load_q = [&](int jr) {
+      const int row = int(blockIdx.x) + jr * int(gridDim.x);
+      mbar_expect_tx(&q_full, uint32_t(NH) * 1024u);
+#pragma unroll 1
+      for (int j = 0; j < 8; ++j) tma_load_2d(Qs + j * AD_PLANE, &q_map, 64 * j, row * NH, &q_full);
+    };
+    auto issue_s = [&](long long g) {
+      const int s = int(g & 1);
+      umma::fence_after();
+      const uint64_t da0 = umma::desc_sw128(q0, 16, 1024);
+      const uint64_t db0 = umma::desc_sw128(kv0 + s * AD_SLOT_BYTES, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < 32; ++ks) {
+        const uint32_t off = uint32_t(((ks >> 2) * AD_PLANE + (ks & 3) * 32) >> 4);
+        umma::mma_f16(tmem + AD_S_COL + 64 * s, da0 + off, db0 + off, idesc_s, ks > 0 ? 1u : 0u);
+      }
+      umma::commit(&s_full[s]);
+    };
+    auto issue_pv = [&](long long g, bool first) {
+      const int s = int(g & 1);
+      umma::fence_after();
+      const uint64_t pa0 = umma::desc_sw128(kv0 + s * AD_SLOT_BYTES, AD_PLANE, 1024);
+      const uint64_t pb0 = desc_noswz(p0 + s * AD_P_BYTES, 128, AD_P_SBO);
+#pragma unroll
+      for (int kk = 0; kk < AD_CH / 16; ++kk)
+#pragma unroll
+        for (int dt = 0; dt < 4; ++dt)
+          umma::mma_f16(tmem + AD_O_COL + 64 * dt, pa0 + uint32_t(((2 * dt) * AD_PLANE + kk * 2048) >> 4),
+                        pb0 + uint32_t((kk * 256) >> 4), idesc_o, (!first || kk > 0) ? 1u : 0u);
+      umma::commit(&kv_empty[s]);
+    };
+    if (n_rows > 0) load_q(0);
+    int js = 0, cs = 0, jp = 0, cp = 0;        // next S and next P V: row (of this CTA), chunk
+    long long gs = 0, gp = 0;                  // their global chunk indices
+    int nch_s = n_rows > 0 ? row_shape(a, int(blockIdx.x)).n_ch : 0, nch_p = nch_s;
+    int q_wait = -1;                           // row whose queries wait for the previous row's S
+    uint32_t idle = 0;
+    while (jp < n_rows) {
+      if (q_wait >= 0 && umma::mbar_test(&q_free, (q_wait - 1) & 1)) {
+        load_q(q_wait);
+        q_wait = -1;
+        idle = 0;
+      }
+      if (js < n_rows && gs <= gp + 1) {
+        const int s = int(gs & 1);
+        if (umma::mbar_test(&kv_full[s], (gs >> 1) & 1) && (cs != 0 || umma::mbar_test(&q_full, js & 1)) &&
+            (gs < 2 || umma::mbar_test(&s_empty[s], ((gs >> 1) - 1) & 1))) {
+          issue_s(gs);
+          ++gs;
+          if (++cs == nch_s) {   // the row's queries are read once these products complete
+            umma::commit(&q_free);
+            if (++js < n_rows) {
+              q_wait = js;
+              nch_s = row_shape(a, int(blockIdx.x) + js * int(gridDim.x)).n_ch;
+            }
+            cs = 0;
+          }
+          idle = 0;
+          continue;
+        }
+      }
+      if (gp < gs && umma::mbar_test(&p_full[gp & 1], (gp >> 1) & 1)) {
+        issue_pv(gp, cp == 0);
+        ++gp;
+        if (++cp == nch_p) {
+          umma::commit(&o_ready);
+          if (++jp < n_rows) nch_p = row_shape(a, int(blockIdx.x) + jp * int(gridDim.x)).n_ch;
+          cp = 0;
+        }
+        idle = 0;
+        continue;
+      }
+      if (++idle > (1u << 26)) { atomicOr(&d_err_attn, ERR_TIMEOUT); break; }
+    }
+  }
+  umma::fence_before();
+  __syncthreads();
+  umma::fence_after();
+  if (warp == 0) umma::tmem_free(tmem, 512);
+}
+
 }  // namespace
 }  // namespace csa2
 
@@ -983,6 +1354,10 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
         e0 = cudaFuncSetAttribute(attn_decode_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
       if (e0 == cudaSuccess)
         e0 = cudaFuncSetAttribute(attn_decode_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(attn_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
+      if (e0 == cudaSuccess)
+        e0 = cudaFuncSetAttribute(attn_rows_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(AD_SMEM));
       if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       if (e0 != cudaSuccess) return cuda_fail(e0, "sparse_attn: attributes");
       sms_cache[dev].store(sms, std::memory_order_release);
@@ -1032,7 +1407,12 @@ int sparse_attn_impl(const void* q, int B, int Tq, int H, int q_pos0, const void
     AttnDecodeArgs da{aa, n_split, win_tma};
     const dim3 grid(unsigned(rows * n_split), 1, 1), block(AD_T, 1, 1);
     const bool q8 = fp4 || fp8w;
-    if (H == 64)
+    if (n_split == 1 && !q8 && rows > sms) {
+      // more rows than SMs, bf16 rows: one persistent CTA per SM walks its rows
+      const dim3 pgrid(unsigned(sms), 1, 1);
+      e0 = H == 64 ? launch_k(attn_rows_kernel<true>, pgrid, block, AD_SMEM, st, 1u, aa, q_map)
+                   : launch_k(attn_rows_kernel<false>, pgrid, block, AD_SMEM, st, 1u, aa, q_map);
+    } else if (H == 64)
       e0 = q8 ? launch_k(attn_decode_kernel<true, true>, grid, block, AD_SMEM, st, unsigned(n_split), da, q_map, swa_map)
               : launch_k(attn_decode_kernel<false, true>, grid, block, AD_SMEM, st, unsigned(n_split), da, q_map, swa_map);
     else

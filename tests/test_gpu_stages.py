@@ -469,6 +469,11 @@ def _topk_input(seed, B, Tq, k, n_entries, holes=True):
     # 16 heads at the decode batch (two CTAs per row) with a sink, 32 heads over a prefill chunk
     (64, 1, 16, 131071, 3000, 512, 128, 131071 - 127, True),
     (3, 5, 32, 900, 800, 200, 256, 700, False),
+    # more rows than SMs: one persistent CTA per SM walks several rows (window rows gathered,
+    # rows of different lengths, 64 and 16 heads)
+    (1, 400, 64, 0, 300, 128, 400, 0, True),
+    (200, 1, 64, 4095, 2000, 256, 128, 4095 - 127, False),
+    (1, 300, 16, 500, 700, 64, 720, 100, False),
     # enough rows for one CTA per row, and the decode batch (two CTAs per row)
     (80, 1, 64, 4095, 2000, 256, 128, 4095 - 127, False),
     (64, 1, 64, 131071, 3000, 512, 128, 131071 - 127, True),
