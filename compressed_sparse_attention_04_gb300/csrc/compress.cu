@@ -100,15 +100,30 @@ constexpr int PU_STAGES = 4;
 constexpr uint32_t PU_STAGE_BYTES = 2 * PU_TILE * PU_KC * 2;   // 32 KB (W tile + X tile)
 constexpr uint32_t PU_SMEM = PU_STAGES * PU_STAGE_BYTES + 1024;
 
-__global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __restrict__ X,
-                                                            const uint16_t* __restrict__ W0,
-                                                            const uint16_t* __restrict__ W1, int M,
-                                                            int K, int Nout, int k_per_split,
+// Operand tiles by TMA (128-byte swizzle, the layout the MMA descriptors read): thread 0 of
+// warp 0 keeps PU_STAGES stages of (W tile, X tile) in flight on full / empty mbarriers,
+// thread 0 of warp 1 issues the MMAs; X rows past M arrive as zeros.  W rows n < 512 come
+// from w_kv, the others from w_gate (a 128-channel tile lies in one of them).
+__device__ __forceinline__ void pu_tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];"
+      :: "r"(umma::smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(umma::smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void pu_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"
+               :: "r"(umma::smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const __grid_constant__ CUtensorMap x_map,
+                                                            const __grid_constant__ CUtensorMap w0_map,
+                                                            const __grid_constant__ CUtensorMap w1_map,
+                                                            int M, int Nout, int k_per_split,
                                                             float* __restrict__ P) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t empty_bar[PU_STAGES], done_bar;
+  __shared__ __align__(8) uint64_t full_bar[PU_STAGES], empty_bar[PU_STAGES], done_bar;
   __shared__ uint32_t tmem_slot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * PU_TILE;            // channel tile
@@ -117,7 +132,10 @@ __global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __re
   const int k_begin = split * k_per_split;
   const int n_iter = k_per_split / PU_KC;
   if (tid == 0) {
-    for (int s = 0; s < PU_STAGES; ++s) umma::mbar_init(&empty_bar[s], 1);
+    for (int s = 0; s < PU_STAGES; ++s) {
+      umma::mbar_init(&full_bar[s], 1);
+      umma::mbar_init(&empty_bar[s], 1);
+    }
     umma::mbar_init(&done_bar, 1);
     umma::mbar_fence_init();
   }
@@ -126,48 +144,30 @@ __global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __re
   __syncthreads();
   umma::fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint16_t* wsrc[PU_TILE / 32];             // this thread's 4 channel rows
-  (void)wsrc;
-
-  auto load_stage = [&](int it) {
-    const int s = it % PU_STAGES;
-    uint8_t* Ws = base + s * PU_STAGE_BYTES;
-    uint8_t* Xs = Ws + PU_TILE * PU_KC * 2;
-    const int k0 = k_begin + it * PU_KC;
-    for (int c = tid; c < PU_TILE * 8; c += PU_T) {
-      const int r = c >> 3, ch = c & 7;
-      const int n = n0 + r;
-      const uint16_t* wrow = (n < 512) ? (W0 + size_t(n) * K) : (W1 + size_t(n - 512) * K);
-      umma::cp_async16(Ws + umma::kmajor_sw128_offset(r, ch * 8, PU_TILE), wrow + k0 + ch * 8, 16u);
-      const int m = m0 + r;
-      const uint16_t* xrow = X + size_t(m < M ? m : 0) * K;
-      umma::cp_async16(Xs + umma::kmajor_sw128_offset(r, ch * 8, PU_TILE), xrow + k0 + ch * 8,
-                       m < M ? 16u : 0u);
-    }
-  };
-  constexpr uint32_t idesc = umma::idesc_f16(PU_TILE, PU_TILE, 1, 0, 0);
   bool ok = true;
-  // prologue: PU_STAGES - 1 stages in flight
-  for (int it = 0; it < PU_STAGES - 1; ++it) {
-    if (it < n_iter) load_stage(it);
-    umma::cp_async_commit();
-  }
-  for (int it = 0; it < n_iter; ++it) {
-    const int nxt = it + PU_STAGES - 1;
-    if (nxt < n_iter) {
-      // the stage being refilled was last read by the MMAs of iteration nxt - PU_STAGES
-      if (nxt >= PU_STAGES)
-        ok = ok && umma::mbar_wait(&empty_bar[nxt % PU_STAGES], ((nxt / PU_STAGES) - 1) & 1, &d_err_compress);
-      load_stage(nxt);
-    }
-    umma::cp_async_commit();
-    umma::cp_async_wait_pending(PU_STAGES - 1);   // stage `it` landed for this thread
-    umma::fence_proxy_async();
-    umma::fence_before();
-    __syncthreads();
-    umma::fence_after();
-    if (tid == 0 && ok) {
+  int issued = 0;                                  // producer: stages loaded so far
+  if (warp == 0 && lane == 0) {
+    // ---------------- producer
+    const CUtensorMap* wmap = n0 < 512 ? &w0_map : &w1_map;
+    const int wy = n0 < 512 ? n0 : n0 - 512;
+    for (int it = 0; it < n_iter; ++it, ++issued) {
       const int s = it % PU_STAGES;
+      if (it >= PU_STAGES &&
+          !umma::mbar_wait(&empty_bar[s], ((it / PU_STAGES) - 1) & 1, &d_err_compress)) { ok = false; break; }
+      uint8_t* Ws = base + s * PU_STAGE_BYTES;
+      uint8_t* Xs = Ws + PU_TILE * PU_KC * 2;
+      const int k0 = k_begin + it * PU_KC;
+      pu_expect_tx(&full_bar[s], PU_STAGE_BYTES);
+      pu_tma_2d(Ws, wmap, k0, wy, &full_bar[s]);
+      pu_tma_2d(Xs, &x_map, k0, m0, &full_bar[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = umma::idesc_f16(PU_TILE, PU_TILE, 1, 0, 0);
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % PU_STAGES;
+      if (!umma::mbar_wait(&full_bar[s], (it / PU_STAGES) & 1, &d_err_compress)) { ok = false; break; }
+      umma::fence_after();
       const uint32_t wb = umma::smem_u32(base + s * PU_STAGE_BYTES);
       const uint32_t xb = wb + PU_TILE * PU_KC * 2;
 #pragma unroll
@@ -175,11 +175,17 @@ __global__ void __launch_bounds__(PU_T, 1) proj_umma_kernel(const uint16_t* __re
         umma::mma_f16(tmem, umma::desc_sw128(wb + kk * 32, 16, 1024),
                       umma::desc_sw128(xb + kk * 32, 16, 1024), idesc, (it | kk) != 0);
       umma::commit(&empty_bar[s]);
-      if (it == n_iter - 1) umma::commit(&done_bar);
     }
+    umma::commit(&done_bar);   // (all MMAs issued by this thread, also after an early stop)
   }
-  umma::cp_async_wait_all();
-  if (ok) ok = umma::mbar_wait(&done_bar, 0, &d_err_compress);
+  __syncwarp();
+  ok = umma::mbar_wait(&done_bar, 0, &d_err_compress) && ok;
+  ok = __syncthreads_and(ok);
+  if (!ok && warp == 0 && lane == 0) {
+    // a wait gave up: let the copies still in flight land before the CTA leaves
+    for (int it = issued - 1; it >= 0 && it >= issued - PU_STAGES; --it)
+      umma::mbar_wait(&full_bar[it % PU_STAGES], (it / PU_STAGES) & 1, &d_err_compress);
+  }
   umma::fence_after();
   if (ok) {
     // D^T: lane = channel n0 + 32*warp + lane, column = row m0 + c
@@ -618,8 +624,24 @@ int compress_impl(const char* who, const void* x, int B, int T, int hidden, int 
     cudaError_t e0 = cudaFuncSetAttribute(proj_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           int(PU_SMEM));
     if (e0 != cudaSuccess) return cuda_fail(e0, "compress: shared memory attribute");
+    // operand tensor maps: [rows][hidden] bf16, boxes of 64 elements (128 bytes) x 128 rows
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return fail(CSA2_ERR_CUDA, "%s: cuTensorMapEncodeTiled not available", who);
+    auto make_map = [&](CUtensorMap* map, const void* ptr, long long rows_) -> bool {
+      const cuuint64_t dims[2] = {cuuint64_t(hidden), cuuint64_t(rows_)};
+      const cuuint64_t strides[1] = {cuuint64_t(hidden) * 2};
+      const cuuint32_t box[2] = {cuuint32_t(PU_KC), cuuint32_t(PU_TILE)};
+      const cuuint32_t estr[2] = {1, 1};
+      return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    CUtensorMap x_map, w0_map, w1_map;
+    if (!make_map(&x_map, x, M) || !make_map(&w0_map, w_kv, 512) ||
+        !make_map(&w1_map, w_gate ? w_gate : w_kv, 512))
+      return fail(CSA2_ERR_CUDA, "%s: operand tensor maps", who);
     dim3 grid(nout / PU_TILE, ceil_div(M, PU_TILE), splits);
-    CSA2_LAUNCH("proj_umma launch", proj_umma_kernel, grid, PU_T, PU_SMEM, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, hidden / splits, P);
+    CSA2_LAUNCH("proj_umma launch", proj_umma_kernel, grid, PU_T, PU_SMEM, st, x_map, w0_map, w1_map, M, nout, hidden / splits, P);
   } else {
     dim3 grid(nout / GN, ceil_div(M, GM));
     CSA2_LAUNCH("proj_gemm launch", proj_gemm_kernel, grid, GT, 0, st, (const uint16_t*)x, (const uint16_t*)w_kv, (const uint16_t*)w_gate, M, hidden, nout, P);
