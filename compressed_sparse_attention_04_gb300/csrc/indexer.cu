@@ -294,7 +294,7 @@ constexpr int PF_QG = 4;                        // queries per group (N = 128)
 constexpr int PF_TILE = 128;                    // keys per step (M)
 constexpr int PF_STAGES = 8;                    // key ring
 constexpr int PF_ND = 3;                        // TMEM accumulators (steps)
-constexpr int PF_T = 448;                       // copy, MMA, 4 scale-factor and 8 epilogue warps
+constexpr int PF_T = 704;                       // copy, MMA, 4 scale-factor and 16 epilogue warps
 constexpr uint32_t PF_A_BYTES = PF_TILE * 64;   // 8 KB of codes per step
 constexpr uint32_t PF_Q_IMG = PF_QG * SU_Q_BYTES;            // 8 KB of query codes per group
 constexpr uint32_t PF_Q_SC = PF_QG * 128;                    // their scale words
@@ -790,7 +790,7 @@ __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, con
     }
     for (int d = 0; d < PF_ND; ++d) {
       umma::mbar_init(&d_full[d], 1);
-      umma::mbar_init(&d_empty[d], 8);
+      umma::mbar_init(&d_empty[d], 16);
     }
     umma::mbar_init(&q_empty[0], 1);
     umma::mbar_init(&q_empty[1], 1);
@@ -892,49 +892,38 @@ __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, con
     }
   } else {
     // ---------------- epilogue: lane quadrant warp % 4 (keys 32 q .. 32 q + 31 of the step),
-    // queries 2 hq and 2 hq + 1 of the group
-    const int q = warp & 3, hq = (warp - 6) >> 2;
+    // query qq of the group (one query per warp keeps a warp's registers to one query's
+    // weights and one 32-column slice, so that sixteen warps hide each other's waits)
+    const int q = warp & 3, qq = (warp - 6) >> 2;
     const uint32_t lane_addr = uint32_t(q * 32) << 16;
     GroupCursor ce;
     ce.init(a, G, s_begin);
-    float w0[32], w1[32];
+    float w0[32];
     for (int g = 0; g < L; ++g) {
       const bool new_grp = g == 0 || (g > 0 && ce.next(a, G));
-      const int i0 = ce.g * PF_QG + 2 * hq;              // this warp's first query index
+      const int i0 = ce.g * PF_QG + qq;                  // this warp's query index
       const size_t row0 = size_t(ce.b) * a.Tq + i0;
-      const bool ok0 = i0 < a.Tq, ok1 = i0 + 1 < a.Tq;
+      const bool ok0 = i0 < a.Tq;
       if (new_grp) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          w0[h] = ok0 ? a.w[row0 * 32 + h] : 0.f;
-          w1[h] = ok1 ? a.w[(row0 + 1) * 32 + h] : 0.f;
-        }
+        for (int h = 0; h < 32; ++h) w0[h] = ok0 ? a.w[row0 * 32 + h] : 0.f;
       }
       const int d = g % PF_ND;
       if (!umma::mbar_wait(&d_full[d], (g / PF_ND) & 1, &d_err_indexer)) break;
       umma::fence_after();
-      // one query's 32 head sums at a time (registers: both queries' weights + one slice)
       const int key = ce.st * PF_TILE + 32 * q + lane;
-      float sc0, sc1;
+      float sc0;
       {
         uint32_t v[32];
-        umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * (2 * hq)), v);
+        umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * qq), v);
         umma::tmem_ld_wait();
         sc0 = relu_dot32(v, w0);
-      }
-      {
-        uint32_t v[32];
-        umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * (2 * hq + 1)), v);
-        umma::tmem_ld_wait();
-        sc1 = relu_dot32(v, w1);
       }
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&d_empty[d]);      // accumulators copied out
       if (ok0 && key < n_visible((long long)a.q_pos0 + i0, a.m, a.n_entries))
         a.scores[row0 * a.row_len + key] = sc0;
-      if (ok1 && key < n_visible((long long)a.q_pos0 + i0 + 1, a.m, a.n_entries))
-        a.scores[(row0 + 1) * a.row_len + key] = sc1;
     }
   }
   umma::fence_before();
