@@ -747,20 +747,23 @@ struct GroupCursor {
 };
 
 __device__ __forceinline__ float relu_dot32(const uint32_t (&v)[32], const float (&w)[32]) {
-  // sum_h w_h max(s_h, 0) with packed pair FMAs (even heads in .x, odd in .y)
-  uint64_t acc;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(acc) : "f"(0.f));
+  // sum_h w_h max(s_h, 0) with packed pair FMAs into two accumulators (head pairs 4j, 4j + 1
+  // and 4j + 2, 4j + 3), so that the chain of dependent FMAs is half as long
+  uint64_t acc[2];
+  asm("mov.b64 %0, {%1, %1};" : "=l"(acc[0]) : "f"(0.f));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(acc[1]) : "f"(0.f));
 #pragma unroll
   for (int h = 0; h < 32; h += 2) {
     uint64_t ww, rr;
     asm("mov.b64 %0, {%1, %2};" : "=l"(ww) : "f"(w[h]), "f"(w[h + 1]));
     asm("mov.b64 %0, {%1, %2};" : "=l"(rr) : "f"(fmaxf(__uint_as_float(v[h]), 0.f)),
                                              "f"(fmaxf(__uint_as_float(v[h + 1]), 0.f)));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(ww), "l"(rr));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc[(h >> 1) & 1]) : "l"(ww), "l"(rr));
   }
-  float x, y;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(acc));
-  return x + y;
+  float x0, y0, x1, y1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(y0) : "l"(acc[0]));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x1), "=f"(y1) : "l"(acc[1]));
+  return (x0 + y0) + (x1 + y1);
 }
 
 __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, const uint8_t* qimg,
