@@ -902,6 +902,7 @@ __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, con
     GroupCursor ce;
     ce.init(a, G, s_begin);
     float w0[32];
+    int nv0 = 0;   // entries this warp's query sees (0 past the last query)
     for (int g = 0; g < L; ++g) {
       const bool new_grp = g == 0 || (g > 0 && ce.next(a, G));
       const int i0 = ce.g * PF_QG + qq;                  // this warp's query index
@@ -910,6 +911,7 @@ __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, con
       if (new_grp) {
 #pragma unroll
         for (int h = 0; h < 32; ++h) w0[h] = ok0 ? a.w[row0 * 32 + h] : 0.f;
+        nv0 = ok0 ? n_visible((long long)a.q_pos0 + i0, a.m, a.n_entries) : 0;
       }
       const int d = g % PF_ND;
       if (!umma::mbar_wait(&d_full[d], (g / PF_ND) & 1, &d_err_indexer)) break;
@@ -925,8 +927,7 @@ __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, con
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&d_empty[d]);      // accumulators copied out
-      if (ok0 && key < n_visible((long long)a.q_pos0 + i0, a.m, a.n_entries))
-        a.scores[row0 * a.row_len + key] = sc0;
+      if (key < nv0) a.scores[row0 * a.row_len + key] = sc0;
     }
   }
   umma::fence_before();
