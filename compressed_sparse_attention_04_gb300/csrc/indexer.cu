@@ -917,16 +917,13 @@ __global__ void __launch_bounds__(PF_T, 1) score_prefill_kernel(ScoreArgs a, con
       if (!umma::mbar_wait(&d_full[d], (g / PF_ND) & 1, &d_err_indexer)) break;
       umma::fence_after();
       const int key = ce.st * PF_TILE + 32 * q + lane;
-      float sc0;
-      {
-        uint32_t v[32];
-        umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * qq), v);
-        umma::tmem_ld_wait();
-        sc0 = relu_dot32(v, w0);
-      }
+      uint32_t v[32];
+      umma::tmem_ld32(tmem + lane_addr + uint32_t(128 * d + 32 * qq), v);
+      umma::tmem_ld_wait();
       umma::fence_before();
       __syncwarp();
       if (lane == 0) umma::mbar_arrive(&d_empty[d]);      // accumulators copied out
+      const float sc0 = relu_dot32(v, w0);
       if (key < nv0) a.scores[row0 * a.row_len + key] = sc0;
     }
   }
