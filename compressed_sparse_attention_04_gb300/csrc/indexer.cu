@@ -544,14 +544,15 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
     StepCursor ce;
     ce.init(a, s_begin);
     float wv[32];
+    int n_vis = 0;   // entries the current row sees (computed once per row)
     for (int g = 0; g < L; ++g) {
       const bool new_row = g == 0 || ce.next(a);
       const int row = ce.row(a);
       if (new_row) {
 #pragma unroll
         for (int h = 0; h < 32; ++h) wv[h] = a.w[size_t(row) * 32 + h];
+        n_vis = n_visible((long long)a.q_pos0 + ce.i, a.m, a.n_entries);
       }
-      const int n_vis = n_visible((long long)a.q_pos0 + ce.i, a.m, a.n_entries);
       const int limit = pool ? a.row_len : n_vis;
       const int d = g % SU_ND;
       if (!umma::mbar_wait(&d_full[d], (g / SU_ND) & 1, &d_err_indexer, polls)) break;
