@@ -644,6 +644,7 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
     const long long total_keys = (long long)a.rows / a.Tq * a.n_cap;   // B * n_cap
     StepCursor cc;
     cc.init(a, s_begin);
+    int n_vis = 0;   // entries the current row sees (computed once per row)
     // (stall) a wait that runs out: nothing is copied, so every other role's first wait
     // runs out too and each role leaves its loop with no copy or MMA in flight
     const bool go = !a.stall || umma::mbar_wait(&never, 0, &d_err_indexer, polls);
@@ -656,12 +657,13 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
       if (new_row && cc.k >= 2 &&
           !umma::mbar_wait(&q_empty[qb], ((cc.k >> 1) - 1) & 1, &d_err_indexer, polls)) break;
       const int row = cc.row(a);
+      if (new_row) n_vis = n_visible((long long)a.q_pos0 + cc.i, a.m, a.n_entries);
       long long blk_key[4] = {-1, -1, -1, -1};   // pool steps: the four blocks' first keys
       long long dense_key = -1;                   // dense steps: the step's first key
       uint32_t bytes = new_row ? SU_QROW_BYTES : 0u;
       if (a.use_tma) {
         const int p0 = cc.st * SU_STEP;                // first slot of the step (64-aligned)
-        const int limit = pool ? a.row_len : n_visible((long long)a.q_pos0 + cc.i, a.m, a.n_entries);
+        const int limit = pool ? a.row_len : n_vis;
         const long long cache_row0 = (long long)cc.b * a.n_cap;
         if (!pool) {
           // four consecutive blocks in two 8 KB boxes (blocks past the end of the cache
@@ -715,8 +717,8 @@ __global__ void __launch_bounds__(SU_T, 2) score_fp4_kernel(ScoreArgs a, const _
 // over persistent CTAs (one per SM).  A step's keys (128 keys x 64 code bytes: one TMA box
 // of two 64-key blocks, plus 512 scale bytes) are the MMA's A operand (M = 128); the group's
 // four query images (32 heads each, consecutive in the workspace) are B (N = 128); two
-// K = 64 block-scaled FP4 MMAs per step into one of three TMEM accumulators.  Eight epilogue
-// warps (two per TMEM lane quadrant, two queries each) apply ReLU and the head weights
+// K = 64 block-scaled FP4 MMAs per step into one of three TMEM accumulators.  Sixteen
+// epilogue warps (four per TMEM lane quadrant, one query each) apply ReLU and the head weights
 // (packed float pairs) and store the scores of the keys each query sees.
 struct GroupCursor {
   int b, g, st, n;   // sequence, group, step within the group, steps in the group
