@@ -457,3 +457,67 @@ def test_sparse_attention_fp4kv_fp8_window_full_size_sampled_rows():
         rows_ = np.concatenate([_host_main_kv_rows(seed, 2, b, n_cap, tk[b, 0]),
                                 R.attention_rows(np.zeros((0, 512)), [], swa_b, swa_pos0, q_pos0, W)])
         Hp.check_attention(g[b, 0], R.sparse_attention(q64, rows_, R.ATTN_SCALE, None), f"sequence {b}")
+
+
+# ---------------------------------------------------------------- runner, full decoder group
+def test_runner_decoder_group_full_size_sampled_sequences():
+    # The decoder group of the benchmark (Full m = 1 building the HSI pool, Reindex, two Reuse
+    # layers) through csa2_runner_step at its stated size: batch 32, token 65535 completing
+    # entry 65535 of a 65536-entry cache (prefix entries and index keys from the generator).
+    # The oracle's run_step replays sequences 0 and 31 alone (sequences are independent) from
+    # the same generator rows, and every layer's top-k, the pool and the outputs are compared.
+    from synth import gpu as sg
+    from oracle import layers as Lr
+    from test_gpu_runner import run_gpu
+    B, t, n_cap, hidden, H, k, W, seed = 32, 65535, 65536, 4096, 64, 512, 128, 9900
+    kv_src, idx_src, ratio = [0, 0, 0, 0], [0, 1, 1, 1], [1, 0, 0, 0]
+    n0, S, swa_pos0 = t, W, t - W + 1
+    kv = sg.fill_normal(torch.empty(B, n_cap, 512, dtype=torch.bfloat16, device="cuda"), seed, 20)
+    codes, scales = _device_index_cache(seed, 21, B, n_cap)
+    gpu, orc = [], []
+    for l in range(4):
+        s = seed + 10 * l
+        q, q64 = Hp.bf16_input(s, 5, (B, 1, H, 512), 1.28)
+        swa, swa64 = Hp.bf16_input(s, 8, (B, S, 512))
+        g = dict(q=q, swa_kv=swa, swa_len=S, swa_pos0=swa_pos0, out=torch.empty_like(q))
+        o = dict(q=q64, swa=swa64, swa_pos0=swa_pos0)
+        if l in (0, 1):
+            qi, qi64 = Hp.bf16_input(s, 6, (B, 1, 32, 128), 1.28)
+            wi, wi64 = Hp.f32_input(s, 7, (B, 1, 32), 1.28)
+            g.update(q_idx=qi, w_idx=wi, topk_out=None)
+            o.update(q_idx=qi64, w_idx=wi64)
+        if l == 0:
+            x, x64 = Hp.bf16_input(s, 1, (B, 1, hidden))
+            wkv, wkv64 = Hp.bf16_input(s, 2, (512, hidden), 0.02)
+            wik, wik64 = Hp.bf16_input(s, 4, (128, 512), 0.02)
+            gam = torch.ones(512, dtype=torch.float32, device="cuda")
+            g.update(x=x, w_kv=wkv, w_gate=None, norm_w=gam, w_ik=wik, kv_cache=kv, idx_codes=codes,
+                     idx_scales=scales, n_cap=n_cap, x_tokens=1, x_pos0=n0)
+            o.update(x=x64, x_pos0=n0, w_kv=wkv64, w_gate=None, gamma=np.ones(512), w_ik=wik64)
+        gpu.append(g)
+        orc.append(o)
+    runner, topks, cands = run_gpu(kv_src, idx_src, ratio, gpu, B, 1, t, H, hidden, k, 64, 64)
+    _ok()
+    got_top = {l: topks[l].cpu().numpy() for l in topks}
+    got_cand = cands[0].cpu().numpy()
+    got_out = [Hp.bf16_of(g["out"]) for g in gpu]
+    del kv, codes, scales
+    for b in (0, 31):
+        ob = []
+        for l, o in enumerate(orc):
+            d = {key: (v[b:b + 1] if isinstance(v, np.ndarray) and v.ndim >= 3 else v)
+                 for key, v in o.items()}
+            if l == 0:
+                prev = synth.normal_bf16_bits(seed, 20, b * n_cap * 512, n0 * 512, 1.0)
+                d["prev_kv"] = R.bf16_to_f64(prev).reshape(1, n0, 512)
+                pc, ps = _host_index_rows(seed, 21, b, n_cap, n0)
+                d["prev_codes"], d["prev_scales"] = pc[None], ps[None]
+            ob.append(d)
+        outs, trace = Lr.run_step(kv_src, idx_src, ratio, ob, 1, 1, t, k, hsi_blk=64, hsi_nb=64)
+        for l in (0, 1):
+            for (_, i), sc in trace[l]["scores"].items():
+                Hp.check_topk_row(got_top[l][b, i], sc, trace[l]["valid"][0, i], k,
+                                  f"layer {l} sequence {b}")
+        np.testing.assert_array_equal(got_cand[b], trace[0]["candidates"][0])
+        for l in range(4):
+            Hp.check_attention(got_out[l][b:b + 1], outs[l], f"layer {l} sequence {b}")
