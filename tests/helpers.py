@@ -98,9 +98,11 @@ def _e2m1_margin(u):
     return np.min(np.abs(np.abs(u)[..., None] - mids), axis=-1)
 
 
-def check_codes(gpu_codes, gpu_scales, k_oracle, tol=1e-4):
+def check_codes(gpu_codes, gpu_scales, k_oracle, tol=2e-5):
     """FP4 codes of keys computed in float64 by the oracle vs the GPU's codes.
 
+    The GPU forms the key in float32 (a 4096-long projection, then 512 -> 128), so its value
+    carries a relative error of a few 1e-6; tol = 2e-5 admits that and no more.
     Blocks must match bit for bit unless the oracle value lies within `tol`
     (relative) of a scale midpoint, or (elementwise) within tol * 6 of an E2M1
     midpoint in units of the scale, or within tol * scale of zero (sign).
